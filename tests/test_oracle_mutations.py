@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that at least one pin fails for each: the pins are strong enough to notice a
+dropped term, a wrong sign or index, or a transposed operand."""
+import os
+import sys
+import types
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(__file__))
+from oracle_pins import ALL_PINS  # noqa: E402
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "attention.py")
+
+MUTATIONS = {
+    "gqa_index": ("j = h // G                                          # GQA", "j = h % Hkv                                          # GQA"),
+    "causal_strict": ("m &= k_pos <= q_pos", "m &= k_pos < q_pos"),
+    "dropped_scale": ("S = sc * (q[rb, h, :] @ k[:, j, :].T)", "S = (q[rb, h, :] @ k[:, j, :].T)"),
+    "scale_1_over_d": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
+    "transposed_pv": ("O[b0:b0 + len(rb), h, :] = P @ v[:, j, :]", "O[b0:b0 + len(rb), h, :] = P @ k[:, j, :]"),
+    "merge_weight_index": ("cb = np.where(empty, 0.0, np.exp(lse_b - ls))", "cb = np.where(empty, 0.0, np.exp(lse_a - ls))"),
+    "merge_dropped_log": ("lse = np.where(empty, NEG_INF, ms + np.log(wa + wb))", "lse = np.where(empty, NEG_INF, ms + (wa + wb))"),
+    "zigzag_chunk": ("(2 * R - 1 - r) * c + np.arange(c)", "(2 * R - 2 - r) * c + np.arange(c)"),
+    "reshard_transposed": ("y[u, s * n:(s + 1) * n] = x[s, :, u * Hl:(u + 1) * Hl]", "y[u, s * n:(s + 1) * n] = x[u, :, s * Hl:(s + 1) * Hl]"),
+    "doc_boundary": ('idx = np.searchsorted(offsets, pos, side="right") - 1', 'idx = np.searchsorted(offsets, pos, side="left") - 1'),
+    "bwd_sign": ("dS = P * (dP - D[:, None])", "dS = P * (dP + D[:, None])"),
+    "bwd_gqa_overwrite": ("dk[:, j, :] += sc * (dS.T @ q[:, h, :])", "dk[:, j, :] = sc * (dS.T @ q[:, h, :])"),
+    "bwd_dropped_scale": ("dq[:, h, :] = sc * (dS @ k[:, j, :])", "dq[:, h, :] = (dS @ k[:, j, :])"),
+    "lse_reshard_back": ("out[s, u * Hl:(u + 1) * Hl, :] = lse[u, :, s * n:(s + 1) * n]", "out[s, u * Hl:(u + 1) * Hl, :] = lse[s, :, u * n:(u + 1) * n]"),
+}
+
+
+def _mutant(old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name):
+    mod = _mutant(*MUTATIONS[name])
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:  # an AssertionError, or a crash the mistake causes
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches mutation {name}"
