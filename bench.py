@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of causal context-parallel attention forward on GB300.
+
+One step = one cp_attn_fwd call over the whole workload (every emulated
+rank): with Ulysses, the seq->head reshard of Q, K, V, the per-head-group
+ring attention and the head->seq reshard of O and LSE; with emit-partials,
+the per-step partials and their merge.  Inputs are seeded synthetic bf16
+N(0,1) tensors resident in HBM; L2 is flushed (a 256 MiB write) before every
+timed step and the flush is outside the step's CUDA-event bracket.
+
+Prints one JSON line.  ``value`` is useful TFLOP/s (4 * d * Hq * visible
+(query, key) pairs per step, summed over ranks, / the max-over-ranks time).
+``--impl reference`` times the CPU oracle instead, on bounded samples of the
+same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def useful_flops(w: workloads.Workload, offsets) -> int:
+    """4 * d * Hq * (visible pairs): QK^T and PV, 2 FLOPs per multiply-add."""
+    if offsets is None:
+        pairs = w.L * (w.L + 1) // 2
+    else:
+        lens = np.diff(np.asarray(offsets, dtype=np.int64))
+        pairs = int((lens * (lens + 1) // 2).sum())
+    return 4 * w.d * w.Hq * pairs
+
+
+def row_visible(pos: np.ndarray, offsets) -> np.ndarray:
+    if offsets is None:
+        return pos + 1
+    offs = np.asarray(offsets, dtype=np.int64)
+    start = offs[np.searchsorted(offs, pos, side="right") - 1]
+    return pos - start + 1
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return dict(FALLBACK_PEAKS), "fallback"
+    try:
+        raw = json.load(open(path))
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+    flat = {}
+
+    def walk(x):
+        if isinstance(x, dict):
+            for k, v in x.items():
+                if isinstance(v, (int, float)) and not isinstance(v, bool):
+                    flat.setdefault(k, float(v))
+                else:
+                    walk(v)
+    walk(raw)
+    out = {}
+    for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+        out[key] = flat.get(key, FALLBACK_PEAKS[key])
+    return out, "measured" if all(k in flat for k in ("hbm_gbs", "bf16_tflops")) else "partly fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, f[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh", "kernels.h"):
+        h.update(open(os.path.join(ROOT, "context_long_sequence_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu capture, if the
+    kernel source has not changed since (else None)."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return rec.get("per_launch_bytes", {}).get(workload)
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+
+
+def time_oracle(w, inputs_cpu, offsets, rows_per_call, heads, seed, min_seconds, max_calls=64):
+    """Time the oracle on seeded random query rows until at least min_seconds."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    flops = 0
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        rows = np.sort(rng.choice(w.L, size=rows_per_call, replace=False))
+        oracle.attention_rows(inputs_cpu["q"], inputs_cpu["k"], inputs_cpu["v"], rows=rows, offsets=offsets,
+                              heads=heads)
+        flops += 4 * w.d * len(heads) * int(row_visible(rows, offsets).sum())
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or calls >= max_calls:
+            return flops, el, calls
+
+
+def cpu_inputs(w, device_inputs=None):
+    import torch
+    if device_inputs is not None:
+        return {k: v.cpu() for k, v in device_inputs.items()}
+    return workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device="cpu", k_scale=w.k_scale)
+
+
+# ---------------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workloads.WORKLOAD_BY_NAME[args.workload]
+    offsets = workloads.workload_doc_offsets(w)
+    flops_step = useful_flops(w, offsets)
+    warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, w, offsets, flops_step, warmup, world)
+
+    import torch
+    import context_long_sequence_gb300 as cpa
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+
+    plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
+                    doc_offsets=offsets, emit_partials=w.emit_partials)
+    # Independent replica per GPU (the emulated ranks all live on one GPU):
+    # each rank draws its own sequence.
+    g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
+    q, k, v = (g_inputs[n][idx].contiguous() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device=dev)
+    ws = cpa.alloc_workspace(plan, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    status = cpa.cp_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    clock_rec = clocks.stop()
+    barrier()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    if cpa.cp_get_status(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    # ---- end to end through the public API with host buffers
+    q_h, k_h, v_h = (t.cpu().pin_memory() for t in (q, k, v))
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ee0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    # ---- per-kernel breakdown (the dominant kernel's roofline)
+    kern = {}
+    U, R = w.ulysses, w.ring
+    if U > 1:
+        qh = torch.empty(R, U, plan.L // R, w.Hq // U, w.d, dtype=torch.bfloat16, device=dev)
+        kh = torch.empty(R, U, plan.L // R, w.Hkv // U, w.d, dtype=torch.bfloat16, device=dev)
+        vh = torch.empty_like(kh)
+        oh = torch.empty_like(qh)
+        lh = torch.empty(R, U, w.Hq // U, plan.L // R, dtype=torch.float32, device=dev)
+    else:
+        qh, kh, vh, oh, lh = q, k, v, o, lse
+
+    def timed(fn, reps):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
+
+    reps = max(3, min(args.steps, 10))
+    attn_ms = timed(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
+    kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_step / attn_ms / 1e9}
+    if U > 1:
+        def rin():
+            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh, stream=stream)
+            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh, stream=stream)
+            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, v, vh, stream=stream)
+
+        def rout():
+            cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, oh, o, stream=stream)
+            cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, w.Hq, 1, 4, lh, lse, stream=stream)
+        bytes_in = 2 * 2 * w.L * w.d * (w.Hq + 2 * w.Hkv)
+        bytes_out = 2 * (2 * w.L * w.d * w.Hq + 4 * w.L * w.Hq)
+        t_in = timed(rin, reps)
+        t_out = timed(rout, reps)
+        kern["reshard_seq_to_head"] = {"ms": t_in, "gbs": bytes_in / t_in / 1e6, "bytes": bytes_in}
+        kern["reshard_head_to_seq"] = {"ms": t_out, "gbs": bytes_out / t_out / 1e6, "bytes": bytes_out}
+
+    peaks, peak_src = load_peaks()
+    # Max over ranks of the timed totals.
+    times = torch.tensor([total_ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms_max, attn_ms_max = times.tolist()
+
+    result = None
+    if rank == 0:
+        ms_per_step = total_ms / args.steps
+        value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+        launches_per_step = (6 if U > 1 else 1) + (1 if w.emit_partials else 0)
+        achieved = flops_step / (attn_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        result = {
+            "metric": "CP causal attention forward, useful TFLOP/s",
+            "value": round(value, 3),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": U, "ring": R,
+                       "layout": "zigzag" if w.layout else "contiguous", "docs": bool(offsets is not None),
+                       "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
+                       "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",
+                       "l2": "flushed (256 MiB write) before every timed step"},
+            "tokens_per_s": round(world * w.L / (ms_per_step * 1e-3), 1),
+            "useful_flops_per_step": flops_step,
+            "e2e": {"value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"bf16 dense burst, {peak_src}",
+                         "traffic": profiled_traffic(w.name)},
+            "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for k, v in kern.items()},
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "clocks": clock_rec,
+            "wall_s_timed": round(t_wall, 3),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, g_inputs, offsets)
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def cpu_baseline(w, g_inputs, offsets):
+    """The oracle, as it stands, on a bounded seeded sample of the workload."""
+    cpu = cpu_inputs(w, g_inputs)
+    heads = list(range(w.Hq))
+    rows = 64
+    flops, el, calls = time_oracle(w, cpu, offsets, rows, heads, seed=0, min_seconds=10.0, max_calls=16)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{calls} x {rows} seeded random query rows x {len(heads)} heads of {w.name} "
+                      f"(fp64 numpy, {el:.1f} s)"}
+
+
+def run_reference(args, w, offsets, flops_step, warmup, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample (a
+    fixed number of seeded random query rows over all heads)."""
+    cpu = cpu_inputs(w)
+    heads = list(range(w.Hq))
+    rows = 16 if w.L >= 65536 else 32
+    rng_seed = 0
+    for i in range(warmup):
+        time_oracle(w, cpu, offsets, rows, heads, seed=rng_seed + i, min_seconds=0.0, max_calls=1)
+    flops = 0
+    t = 0.0
+    for i in range(args.steps):
+        f, el, _ = time_oracle(w, cpu, offsets, rows, heads, seed=1000 + i, min_seconds=0.0, max_calls=1)
+        flops += f
+        t += el
+    value = flops / t / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = f"per step {rows} seeded random query rows x {len(heads)} heads of {w.name} (fp64 numpy oracle)"
+    line = {
+        "impl": "reference", "metric": "CP causal attention forward, useful TFLOP/s", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
+        "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": w.ulysses,
+                   "ring": w.ring},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

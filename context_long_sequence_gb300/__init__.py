@@ -1,0 +1,224 @@
+"""Python binding of libcpattn (include/cp_attn.h): argument marshalling only.
+
+Every function here forwards to the C ABI of the same name; all computation
+runs in the library's CUDA kernels.  PyTorch is used only to own device
+memory and to name the current stream.  Using this module fails loudly if
+the library has not been built (``python -m context_long_sequence_gb300.build``):
+the first call raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcpattn.so")
+
+# Constants (mirrors include/cp_attn.h).
+CP_ATTN_PLAN_VERSION = 1
+CP_OK = 0
+CP_ERR_INVALID_ARG = -1
+CP_ERR_UNSUPPORTED = -2
+CP_ERR_ALIGNMENT = -3
+CP_ERR_CUDA = -4
+CP_ERR_DEVICE_TIMEOUT = -5
+CP_ERR_DEVICE_BOUNDS = -6
+CP_ERR_WORKSPACE = -7
+CP_ERR_ARCH = -8
+CP_LAYOUT_CONTIGUOUS = 0
+CP_LAYOUT_ZIGZAG = 1
+CP_SEQ_TO_HEAD = 0
+CP_HEAD_TO_SEQ = 1
+CP_TOKEN_MAJOR = 0
+CP_HEAD_MAJOR = 1
+CP_OP_FWD = 0
+CP_OP_BWD = 1
+
+
+class cp_plan_desc_t(ctypes.Structure):
+    _fields_ = [
+        ("version", ctypes.c_int32),
+        ("L", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("ulysses_degree", ctypes.c_int32),
+        ("ring_degree", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("num_docs", ctypes.c_int32),
+        ("doc_offsets", ctypes.POINTER(ctypes.c_int32)),
+        ("softmax_scale", ctypes.c_float),
+        ("emit_partials", ctypes.c_int32),
+    ]
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_lib = None
+
+
+def _L():
+    """The loaded library; raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libcpattn.so is not built ({LIB_PATH}); run "
+                           "`python -m context_long_sequence_gb300.build` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.cp_plan_create.argtypes = [ctypes.POINTER(cp_plan_desc_t), ctypes.POINTER(_vp)]
+    lib.cp_plan_destroy.argtypes = [_vp]
+    lib.cp_plan_destroy.restype = None
+    lib.cp_index_map.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.cp_workspace_size.argtypes = [_vp, _i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ulysses_reshard.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+    lib.cp_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.cp_attn_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
+    lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.cp_strerror.argtypes = [_i]
+    lib.cp_strerror.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
+            "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_bwd", "cp_merge_lse", "cp_get_status", "cp_strerror"]
+
+
+class CPError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {cp_strerror(code)} ({code})")
+
+
+def cp_strerror(code: int) -> str:
+    return _L().cp_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != CP_OK:
+        raise CPError(rc, where)
+
+
+def _ptr(x):
+    """Device address of a tensor (or an int address); None -> NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """Owns a cp_plan_t (cp_plan_create / cp_plan_destroy)."""
+
+    def __init__(self, L, Hq, Hkv, d, ulysses_degree=1, ring_degree=1, layout=CP_LAYOUT_CONTIGUOUS,
+                 doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True):
+        self._h = None
+        desc = cp_plan_desc_t()
+        desc.version = CP_ATTN_PLAN_VERSION
+        desc.L, desc.Hq, desc.Hkv, desc.d = int(L), int(Hq), int(Hkv), int(d)
+        desc.ulysses_degree, desc.ring_degree = int(ulysses_degree), int(ring_degree)
+        desc.layout = int(layout)
+        desc.causal = 1 if causal else 0
+        self._offsets = None
+        if doc_offsets is not None and len(doc_offsets) > 2:
+            self._offsets = (ctypes.c_int32 * len(doc_offsets))(*[int(x) for x in doc_offsets])
+            desc.num_docs = len(doc_offsets) - 1
+            desc.doc_offsets = ctypes.cast(self._offsets, ctypes.POINTER(ctypes.c_int32))
+        else:
+            desc.num_docs = 0
+            desc.doc_offsets = None
+        desc.softmax_scale = float(softmax_scale)
+        desc.emit_partials = 1 if emit_partials else 0
+        h = _vp()
+        _check(_L().cp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "cp_plan_create")
+        self._h = h
+        self.L, self.Hq, self.Hkv, self.d = desc.L, desc.Hq, desc.Hkv, desc.d
+        self.U, self.R = desc.ulysses_degree, desc.ring_degree
+        self.P = self.U * self.R
+        self.n = self.L // self.P
+        self.layout = desc.layout
+        self.emit_partials = bool(emit_partials)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h is not None:
+            _L().cp_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def index_map(self) -> np.ndarray:
+        out = np.empty(self.L, dtype=np.int32)
+        _check(_L().cp_index_map(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "cp_index_map")
+        return out
+
+    def workspace_size(self, op=CP_OP_FWD) -> int:
+        n = ctypes.c_size_t()
+        _check(_L().cp_workspace_size(self._h, int(op), ctypes.byref(n)), "cp_workspace_size")
+        return n.value
+
+
+def ulysses_reshard(plan: Plan, direction, tensor_kind, H, row_elems, elem_bytes, inp, out, stream=None):
+    _check(_L().ulysses_reshard(plan.handle, int(direction), int(tensor_kind), int(H), int(row_elems),
+                                int(elem_bytes), _ptr(inp), _ptr(out), _stream(stream)), "ulysses_reshard")
+
+
+def cp_attn_fwd(plan: Plan, q, k, v, o, lse, workspace=None, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L().cp_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                            int(workspace_bytes), _stream(stream)), "cp_attn_fwd")
+
+
+def cp_attn_fwd_local(plan: Plan, q, k, v, o, lse, stream=None):
+    _check(_L().cp_attn_fwd_local(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)),
+           "cp_attn_fwd_local")
+
+
+def cp_attn_bwd(plan: Plan, q, k, v, o, lse, dO, dq, dk, dv, workspace=None, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L().cp_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "cp_attn_bwd")
+
+
+def cp_merge_lse(n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream=None):
+    _check(_L().cp_merge_lse(int(n_parts), int(rows), int(H), int(d), _ptr(o_parts), _ptr(lse_parts),
+                             _ptr(o_out), _ptr(lse_out), _stream(stream)), "cp_merge_lse")
+
+
+def cp_get_status(stream=None) -> int:
+    code = ctypes.c_int32()
+    _check(_L().cp_get_status(_stream(stream), ctypes.byref(code)), "cp_get_status")
+    return code.value
+
+
+def alloc_workspace(plan: Plan, op=CP_OP_FWD, device="cuda"):
+    """A device byte buffer of cp_workspace_size() bytes (None when zero)."""
+    import torch
+    n = plan.workspace_size(op)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None

@@ -1,0 +1,447 @@
+// attn_fwd.cu -- causal context-parallel attention forward on sm_103a.
+//
+// One CTA computes one 128-row query tile of one head of one attention rank.
+// It walks the KV chunks of the ring in ring order -- at step s the chunk of
+// ring rank (r - s) mod R ([MTX] nougat.kr "MaxText long-context training and
+// KV parallelism", section "Split heads or rotate KV": P2P keeps token
+// sharding and computes a partial with each visiting KV chunk) -- and, per
+// 128-key tile that has at least one visible (query, key) pair:
+//
+//   S = Q K^T             tcgen05.mma, bf16 operands in shared memory (TMA,
+//                         128-byte swizzle), fp32 accumulator in TMEM
+//   mask, online softmax  one thread per query row (TMEM lane = row), exp2
+//   O += P V              tcgen05.mma, P staged in shared memory as bf16
+//
+// Tiles with no visible pair are never visited; tiles wholly inside the
+// causal and document window skip the mask.  The merge of the ring partials
+// is fused: the online softmax simply continues across ring steps, which is
+// the exact merge evaluated incrementally.  In emit-partials mode a CTA
+// covers one ring step and writes that step's normalised partial (O, LSE) in
+// fp32 for the separate merge kernel.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator
+// and MMA issuer, warps 2..5 = softmax / correction / epilogue (thread t of
+// warp w owns query row 32*(w%4)+t, the TMEM lanes that warp may access).
+//
+// Pipeline: K and V have two shared-memory stages each; S is double-buffered
+// in TMEM so QK^T of tile j+1 runs while the softmax of tile j runs.  The
+// running max is only raised when it grows by more than 2^8 (log2 units), so
+// O is rescaled in TMEM rarely; the final normalisation uses the same max,
+// which keeps the result exact.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int BM = 128;                      // query rows per tile
+constexpr int BN = 128;                      // keys per tile
+constexpr uint32_t HALF_BYTES = 128 * 128;   // one 64-column (128-byte) swizzled half of a 128-row tile
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr int kThreads = 192;
+
+enum Bar {
+  BAR_Q = 0,
+  BAR_K_FULL = 1,   // +stage
+  BAR_K_EMPTY = 3,  // +stage
+  BAR_V_FULL = 5,   // +stage
+  BAR_V_EMPTY = 7,  // +stage
+  BAR_S_FULL = 9,   // +buffer
+  BAR_S_EMPTY = 11, // +buffer
+  BAR_P_FULL = 13,
+  BAR_O_FULL = 14,
+  BAR_DRAIN = 15,
+  NUM_BARS = 16
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr uint32_t kQ = BM * D * 2;
+  static constexpr uint32_t kKV = BN * D * 2;
+  static constexpr uint32_t kP = BM * BN * 2;
+  static constexpr uint32_t offQ = 0;
+  static constexpr uint32_t offK = offQ + kQ;
+  static constexpr uint32_t offV = offK + 2 * kKV;
+  static constexpr uint32_t offP = offV + 2 * kKV;
+  static constexpr uint32_t offBar = offP + kP;
+  static constexpr uint32_t offMisc = offBar + NUM_BARS * 8;
+  static constexpr uint32_t kUsed = offMisc + 16;
+  // 1 KB alignment slack; D=64 is padded so that one CTA (and one 512-column
+  // TMEM allocation) is resident per SM.
+  static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
+};
+
+// Visit, in ring order, every 128-key tile that may hold a visible key for a
+// query tile with positions [qpos0, qpos_last] and document starts >= lo_min.
+// f(kv_row, kpos0, klen): first row of the tile in the [R*U*T] row space, the
+// tile's first position, and its number of valid keys.
+template <typename F>
+__device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end,
+                                                 int lo_min, int qpos_last, F&& f) {
+  const int nchunks = (g.layout == CP_LAYOUT_CONTIGUOUS) ? 1 : 2;
+  for (int s = s_begin; s < s_end; ++s) {
+    const int src = (r - s + g.R) % g.R;
+    const int a_src = src * g.U + u;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int cslot0 = ch * g.chunk;
+      const int cpos0 = slot_pos(g, src, cslot0);
+      const int lo = max(cpos0, lo_min);
+      const int hi = min(cpos0 + g.chunk - 1, qpos_last);
+      if (lo > hi) continue;
+      const int t1 = (hi - cpos0) / BN;
+      for (int t = (lo - cpos0) / BN; t <= t1; ++t)
+        f(a_src * g.T + cslot0 + t * BN, cpos0 + t * BN, min(BN, g.chunk - t * BN));
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+  using SM = FwdSmem<D>;
+  constexpr int NH = D / 64;  // 64-column halves of a head row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + SM::offQ, sK = s_base + SM::offK, sV = s_base + SM::offV, sP = s_base + SM::offP;
+  auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const AttnGeom& g = args.g;
+  int32_t* status = args.status;
+  const int item_idx = blockIdx.x / g.Hq_loc;
+  const int h = blockIdx.x % g.Hq_loc;
+  const WorkItem it = args.items[item_idx];
+  const int a = it.a, r = a / g.U, u = a % g.U;
+  const int qpos0 = slot_pos(g, r, it.q0);
+  const int qpos_last = qpos0 + it.len - 1;
+  const int lo_min = g.doc_start ? g.doc_start[qpos0] : 0;
+  const int lo_max = g.doc_start ? g.doc_start[qpos_last] : 0;
+  const int s_begin = it.step < 0 ? 0 : it.step;
+  const int s_end = it.step < 0 ? g.R : it.step + 1;
+  const int hkv = h / g.G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_Q), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_K_FULL + i), 1);
+      mbar_init(bar(BAR_K_EMPTY + i), 1);
+      mbar_init(bar(BAR_V_FULL + i), 1);
+      mbar_init(bar(BAR_V_EMPTY + i), 1);
+      mbar_init(bar(BAR_S_FULL + i), 1);
+      mbar_init(bar(BAR_S_EMPTY + i), 4);
+    }
+    mbar_init(bar(BAR_P_FULL), 4);
+    mbar_init(bar(BAR_O_FULL), 1);
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(BAR_Q), SM::kQ);
+      const int qrow = a * g.T + it.q0;
+      for (int hh = 0; hh < NH; ++hh) tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow);
+      int nk = 0, nv = 0;
+      for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row, int, int) {
+        if (*abort_flag) return;
+        const int st = nk & 1;
+        const uint32_t ph = ((nk >> 1) & 1) ^ 1;
+        if (!mbar_wait(bar(BAR_K_EMPTY + st), ph, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(BAR_K_FULL + st), SM::kKV);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sK + st * SM::kKV + hh * HALF_BYTES, &tm_k, bar(BAR_K_FULL + st), hkv * D + hh * 64, kv_row);
+        ++nk;
+        if (!mbar_wait(bar(BAR_V_EMPTY + st), ph, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(BAR_V_FULL + st), SM::kKV);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sV + st * SM::kKV + hh * HALF_BYTES, &tm_v, bar(BAR_V_FULL + st), hkv * D + hh * 64, kv_row);
+        ++nv;
+      });
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA exits.
+        mbar_wait(bar(BAR_Q), 0, nullptr, status);
+        for (int i = max(0, nk - 2); i < nk; ++i) mbar_wait(bar(BAR_K_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
+        for (int i = max(0, nv - 2); i < nv; ++i) mbar_wait(bar(BAR_V_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(bar(BAR_P_FULL), i & 1, abort_flag, status)) return false;
+        if (!mbar_wait(bar(BAR_V_FULL + st), (i >> 1) & 1, abort_flag, status)) return false;
+        tc_fence_after();
+        const uint32_t vb = sV + st * SM::kKV;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // A = P [128 x 128 keys], K-major: 16 keys = 32 bytes inside a 64-key half.
+          const uint64_t ad = smem_desc_sw128(sP + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
+          // B = V [keys x d] read as N=d x K=keys, MN-major: 16 keys = 16 rows of 128 bytes;
+          // the two 64-column halves of d are HALF_BYTES apart (leading offset).
+          const uint64_t bd = smem_desc_sw128(vb + kk * 2048, HALF_BYTES, 1024);
+          mma_bf16_ss(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_O_FULL));
+        mma_commit(bar(BAR_V_EMPTY + st));
+        return true;
+      };
+      int j = 0;
+      if (mbar_wait(bar(BAR_Q), 0, abort_flag, status)) {
+        for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) {
+          if (*abort_flag) return;
+          const int st = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait(bar(BAR_K_FULL + st), ph, abort_flag, status)) return;
+          if (!mbar_wait(bar(BAR_S_EMPTY + st), ph ^ 1, abort_flag, status)) return;
+          tc_fence_after();
+          const uint32_t kb = sK + st * SM::kKV;
+          const uint32_t tS = st ? tS1 : tS0;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+            mma_bf16_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc_qk,
+                        kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_S_FULL + st));
+          mma_commit(bar(BAR_K_EMPTY + st));
+          if (j > 0 && !issue_pv(j - 1)) return;
+          ++j;
+        });
+        if (j > 0 && !*abort_flag) issue_pv(j - 1);
+      }
+      // Every MMA issued so far completes before TMEM and shared memory are released.
+      mma_commit(bar(BAR_DRAIN));
+      mbar_wait(bar(BAR_DRAIN), 0, nullptr, status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const bool row_valid = row < it.len;
+    const int my_pos = row_valid ? qpos0 + row : -1;
+    const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
+    const float sl2 = g.scale * 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
+    int j = 0;
+    bool ok = true;
+    for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int kpos0, int klen) {
+      if (!ok) return;
+      const int b = j & 1;
+      ok = warp_all(mbar_wait(bar(BAR_S_FULL + b), (j >> 1) & 1, abort_flag, status));
+      if (!ok) return;
+      tc_fence_after();
+      uint32_t sr[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32((b ? tS1 : tS0) + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY + b));
+      float* s = reinterpret_cast<float*>(sr);
+      const bool full = (klen == BN) && (kpos0 + BN - 1 <= qpos0) && (lo_max <= kpos0);
+      if (!full) {
+        const int c_lo = my_lo - kpos0;
+        const int c_hi = min(my_pos - kpos0, klen - 1);
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c < c_lo || c > c_hi) s[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m, mx * sl2);
+      float alpha = 1.f;
+      if (m_new > m + kRescaleThreshold) {
+        alpha = ex2_approx(m - m_new);
+        m = m_new;
+      }
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const float p = ex2_approx(fmaf(s[c], sl2, -mb));
+        s[c] = p;
+        rs += p;
+      }
+      l = l * alpha + rs;
+      if (j > 0) {
+        // PV of the previous tile must be done: it reads P and writes O.
+        ok = warp_all(mbar_wait(bar(BAR_O_FULL), (j - 1) & 1, abort_flag, status));
+        if (!ok) return;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + lane_off + c * 32, ov);
+            tmem_wait_ld();
+            reg_fence(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P -> shared memory, bf16, K-major with 128-byte swizzle.
+      const uint32_t prow = sP + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        const uint32_t addr = prow + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (row & 7)) << 4);
+        st_shared_v4(addr, pack_bf16x2(s[8 * ch + 0], s[8 * ch + 1]), pack_bf16x2(s[8 * ch + 2], s[8 * ch + 3]),
+                     pack_bf16x2(s[8 * ch + 4], s[8 * ch + 5]), pack_bf16x2(s[8 * ch + 6], s[8 * ch + 7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
+      ++j;
+    });
+    if (ok && j > 0) {
+      ok = warp_all(mbar_wait(bar(BAR_O_FULL), (j - 1) & 1, abort_flag, status));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      const float lse = has ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+      const bool partial = args.o_part != nullptr;
+      const int s_idx = s_begin;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        if (j > 0) {
+          tmem_ld32(tO + lane_off + c * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+        }
+        if (!row_valid) continue;
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = (j > 0) ? __uint_as_float(ov[e]) * inv_l : 0.f;
+        if (partial) {
+          float* dst = args.o_part +
+                       ((static_cast<size_t>(r * g.R + s_idx) * g.T + it.q0 + row) * g.Hq_loc + h) * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        } else {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) +
+                               (static_cast<size_t>(a * g.T + it.q0 + row) * g.Hq_loc + h) * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *reinterpret_cast<uint4*>(dst + e) =
+                make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
+                           pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
+        }
+      }
+      if (row_valid) {
+        if (partial)
+          args.lse_part[(static_cast<size_t>(r * g.R + s_idx) * g.Hq_loc + h) * g.T + it.q0 + row] = lse;
+        else
+          args.lse[(static_cast<size_t>(a) * g.Hq_loc + h) * g.T + it.q0 + row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a [rows][cols] row-major matrix, box 64 cols x 128 rows,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_d(const FwdArgs& a, cudaStream_t stream) {
+  const AttnGeom& g = a.g;
+  const uint64_t rows = static_cast<uint64_t>(g.R) * g.U * g.T;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
+      !make_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, rows) ||
+      !make_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, rows))
+    return CP_ERR_CUDA;
+  const uint32_t smem = FwdSmem<D>::kBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return CP_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long grid = static_cast<long long>(a.n_items) * g.Hq_loc;
+  if (grid <= 0) return CP_OK;
+  if (grid > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
+  attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128) return launch_d<128>(a, stream);
+  if (a.d == 64) return launch_d<64>(a, stream);
+  return CP_ERR_UNSUPPORTED;
+}
+
+}  // namespace cpattn

@@ -1,0 +1,469 @@
+// cp_attn.cu -- the C ABI (include/cp_attn.h): plan validation and tables,
+// workspace sizing, argument checks, and the order of kernel launches for
+// each entry point.  Host code only; the kernels live in attn_fwd.cu,
+// attn_bwd.cu, reshard.cu and merge.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "cp_attn.h"
+#include "kernels.h"
+
+using cpattn::AttnGeom;
+using cpattn::WorkItem;
+
+// Device status word: first device-side error since the last cp_get_status().
+__device__ int32_t g_cp_status;
+
+struct cp_plan {
+  cp_plan_desc_t desc;
+  std::vector<int32_t> offsets;  // empty: one document
+  int P, n, T, chunk, nchunks;
+  float scale;
+  bool on_device;
+  int device;
+  int32_t* d_doc_start;          // [L] or null
+  WorkItem* d_items_fused;
+  int n_items_fused;
+  WorkItem* d_items_steps;       // emit-partials: one item per (query tile, ring step)
+  int n_items_steps;
+};
+
+namespace {
+
+constexpr int kTile = 128;
+
+int32_t* status_ptr() {
+  static int32_t* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cp_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int doc_start_host(const cp_plan* p, int pos) {
+  if (p->offsets.empty()) return 0;
+  auto it = std::upper_bound(p->offsets.begin(), p->offsets.end(), pos);
+  return *(it - 1);
+}
+
+AttnGeom geom(const cp_plan* p) {
+  AttnGeom g;
+  const cp_plan_desc_t& d = p->desc;
+  g.L = d.L;
+  g.R = d.ring_degree;
+  g.U = d.ulysses_degree;
+  g.T = p->T;
+  g.Hq_loc = d.Hq / d.ulysses_degree;
+  g.Hkv_loc = d.Hkv / d.ulysses_degree;
+  g.G = d.Hq / d.Hkv;
+  g.layout = d.layout;
+  g.chunk = p->chunk;
+  g.scale = p->scale;
+  g.doc_start = p->d_doc_start;
+  return g;
+}
+
+// Number of 128-key tiles the forward kernel visits for a query tile (the
+// same walk as the kernel's, evaluated on the host for scheduling).
+int visited_tiles(const cp_plan* p, const AttnGeom& g, int r, int q0, int len, int s_begin, int s_end) {
+  const int qpos0 = cpattn::slot_pos(g, r, q0);
+  const int qpos_last = qpos0 + len - 1;
+  const int lo_min = doc_start_host(p, qpos0);
+  int count = 0;
+  for (int s = s_begin; s < s_end; ++s) {
+    const int src = (r - s + g.R) % g.R;
+    for (int ch = 0; ch < p->nchunks; ++ch) {
+      const int cpos0 = cpattn::slot_pos(g, src, ch * g.chunk);
+      const int lo = std::max(cpos0, lo_min);
+      const int hi = std::min(cpos0 + g.chunk - 1, qpos_last);
+      if (lo > hi) continue;
+      count += (hi - cpos0) / kTile - (lo - cpos0) / kTile + 1;
+    }
+  }
+  return count;
+}
+
+// Query tiles ordered by descending work (longest first onto the SMs).
+std::vector<WorkItem> build_items(const cp_plan* p, bool per_step) {
+  const AttnGeom g = geom(p);
+  struct Keyed {
+    int work;
+    WorkItem it;
+  };
+  std::vector<Keyed> v;
+  const int A = g.R * g.U;
+  for (int a = 0; a < A; ++a) {
+    const int r = a / g.U;
+    for (int ch = 0; ch < p->nchunks; ++ch)
+      for (int t0 = 0; t0 < p->chunk; t0 += kTile) {
+        const int q0 = ch * p->chunk + t0;
+        const int len = std::min(kTile, p->chunk - t0);
+        if (per_step) {
+          for (int s = 0; s < g.R; ++s)
+            v.push_back({visited_tiles(p, g, r, q0, len, s, s + 1), WorkItem{a, q0, len, s}});
+        } else {
+          v.push_back({visited_tiles(p, g, r, q0, len, 0, g.R), WorkItem{a, q0, len, -1}});
+        }
+      }
+  }
+  std::stable_sort(v.begin(), v.end(), [](const Keyed& x, const Keyed& y) { return x.work > y.work; });
+  std::vector<WorkItem> out(v.size());
+  for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].it;
+  return out;
+}
+
+template <typename T>
+int upload(const std::vector<T>& h, T** d) {
+  *d = nullptr;
+  if (h.empty()) return CP_OK;
+  if (cudaMalloc(reinterpret_cast<void**>(d), h.size() * sizeof(T)) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess) return CP_ERR_CUDA;
+  return CP_OK;
+}
+
+int check_device(const cp_plan* p) {
+  if (!p->on_device) return CP_ERR_CUDA;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  if (dev != p->device) return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+struct FwdWorkspace {
+  size_t qh, kh, vh, oh, lseh, opart, lsepart, total;
+};
+
+FwdWorkspace fwd_workspace(const cp_plan* p) {
+  const cp_plan_desc_t& d = p->desc;
+  const size_t L = d.L;
+  FwdWorkspace w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  if (d.ulysses_degree > 1) {
+    w.qh = take(L * d.Hq * d.d * 2);
+    w.kh = take(L * d.Hkv * d.d * 2);
+    w.vh = take(L * d.Hkv * d.d * 2);
+    w.oh = take(L * d.Hq * d.d * 2);
+    w.lseh = take(L * d.Hq * 4);
+  }
+  if (d.emit_partials) {
+    w.opart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * d.d * 4);
+    w.lsepart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+size_t bwd_workspace(const cp_plan* p) {
+  return align256(static_cast<size_t>(p->desc.L) * p->desc.Hq * 4);  // delta = rowsum(dO * O)
+}
+
+}  // namespace
+
+extern "C" {
+
+int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
+  if (!desc || !out) return CP_ERR_INVALID_ARG;
+  const cp_plan_desc_t& d = *desc;
+  if (d.version != CP_ATTN_PLAN_VERSION) return CP_ERR_INVALID_ARG;
+  if (d.L <= 0 || d.Hq <= 0 || d.Hkv <= 0 || d.ulysses_degree <= 0 || d.ring_degree <= 0) return CP_ERR_INVALID_ARG;
+  if (d.Hq % d.Hkv) return CP_ERR_INVALID_ARG;
+  if (d.layout != CP_LAYOUT_CONTIGUOUS && d.layout != CP_LAYOUT_ZIGZAG) return CP_ERR_INVALID_ARG;
+  if (d.num_docs < 0) return CP_ERR_INVALID_ARG;
+  if (!(d.softmax_scale >= 0.f) || std::isinf(d.softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (d.d != 64 && d.d != 128) return CP_ERR_UNSUPPORTED;
+  if (d.causal != 1) return CP_ERR_UNSUPPORTED;
+  if (d.Hkv % d.ulysses_degree) return CP_ERR_UNSUPPORTED;  // KV heads cap the A2A degree
+  const int R = d.ring_degree, U = d.ulysses_degree;
+  if (d.layout == CP_LAYOUT_CONTIGUOUS ? (d.L % R) : (d.L % (2 * R))) return CP_ERR_INVALID_ARG;
+  const int T = d.L / R;
+  if (T % U) return CP_ERR_INVALID_ARG;
+  if (d.emit_partials && U != 1) return CP_ERR_UNSUPPORTED;
+  // Index arithmetic in the kernels is 32-bit for positions and slots.
+  if (static_cast<long long>(d.L) * U >= (1LL << 31)) return CP_ERR_UNSUPPORTED;
+
+  cp_plan* p = new (std::nothrow) cp_plan();
+  if (!p) return CP_ERR_INVALID_ARG;
+  p->desc = d;
+  p->desc.doc_offsets = nullptr;
+  if (d.num_docs > 1) {
+    if (!d.doc_offsets) {
+      delete p;
+      return CP_ERR_INVALID_ARG;
+    }
+    p->offsets.assign(d.doc_offsets, d.doc_offsets + d.num_docs + 1);
+    bool ok = p->offsets.front() == 0 && p->offsets.back() == d.L;
+    for (int i = 0; i < d.num_docs && ok; ++i) ok = p->offsets[i] < p->offsets[i + 1];
+    if (!ok) {
+      delete p;
+      return CP_ERR_INVALID_ARG;
+    }
+  }
+  p->P = R * U;
+  p->T = T;
+  p->n = T / U;
+  p->nchunks = d.layout == CP_LAYOUT_CONTIGUOUS ? 1 : 2;
+  p->chunk = T / p->nchunks;
+  p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
+  p->on_device = false;
+  p->d_doc_start = nullptr;
+  p->d_items_fused = p->d_items_steps = nullptr;
+  p->n_items_fused = p->n_items_steps = 0;
+
+  // Device tables, when a CUDA device is present (host-only use -- index
+  // maps, workspace sizes -- works without one).
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      delete p;
+      return CP_ERR_CUDA;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+      delete p;
+      return CP_ERR_ARCH;
+    }
+    p->device = dev;
+    int rc = CP_OK;
+    if (!p->offsets.empty()) {
+      std::vector<int32_t> ds(d.L);
+      for (int i = 0; i < d.num_docs; ++i)
+        for (int x = p->offsets[i]; x < p->offsets[i + 1]; ++x) ds[x] = p->offsets[i];
+      rc = upload(ds, &p->d_doc_start);
+    }
+    std::vector<WorkItem> fused = build_items(p, false);
+    p->n_items_fused = static_cast<int>(fused.size());
+    if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
+    if (rc == CP_OK && d.emit_partials) {
+      std::vector<WorkItem> steps = build_items(p, true);
+      p->n_items_steps = static_cast<int>(steps.size());
+      rc = upload(steps, &p->d_items_steps);
+    }
+    if (rc != CP_OK) {
+      cudaFree(p->d_doc_start);
+      cudaFree(p->d_items_fused);
+      cudaFree(p->d_items_steps);
+      delete p;
+      return rc;
+    }
+    p->on_device = true;
+  }
+  *out = p;
+  return CP_OK;
+}
+
+void cp_plan_destroy(cp_plan_t* p) {
+  if (!p) return;
+  if (p->on_device) {
+    cudaFree(p->d_doc_start);
+    cudaFree(p->d_items_fused);
+    cudaFree(p->d_items_steps);
+  }
+  delete p;
+}
+
+int cp_index_map(const cp_plan_t* p, int32_t* host_out) {
+  if (!p || !host_out) return CP_ERR_INVALID_ARG;
+  const AttnGeom g = geom(p);
+  // Sequence-sharded slot order: rank g = r*U + u holds ring-local slots
+  // [u*n, (u+1)*n) of ring rank r, so the slot order is ring rank major.
+  for (int r = 0; r < g.R; ++r)
+    for (int t = 0; t < g.T; ++t) host_out[static_cast<size_t>(r) * g.T + t] = cpattn::slot_pos(g, r, t);
+  return CP_OK;
+}
+
+int cp_workspace_size(const cp_plan_t* p, int op, size_t* bytes) {
+  if (!p || !bytes) return CP_ERR_INVALID_ARG;
+  if (op == CP_OP_FWD)
+    *bytes = fwd_workspace(p).total;
+  else if (op == CP_OP_BWD)
+    *bytes = bwd_workspace(p);
+  else
+    return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+int ulysses_reshard(const cp_plan_t* p, int direction, int tensor_kind, int H, int row_elems, int elem_bytes,
+                    const void* in, void* out, cudaStream_t stream) {
+  if (!p || !in || !out) return CP_ERR_INVALID_ARG;
+  if (direction != CP_SEQ_TO_HEAD && direction != CP_HEAD_TO_SEQ) return CP_ERR_INVALID_ARG;
+  if (tensor_kind != CP_TOKEN_MAJOR && tensor_kind != CP_HEAD_MAJOR) return CP_ERR_INVALID_ARG;
+  const int U = p->desc.ulysses_degree;
+  if (H <= 0 || row_elems <= 0 || elem_bytes <= 0 || H % U) return CP_ERR_INVALID_ARG;
+  if (tensor_kind == CP_HEAD_MAJOR && row_elems != 1) return CP_ERR_INVALID_ARG;
+  if (!aligned16(in) || !aligned16(out)) return CP_ERR_ALIGNMENT;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const char* a = static_cast<const char*>(in);
+  const char* b = static_cast<const char*>(out);
+  const size_t bytes = static_cast<size_t>(p->desc.L) * H * row_elems * elem_bytes;
+  if (a < b + bytes && b < a + bytes) return CP_ERR_INVALID_ARG;
+  return cpattn::launch_reshard(p->desc.ring_degree, U, p->n, H, row_elems, direction, tensor_kind, elem_bytes, in,
+                                out, stream);
+}
+
+int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!p || !q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (workspace && !aligned16(workspace)))
+    return CP_ERR_ALIGNMENT;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const FwdWorkspace w = fwd_workspace(p);
+  if (w.total > 0 && (!workspace || workspace_bytes < w.total)) return CP_ERR_WORKSPACE;
+  const cp_plan_desc_t& d = p->desc;
+  char* ws = static_cast<char*>(workspace);
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = d.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  if (d.ulysses_degree == 1) {
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    if (d.emit_partials) {
+      a.o_part = reinterpret_cast<float*>(ws + w.opart);
+      a.lse_part = reinterpret_cast<float*>(ws + w.lsepart);
+      a.items = p->d_items_steps;
+      a.n_items = p->n_items_steps;
+      rc = cpattn::launch_attn_fwd(a, stream);
+      if (rc != CP_OK) return rc;
+      return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse, stream);
+    }
+    a.items = p->d_items_fused;
+    a.n_items = p->n_items_fused;
+    return cpattn::launch_attn_fwd(a, stream);
+  }
+  // Ulysses / USP: reshard in, ring attention per head group, reshard out.
+  const int R = d.ring_degree, U = d.ulysses_degree;
+  void* qh = ws + w.qh;
+  void* kh = ws + w.kh;
+  void* vh = ws + w.vh;
+  void* oh = ws + w.oh;
+  float* lseh = reinterpret_cast<float*>(ws + w.lseh);
+  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh, stream))) return rc;
+  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh, stream))) return rc;
+  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh, stream))) return rc;
+  a.q = qh;
+  a.k = kh;
+  a.v = vh;
+  a.o = oh;
+  a.lse = lseh;
+  a.items = p->d_items_fused;
+  a.n_items = p->n_items_fused;
+  if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
+  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 2, oh, o, stream))) return rc;
+  return cpattn::launch_reshard(R, U, p->n, d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse, stream);
+}
+
+int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                      cudaStream_t stream) {
+  if (!p || !q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return CP_ERR_ALIGNMENT;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = p->desc.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.items = p->d_items_fused;
+  a.n_items = p->n_items_fused;
+  return cpattn::launch_attn_fwd(a, stream);
+}
+
+int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream) {
+  if (!p || !q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (workspace && !aligned16(workspace)))
+    return CP_ERR_ALIGNMENT;
+  if (p->desc.ulysses_degree != 1) return CP_ERR_UNSUPPORTED;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const size_t need = bwd_workspace(p);
+  if (!workspace || workspace_bytes < need) return CP_ERR_WORKSPACE;
+  cpattn::BwdArgs a{};
+  a.g = geom(p);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = static_cast<float*>(workspace);
+  a.items = p->d_items_fused;
+  a.n_items = p->n_items_fused;
+  a.d = p->desc.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  return cpattn::launch_attn_bwd(a, stream);
+}
+
+int cp_merge_lse(int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts, void* o_out,
+                 float* lse_out, cudaStream_t stream) {
+  if (n_parts <= 0 || rows < 0 || H <= 0 || !o_parts || !lse_parts || !o_out || !lse_out) return CP_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o_out) || !aligned16(lse_out))
+    return CP_ERR_ALIGNMENT;
+  return cpattn::launch_merge(1, n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream);
+}
+
+int cp_get_status(cudaStream_t stream, int32_t* dev_code) {
+  if (!dev_code) return CP_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
+  int32_t code = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&code, g_cp_status, sizeof(code)) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_cp_status, &zero, sizeof(zero)) != cudaSuccess) return CP_ERR_CUDA;
+  *dev_code = code;
+  return CP_OK;
+}
+
+const char* cp_strerror(int code) {
+  switch (code) {
+    case CP_OK: return "ok";
+    case CP_ERR_INVALID_ARG: return "invalid argument";
+    case CP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CP_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case CP_ERR_CUDA: return "CUDA error";
+    case CP_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case CP_ERR_DEVICE_BOUNDS: return "device-side index check failed";
+    case CP_ERR_WORKSPACE: return "workspace missing or too small";
+    case CP_ERR_ARCH: return "device is not sm_103";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// kernels.h -- internal launch interface between the C-ABI layer (cp_attn.cu)
+// and the kernels.  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace cpattn {
+
+// Query tile of one attention rank: slots [q0, q0+len) of attention rank
+// a = r*U + u, lying inside one contiguous-position chunk; `step` is the ring
+// step this item covers (emit-partials mode) or -1 for all steps.
+struct WorkItem {
+  int32_t a, q0, len, step;
+};
+
+// Geometry shared by the forward and backward kernels.  "Attention rank"
+// (r, u): member u of ring rank r after the Ulysses reshard, holding the T
+// slots of ring rank r's shard for Hq_loc query and Hkv_loc KV heads.
+struct AttnGeom {
+  int L, R, U, T;          // T = L / R slots per attention rank
+  int Hq_loc, Hkv_loc, G;  // G = Hq_loc / Hkv_loc
+  int layout;              // CP_LAYOUT_*
+  int chunk;               // contiguous-position chunk length: T or T/2
+  float scale;             // softmax scale
+  const int32_t* doc_start;  // [L] start of the document holding each position, or null
+};
+
+// Global position of slot t of ring rank r.
+__host__ __device__ inline int slot_pos(const AttnGeom& g, int r, int t) {
+  if (g.layout == 0) return r * g.T + t;
+  const int c = g.chunk;
+  return t < c ? r * c + t : (2 * g.R - 1 - r) * c + (t - c);
+}
+
+struct FwdArgs {
+  AttnGeom g;
+  const void* q;  // [R*U*T][Hq_loc][d] bf16
+  const void* k;  // [R*U*T][Hkv_loc][d] bf16
+  const void* v;
+  void* o;        // [R*U*T][Hq_loc][d] bf16     (fused mode)
+  float* lse;     // [R*U][Hq_loc][T]            (fused mode)
+  float* o_part;  // [R][R][T][Hq][d] fp32       (emit-partials mode, U == 1)
+  float* lse_part;// [R][R][Hq][T]
+  const WorkItem* items;
+  int n_items;
+  int d;
+  int32_t* status;
+};
+
+int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+
+struct BwdArgs {
+  AttnGeom g;
+  const void* q;  const void* k;  const void* v;
+  const void* o;  const float* lse;  const void* dO;
+  float* dq;  float* dk;  float* dv;
+  float* delta;   // [R][Hq][T] workspace: rowsum(dO * O)
+  const WorkItem* items;   // fused-mode work list (all ring steps)
+  int n_items;
+  int d;
+  int32_t* status;
+};
+
+int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+
+// Block-permutation copy behind ulysses_reshard.
+int launch_reshard(int R, int U, int n, int H, int row_bytes_total, int direction, int kind,
+                   int elem_bytes, const void* in, void* out, cudaStream_t stream);
+
+// Merge of `n_parts` partials, `batch` independent groups laid out back to back.
+int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts,
+                 const float* lse_parts, void* o_out, float* lse_out, cudaStream_t stream);
+
+}  // namespace cpattn

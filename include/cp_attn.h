@@ -1,0 +1,204 @@
+/*
+ * cp_attn.h -- C ABI of libcpattn: context-parallel causal attention for one
+ * sm_103a GPU, with all P context-parallel ranks emulated side by side in the
+ * GPU's memory.
+ *
+ * What the operations are (the web pages these follow; each citation names a
+ * page and its section):
+ *
+ *  [MTX] nougat.kr, "MaxText long-context training and KV parallelism":
+ *        "Why KV comes back together even after splitting the input" -- a
+ *        long sequence is split over chips by token, and causal attention
+ *        makes every query need the K/V of all earlier tokens;
+ *        "Split heads or rotate KV" -- A2A (Ulysses) swaps token sharding for
+ *        head sharding before attention and swaps back after it, the KV-head
+ *        count capping the degree under GQA; P2P (ring) keeps token sharding,
+ *        computes a partial with each visiting KV chunk and merges the
+ *        partial results; later tokens carry more causal work, so the load
+ *        must be balanced; USP combines A2A groups with a ring.
+ *  [ULY] aionda.blog, "Ulysses sequence parallelism for long-context
+ *        training", "Current state" -- all-to-all along the sequence axis so
+ *        each GPU computes a subset of heads.
+ *  [L3P] siliconandsystems.com, "Llama 3 parallelism", "Four parallelisms
+ *        secure different resources" -- CP must keep the mask between packed
+ *        documents; "Long context changes more than attention cost" --
+ *        balance by actual attention work; activation recompute trades
+ *        memory for compute.
+ *
+ * The pages give no formula.  The attention computed is textbook scaled
+ * dot-product softmax attention, visibility M(i,k) = [pos_k <= pos_i] and
+ * [same packed document], scale 1/sqrt(d) unless set, LSE in natural log,
+ * query head h reading KV head floor(h / (Hq/Hkv)).
+ *
+ * Conventions common to every call
+ *  - Device pointers are plain CUDA device addresses on the current device;
+ *    host pointers are marked "host".  Nothing here takes ownership of a
+ *    caller's buffer.  Calls are asynchronous on `stream` and return 0 on
+ *    success or a negative CP_ERR_* code; on an error return nothing was
+ *    enqueued.  Errors found on the device while a kernel runs (a bounded
+ *    wait that ran out, an index out of range) are recorded in a device
+ *    status word read by cp_get_status().
+ *  - bf16 = bfloat16 (round-to-nearest-even on every conversion).
+ *  - Token-major tensors are [tokens][heads][d] row-major.  "Sequence-sharded"
+ *    tensors hold the P = U*R ranks' shards back to back, rank-major, rank
+ *    g = r*U + u (Ulysses index innermost), each shard n = L/P tokens in slot
+ *    order; cp_index_map() gives the global position of every slot.
+ *  - LSE tensors are [rank][heads][tokens] fp32.
+ *  - Every device pointer must be 16-byte aligned (CP_ERR_ALIGNMENT).
+ */
+#ifndef CP_ATTN_H
+#define CP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CP_ATTN_PLAN_VERSION 1
+
+/* Return codes. */
+#define CP_OK                  0
+#define CP_ERR_INVALID_ARG    -1  /* a size, pointer or enum is out of range */
+#define CP_ERR_UNSUPPORTED    -2  /* valid but not built: d not in {64,128}, U not dividing Hkv, ... */
+#define CP_ERR_ALIGNMENT      -3  /* a device pointer is not 16-byte aligned */
+#define CP_ERR_CUDA           -4  /* a CUDA runtime/driver call failed */
+#define CP_ERR_DEVICE_TIMEOUT -5  /* a bounded device-side wait ran out (from cp_get_status) */
+#define CP_ERR_DEVICE_BOUNDS  -6  /* a device-side index check failed (from cp_get_status) */
+#define CP_ERR_WORKSPACE      -7  /* workspace pointer null or smaller than cp_workspace_size() */
+#define CP_ERR_ARCH           -8  /* the current device is not sm_103 */
+
+/* Token layouts of a ring rank's shard ([MTX] "Split heads or rotate KV",
+ * [L3P] "Long context changes more than attention cost"). */
+#define CP_LAYOUT_CONTIGUOUS 0    /* ring rank r holds positions [r*L/R, (r+1)*L/R) */
+#define CP_LAYOUT_ZIGZAG     1    /* 2R chunks of c = L/(2R); rank r holds chunk r then chunk 2R-1-r */
+
+/* Reshard directions and tensor kinds for ulysses_reshard(). */
+#define CP_SEQ_TO_HEAD 0
+#define CP_HEAD_TO_SEQ 1
+#define CP_TOKEN_MAJOR 0          /* [tokens][H][row_elems]       (Q, K, V, O) */
+#define CP_HEAD_MAJOR  1          /* [H][tokens], row_elems == 1  (LSE)        */
+
+/* Operations for cp_workspace_size(). */
+#define CP_OP_FWD 0
+#define CP_OP_BWD 1
+
+/* Plan description (host struct; copied by cp_plan_create). */
+typedef struct {
+  int32_t version;            /* CP_ATTN_PLAN_VERSION (a versioned plan: [L3P] "The parallel plan is a per-job contract") */
+  int32_t L;                  /* global tokens (batch 1) */
+  int32_t Hq, Hkv;            /* query heads, KV heads; Hkv divides Hq (GQA) */
+  int32_t d;                  /* head dimension: 64 or 128 */
+  int32_t ulysses_degree;     /* U >= 1; U divides Hkv ([MTX] "Split heads or rotate KV": KV heads cap A2A) */
+  int32_t ring_degree;        /* R >= 1; P = U*R emulated ranks */
+  int32_t layout;             /* CP_LAYOUT_*; R divides L (contiguous) or 2R divides L (zigzag); U divides L/R */
+  int32_t causal;             /* must be 1 (causal attention; [MTX] "Why KV comes back together") */
+  int32_t num_docs;           /* 0 or 1: one document; >1: packed documents */
+  const int32_t *doc_offsets; /* host; num_docs+1 entries, [0]=0, strictly increasing, [num_docs]=L; copied */
+  float softmax_scale;        /* 0 => 1/sqrt(d) */
+  int32_t emit_partials;      /* 1 => the forward writes one normalised (O, LSE) partial per ring step
+                                 into the workspace and merges them in ring order with the same
+                                 kernel as cp_merge_lse(); 0 => the merge is fused (online softmax
+                                 continued across ring steps).  Requires U == 1. */
+} cp_plan_desc_t;
+
+typedef struct cp_plan cp_plan_t;   /* opaque; immutable after creation; usable from any stream */
+
+/* Validate `desc` and build the plan on the current device: the work list
+ * (query tiles ordered by descending visible-tile count, [L3P] "balance by
+ * actual attention work") and, with documents, a per-position document-start
+ * table.  Allocates those device tables with cudaMalloc; they are freed by
+ * cp_plan_destroy().  *out is set only on success. */
+int cp_plan_create(const cp_plan_desc_t *desc, cp_plan_t **out);
+void cp_plan_destroy(cp_plan_t *plan);
+
+/* host_out[L]: global position of every slot of the sequence-sharded layout,
+ * rank-major (rank g = r*U + u; member u of ring rank r holds ring-local slots
+ * [u*n, (u+1)*n) of ring rank r's shard).  Host memory, caller-owned. */
+int cp_index_map(const cp_plan_t *plan, int32_t *host_out);
+
+/* Bytes of device workspace cp_attn_fwd (op CP_OP_FWD) or cp_attn_bwd
+ * (CP_OP_BWD) needs for this plan. */
+int cp_workspace_size(const cp_plan_t *plan, int op, size_t *bytes);
+
+/* Ulysses all-to-all of all R groups at once ([MTX] "Split heads or rotate
+ * KV", [ULY] "Current state"), as an in-memory permutation copy:
+ *   CP_TOKEN_MAJOR, CP_SEQ_TO_HEAD:
+ *     in  [R][U][n][H][E]  ->  out [R][U][U*n][H/U][E],
+ *     out[r][u][s*n+t][h'] = in[r][s][t][u*H/U + h']
+ *   CP_HEAD_MAJOR, CP_SEQ_TO_HEAD (E == 1):
+ *     in  [R][U][H][n]     ->  out [R][U][H/U][U*n]
+ *   CP_HEAD_TO_SEQ: the inverse maps.
+ * n = L/(R*U) from the plan; H is the tensor's head count (U divides H);
+ * E = row_elems elements of elem_bytes each.  in and out must not overlap.
+ * Bit-exact (a copy).  16-byte vectors when H/U*E*elem_bytes (token-major)
+ * or n*elem_bytes (head-major) is a multiple of 16, 4-byte words otherwise
+ * (elem_bytes*E must then be a multiple of 4). */
+int ulysses_reshard(const cp_plan_t *plan, int direction, int tensor_kind, int H,
+                    int row_elems, int elem_bytes, const void *in, void *out,
+                    cudaStream_t stream);
+
+/* Causal CP attention forward for all P emulated ranks.
+ *   q  [P][n][Hq][d]  bf16, sequence-sharded (slot order of cp_index_map)
+ *   k,v[P][n][Hkv][d] bf16
+ *   o  [P][n][Hq][d]  bf16 out
+ *   lse[P][Hq][n]     fp32 out (natural log; -inf for a row with no visible key)
+ * With U > 1 the call reshards Q, K, V to head-sharded layout in the
+ * workspace, runs ring attention per head group and reshards O and LSE back
+ * ([MTX] "Split heads or rotate KV": the two exchanges around attention).
+ * Per ring rank r and step s the visiting chunk comes from rank (r-s) mod R;
+ * tiles with no visible pair are skipped, partially visible tiles are masked.
+ * workspace: cp_workspace_size(plan, CP_OP_FWD) bytes (may be NULL when 0). */
+int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void *v,
+                void *o, float *lse, void *workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+
+/* The attention between the two Ulysses exchanges: ring attention of every
+ * attention rank (ring rank r, Ulysses member u) on head-sharded inputs, the
+ * layout ulysses_reshard(CP_SEQ_TO_HEAD) produces ([MTX] "Split heads or
+ * rotate KV": each chip computes its heads over the whole group sequence;
+ * the ring runs over r for each head group u).
+ *   q  [R][U][T][Hq/U][d] bf16,  k, v [R][U][T][Hkv/U][d] bf16, T = L/R
+ *   o  [R][U][T][Hq/U][d] bf16 out,  lse [R][U][Hq/U][T] fp32 out
+ * With U == 1 this is cp_attn_fwd with the fused merge.  No workspace. */
+int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const void *v,
+                      void *o, float *lse, cudaStream_t stream);
+
+/* Causal CP attention backward (U == 1) from the forward's O and LSE
+ * (activation recompute, [L3P] "Long context changes more than attention
+ * cost"): with P = exp(scale*QK^T - LSE),
+ *   D = rowsum(dO * O); dV = P^T dO; dS = P * (dO V^T - D);
+ *   dQ = scale dS K;  dK = scale dS^T Q;  query heads sum into their KV head.
+ * q, o, dO [P][n][Hq][d] bf16; k, v [P][n][Hkv][d] bf16; lse [P][Hq][n] fp32;
+ * dq [P][n][Hq][d], dk, dv [P][n][Hkv][d] fp32 out (overwritten).
+ * Gradients of a KV chunk land on the rank that owns the chunk.
+ * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes. */
+int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void *v,
+                const void *o, const float *lse, const void *dO,
+                float *dq, float *dk, float *dv, void *workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+
+/* Merge n_parts normalised attention partials over disjoint key sets
+ * ([MTX] "Split heads or rotate KV": partial computation and merge):
+ *   o_parts   [n_parts][rows][H][d] fp32, lse_parts [n_parts][H][rows] fp32
+ *   o_out     [rows][H][d] bf16,          lse_out   [H][rows] fp32
+ *   lse = m + ln(sum_p exp(lse_p - m)), m = max_p lse_p;
+ *   o   = sum_p exp(lse_p - lse) o_p;   all parts -inf => o = 0, lse = -inf.
+ * Parts are folded in index order.  d in {64, 128}. */
+int cp_merge_lse(int n_parts, int rows, int H, int d, const float *o_parts,
+                 const float *lse_parts, void *o_out, float *lse_out, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the device status word:
+ * *dev_code = 0 or the first CP_ERR_DEVICE_* code any kernel recorded since
+ * the last call.  Returns CP_OK or CP_ERR_CUDA. */
+int cp_get_status(cudaStream_t stream, int32_t *dev_code);
+
+/* Static string for a return code. */
+const char *cp_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CP_ATTN_H */

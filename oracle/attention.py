@@ -93,18 +93,25 @@ def _scale_of(d, scale):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
 
-def attention_rows(q, k, v, rows=None, q_pos=None, k_pos=None, offsets=None,
-                   causal=True, scale=None, row_block=256):
-    """O and LSE of the query rows ``rows`` (default: all).
+def _f64(x):
+    """fp64 numpy copy of an array or a (CPU) torch tensor (exact for bf16/fp32)."""
+    if hasattr(x, "detach"):
+        import torch
+        return x.detach().to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
 
-    q [nq, Hq, d], k, v [nk, Hkv, d] (any float type, evaluated in fp64);
-    q_pos / k_pos give each row's global position (default 0..n-1).
-    Returns O [len(rows), Hq, d] float64 and LSE [Hq, len(rows)] float64.
-    A row with no visible key yields O = 0, LSE = -inf.
+
+def attention_rows(q, k, v, rows=None, q_pos=None, k_pos=None, offsets=None,
+                   causal=True, scale=None, heads=None):
+    """O and LSE of the query rows ``rows`` (default: all) for ``heads``
+    (default: all query heads).
+
+    q [nq, Hq, d], k, v [nk, Hkv, d] (numpy arrays or CPU torch tensors of
+    any float type, evaluated in fp64); q_pos / k_pos give each row's global
+    position (default 0..n-1).  Returns O [len(rows), len(heads), d] float64
+    and LSE [len(heads), len(rows)] float64.  A row with no visible key
+    yields O = 0, LSE = -inf.
     """
-    q = np.asarray(q, dtype=np.float64)
-    k = np.asarray(k, dtype=np.float64)
-    v = np.asarray(v, dtype=np.float64)
     nq, Hq, d = q.shape
     nk, Hkv, _ = k.shape
     if Hq % Hkv:
@@ -112,25 +119,33 @@ def attention_rows(q, k, v, rows=None, q_pos=None, k_pos=None, offsets=None,
     G = Hq // Hkv
     sc = _scale_of(d, scale)
     rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    heads = list(range(Hq)) if heads is None else [int(h) for h in heads]
     q_pos = np.arange(nq) if q_pos is None else np.asarray(q_pos, dtype=np.int64)
     k_pos = np.arange(nk) if k_pos is None else np.asarray(k_pos, dtype=np.int64)
-    O = np.zeros((len(rows), Hq, d))
-    LSE = np.full((Hq, len(rows)), NEG_INF)
-    for b0 in range(0, len(rows), row_block):
-        rb = rows[b0:b0 + row_block]
-        M = visible(q_pos[rb], k_pos, offsets, causal)          # [nb, nk]
-        any_vis = M.any(axis=1)
-        for h in range(Hq):
-            j = h // G                                          # GQA: KV head of query head h
-            S = sc * (q[rb, h, :] @ k[:, j, :].T)               # [nb, nk]
+    # Memory bound: a block of rows times all keys stays near 2^24 scores.
+    row_block = max(1, min(256, (1 << 24) // max(nk, 1)))
+    O = np.zeros((len(rows), len(heads), d))
+    LSE = np.full((len(heads), len(rows)), NEG_INF)
+    kv_cache = {}
+    for hi, h in enumerate(heads):
+        j = h // G                                              # GQA: KV head of query head h
+        if j not in kv_cache:
+            kv_cache.clear()
+            kv_cache[j] = (_f64(k[:, j, :]), _f64(v[:, j, :]))
+        Kj, Vj = kv_cache[j]
+        for b0 in range(0, len(rows), row_block):
+            rb = rows[b0:b0 + row_block]
+            M = visible(q_pos[rb], k_pos, offsets, causal)      # [nb, nk]
+            any_vis = M.any(axis=1)
+            S = sc * (_f64(q[rb, h, :]) @ Kj.T)                 # [nb, nk]
             S = np.where(M, S, NEG_INF)
             m = np.where(any_vis, S.max(axis=1), 0.0)
             with np.errstate(divide="ignore"):
                 lse = m + np.log(np.exp(S - m[:, None]).sum(axis=1))
             P = np.exp(S - np.where(any_vis, lse, 0.0)[:, None])
             P[~any_vis] = 0.0
-            O[b0:b0 + len(rb), h, :] = P @ v[:, j, :]
-            LSE[h, b0:b0 + len(rb)] = np.where(any_vis, lse, NEG_INF)
+            O[b0:b0 + len(rb), hi, :] = P @ Vj
+            LSE[hi, b0:b0 + len(rb)] = np.where(any_vis, lse, NEG_INF)
     return O, LSE
 
 

@@ -1,0 +1,59 @@
+"""GPU-side helpers for the parity tests: arrange global-order inputs into the
+sequence-sharded layout with the plan's index map, call the C ABI, and map
+the outputs back to global order.  (Input arrangement and comparison only.)"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import context_long_sequence_gb300 as cpa
+
+O_MAX_ABS = 1e-2    # O: max-abs error bound
+O_MEAN_ABS = 1e-3   # O: mean-abs error bound
+LSE_MAX_ABS = 1e-3  # LSE: max-abs error bound
+
+
+def to_slots(x_global: torch.Tensor, idx: torch.Tensor) -> torch.Tensor:
+    return x_global[idx].contiguous()
+
+
+def fwd(plan: cpa.Plan, q_g, k_g, v_g, device="cuda"):
+    """Run cp_attn_fwd on global-order CPU inputs; return global-order O
+    (float32 [L,Hq,d]) and LSE (float32 [Hq,L]) on the CPU."""
+    idx = torch.from_numpy(plan.index_map().astype(np.int64))
+    q = to_slots(q_g, idx).to(device)
+    k = to_slots(k_g, idx).to(device)
+    v = to_slots(v_g, idx).to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty(plan.P, plan.Hq, plan.n, dtype=torch.float32, device=device)
+    ws = cpa.alloc_workspace(plan)
+    cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws)
+    assert cpa.cp_get_status() == 0
+    return from_slots(plan, o, lse, idx)
+
+
+def from_slots(plan, o, lse, idx):
+    L = plan.L
+    O = torch.empty(L, plan.Hq, plan.d, dtype=torch.float32)
+    O[idx] = o.float().cpu()
+    lse_slots = lse.permute(1, 0, 2).reshape(plan.Hq, L).cpu()
+    LSE = torch.empty(plan.Hq, L, dtype=torch.float32)
+    LSE[:, idx] = lse_slots
+    return O, LSE
+
+
+def errors(O, LSE, O_ref, LSE_ref):
+    O = np.asarray(O, dtype=np.float64)
+    LSE = np.asarray(LSE, dtype=np.float64)
+    eo = np.abs(O - O_ref)
+    fin = np.isfinite(LSE_ref)
+    assert np.array_equal(np.isfinite(LSE), fin), "LSE -inf pattern differs"
+    el = np.abs(LSE[fin] - LSE_ref[fin]) if fin.any() else np.zeros(1)
+    return float(eo.max()), float(eo.mean()), float(el.max())
+
+
+def assert_close(O, LSE, O_ref, LSE_ref, what=""):
+    mx, mean, lmx = errors(O, LSE, O_ref, LSE_ref)
+    assert mx <= O_MAX_ABS and mean <= O_MEAN_ABS and lmx <= LSE_MAX_ABS, \
+        f"{what}: O max {mx:.3e} mean {mean:.3e}, LSE max {lmx:.3e}"
+    return mx, mean, lmx

@@ -1,0 +1,85 @@
+"""Host-side checks of the C ABI that need no GPU: every symbol the header
+declares is exported, plan validation returns the documented codes, the
+index map matches the oracle's, and workspace sizes follow their formula."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cpa():
+    lib = os.path.join(ROOT, "context_long_sequence_gb300", "libcpattn.so")
+    if not os.path.exists(lib):
+        from context_long_sequence_gb300 import build as b
+        b.build()
+    import context_long_sequence_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "cp_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_symbols_exported(cpa):
+    names = declared_functions()
+    assert "cp_attn_fwd" in names and "ulysses_reshard" in names and "cp_merge_lse" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", cpa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    assert sorted(names) == sorted(cpa.EXPORTED)
+    for n in names:
+        getattr(cpa._L(), n)
+
+
+@pytest.mark.parametrize("L,R,U,layout", [(64, 4, 1, 0), (64, 4, 1, 1), (96, 3, 2, 1), (128, 2, 4, 1),
+                                          (1024, 8, 1, 1), (48, 1, 1, 1), (2048, 8, 4, 1)])
+def test_index_map_matches_oracle(cpa, L, R, U, layout):
+    import oracle
+    p = cpa.Plan(L, 8, 4, 64, ulysses_degree=U, ring_degree=R, layout=layout)
+    assert np.array_equal(p.index_map(), oracle.ring_positions(L, R, layout))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(L=100, Hq=8, Hkv=4, d=64, ring_degree=3), -1),                 # R does not divide L
+    (dict(L=96, Hq=8, Hkv=3, d=64), -1),                                 # Hkv does not divide Hq
+    (dict(L=96, Hq=8, Hkv=4, d=96), -2),                                 # head dim not built
+    (dict(L=96, Hq=8, Hkv=4, d=64, ulysses_degree=8), -2),               # U must divide Hkv
+    (dict(L=96, Hq=8, Hkv=4, d=64, causal=False), -2),
+    (dict(L=96, Hq=8, Hkv=4, d=64, ulysses_degree=2, emit_partials=True), -2),
+    (dict(L=96, Hq=8, Hkv=4, d=64, doc_offsets=[0, 50, 40, 96]), -1),    # not increasing
+    (dict(L=96, Hq=8, Hkv=4, d=64, doc_offsets=[0, 50, 95]), -1),        # does not end at L
+    (dict(L=90, Hq=8, Hkv=4, d=64, ring_degree=4, layout=1), -1),        # 2R does not divide L
+    (dict(L=96, Hq=8, Hkv=4, d=64, ulysses_degree=4, ring_degree=5), -1),
+])
+def test_plan_validation(cpa, kw, code):
+    with pytest.raises(cpa.CPError) as e:
+        cpa.Plan(**kw)
+    assert e.value.code == code
+
+
+def test_workspace_sizes(cpa):
+    def al(x):
+        return (x + 255) // 256 * 256
+    p = cpa.Plan(16384, 32, 8, 128, ulysses_degree=4)
+    L = 16384
+    assert p.workspace_size(cpa.CP_OP_FWD) == al(L * 32 * 256) * 2 + al(L * 8 * 256) * 2 + al(L * 32 * 4)
+    assert p.workspace_size(cpa.CP_OP_BWD) == al(L * 32 * 4)
+    p = cpa.Plan(1024, 4, 4, 64, ring_degree=4, emit_partials=True)
+    assert p.workspace_size(cpa.CP_OP_FWD) == al(4 * 1024 * 4 * 64 * 4) + al(4 * 1024 * 4 * 4)
+    p = cpa.Plan(1024, 4, 4, 64, ring_degree=4)
+    assert p.workspace_size(cpa.CP_OP_FWD) == 0
+
+
+def test_strerror(cpa):
+    assert cpa.cp_strerror(0) == "ok"
+    assert "align" in cpa.cp_strerror(cpa.CP_ERR_ALIGNMENT)
+    assert cpa.cp_strerror(12345) == "unknown error"

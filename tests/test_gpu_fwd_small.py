@@ -1,0 +1,133 @@
+"""GPU parity of the forward path against the CPU oracle, element by element,
+at sizes the oracle finishes in seconds (several 128-row tiles, ragged tails,
+documents whose boundaries fall inside tiles, GQA, Ulysses, USP and the
+emit-partials + merge path), plus reshard and merge bit-exactness and
+run-to-run determinism."""
+import os
+import sys
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(__file__))
+
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def cpa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import context_long_sequence_gb300 as m
+    return m
+
+
+def _inputs(L, Hq, Hkv, d, seed):
+    return workloads.make_inputs(L, Hq, Hkv, d, seed)
+
+
+CASES = [
+    # name, L, Hq, Hkv, d, U, R, layout, docs, emit_partials
+    ("cfg1_ring_L1K_P4_partials", 1024, 4, 4, 64, 1, 4, 0, None, True),
+    ("ring_gqa_zigzag_d128", 1536, 8, 2, 128, 1, 3, 1, None, False),
+    ("ragged_chunks_d128", 1000, 4, 2, 128, 1, 2, 1, None, False),
+    ("docs_inside_tiles", 2048, 4, 1, 128, 1, 2, 1, [0, 300, 301, 1100, 2048], False),
+    ("usp_docs", 2048, 8, 4, 128, 2, 2, 1, [0, 777, 2048], False),
+    ("ulysses_d64", 1024, 8, 4, 64, 4, 1, 0, None, False),
+    ("partials_docs_d64", 768, 4, 2, 64, 1, 2, 1, [0, 100, 500, 768], True),
+    ("single_ragged_tile", 72, 2, 1, 128, 1, 1, 0, None, False),
+    ("partials_ragged_d128", 600, 4, 4, 128, 1, 3, 0, None, True),
+    ("contig_ring_R5_docs", 1280, 4, 2, 64, 1, 5, 0, [0, 5, 6, 640, 1279, 1280], False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fwd_matches_oracle(cpa, case):
+    import gpu_harness as gh
+    name, L, Hq, Hkv, d, U, R, layout, docs, partials = case
+    inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(name.encode()) % 1000)
+    plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=layout, doc_offsets=docs,
+                    emit_partials=partials)
+    O, LSE = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
+    O_ref, LSE_ref = oracle.attention(inp["q"], inp["k"], inp["v"], offsets=docs)
+    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name)
+
+
+def test_fwd_deterministic(cpa):
+    import gpu_harness as gh
+    inp = _inputs(1536, 8, 2, 128, seed=7)
+    plan = cpa.Plan(1536, 8, 2, 128, ring_degree=3, layout=1, doc_offsets=[0, 700, 1536])
+    a = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
+    b = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_partials_equal_fused(cpa):
+    """Emit-partials + standalone merge equals the fused ring merge within tolerance."""
+    import gpu_harness as gh
+    inp = _inputs(1024, 4, 4, 64, seed=11)
+    pa = cpa.Plan(1024, 4, 4, 64, ring_degree=4, emit_partials=True)
+    pf = cpa.Plan(1024, 4, 4, 64, ring_degree=4, emit_partials=False)
+    oa, la = gh.fwd(pa, inp["q"], inp["k"], inp["v"])
+    of, lf = gh.fwd(pf, inp["q"], inp["k"], inp["v"])
+    assert (oa - of).abs().max().item() <= 1e-2
+    assert (la - lf).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("R,U,n,H,E,eb", [(2, 4, 48, 8, 128, 2), (1, 4, 64, 32, 64, 2), (3, 2, 10, 4, 3, 4),
+                                         (2, 2, 7, 6, 1, 4)])
+def test_reshard_bit_exact(cpa, R, U, n, H, E, eb):
+    L = R * U * n
+    plan = cpa.Plan(L, 8, 8, 64, ulysses_degree=U if 8 % U == 0 else 1, ring_degree=R)
+    if plan.U != U:
+        pytest.skip("plan shape")
+    g = torch.Generator().manual_seed(R * 100 + U)
+    dt = torch.int16 if eb == 2 else torch.int32
+    x = torch.randint(-30000, 30000, (R, U, n, H, E), generator=g).to(dt)
+    xd = x.cuda()
+    y = torch.empty(R, U, U * n, H // U, E, dtype=dt, device="cuda")
+    cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, H, E, eb, xd, y)
+    ref = np.stack([oracle.ulysses_seq_to_head(x[r].numpy(), U) for r in range(R)])
+    assert np.array_equal(y.cpu().numpy(), ref)
+    back = torch.empty_like(xd)
+    cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, H, E, eb, y, back)
+    assert torch.equal(back, xd)
+    # head-major (LSE) direction
+    lse = torch.randn(R, U, H, n, generator=g)
+    lh = torch.empty(R, U, H // U, U * n, device="cuda")
+    cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_HEAD_MAJOR, H, 1, 4, lse.cuda(), lh)
+    lb = torch.empty(R, U, H, n, device="cuda")
+    cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, H, 1, 4, lh, lb)
+    assert torch.equal(lb.cpu(), lse)
+    ref_l = np.stack([oracle.ulysses_lse_head_to_seq(lh[r].cpu().numpy(), U) for r in range(R)])
+    assert np.array_equal(ref_l, lse.numpy())
+
+
+@pytest.mark.parametrize("n_parts,rows,H,d", [(4, 256, 4, 64), (3, 77, 2, 128), (1, 5, 3, 64), (8, 130, 1, 128)])
+def test_merge_matches_oracle(cpa, n_parts, rows, H, d):
+    g = torch.Generator().manual_seed(n_parts * 7 + rows)
+    o = torch.randn(n_parts, rows, H, d, generator=g)
+    lse = torch.randn(n_parts, H, rows, generator=g) * 4
+    lse[0, :, ::3] = -float("inf")
+    lse[:, 0, 1] = -float("inf")          # a row with every part empty
+    o[lse.permute(0, 2, 1)[..., None].expand_as(o) == -float("inf")] = 0.0
+    oo = torch.empty(rows, H, d, dtype=torch.bfloat16, device="cuda")
+    lo = torch.empty(H, rows, device="cuda")
+    cpa.cp_merge_lse(n_parts, rows, H, d, o.cuda(), lse.cuda(), oo, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.merge([(o[p].numpy(), lse[p].numpy()) for p in range(n_parts)])
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(lo.cpu().numpy()), fin)
+    assert np.abs(lo.cpu().numpy()[fin] - ref_l[fin]).max() <= 1e-5
+    # The merged O is rounded once to bf16 (8 significant bits: unit roundoff
+    # 2^-8 with round-to-nearest-even); the fp32 arithmetic before it adds
+    # ~1e-6.  Random parts reach |o| ~ 4, where one bf16 half-ulp alone
+    # exceeds 1e-2, so the bound is relative.
+    err = np.abs(oo.float().cpu().numpy() - ref_o)
+    assert (err <= 2.0 ** -8 * np.abs(ref_o) + 1e-5).all(), err.max()

@@ -13,11 +13,11 @@ from oracle_pins import ALL_PINS  # noqa: E402
 SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "attention.py")
 
 MUTATIONS = {
-    "gqa_index": ("j = h // G                                          # GQA", "j = h % Hkv                                          # GQA"),
+    "gqa_index": ("j = h // G                                              # GQA", "j = h % Hkv                                              # GQA"),
     "causal_strict": ("m &= k_pos <= q_pos", "m &= k_pos < q_pos"),
-    "dropped_scale": ("S = sc * (q[rb, h, :] @ k[:, j, :].T)", "S = (q[rb, h, :] @ k[:, j, :].T)"),
+    "dropped_scale": ("S = sc * (_f64(q[rb, h, :]) @ Kj.T)", "S = (_f64(q[rb, h, :]) @ Kj.T)"),
     "scale_1_over_d": ("1.0 / math.sqrt(d) if scale is None", "1.0 / d if scale is None"),
-    "transposed_pv": ("O[b0:b0 + len(rb), h, :] = P @ v[:, j, :]", "O[b0:b0 + len(rb), h, :] = P @ k[:, j, :]"),
+    "transposed_pv": ("O[b0:b0 + len(rb), hi, :] = P @ Vj", "O[b0:b0 + len(rb), hi, :] = P @ Kj"),
     "merge_weight_index": ("cb = np.where(empty, 0.0, np.exp(lse_b - ls))", "cb = np.where(empty, 0.0, np.exp(lse_a - ls))"),
     "merge_dropped_log": ("lse = np.where(empty, NEG_INF, ms + np.log(wa + wb))", "lse = np.where(empty, NEG_INF, ms + (wa + wb))"),
     "zigzag_chunk": ("(2 * R - 1 - r) * c + np.arange(c)", "(2 * R - 2 - r) * c + np.arange(c)"),
