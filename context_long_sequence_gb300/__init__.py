@@ -27,6 +27,7 @@ CP_ERR_DEVICE_TIMEOUT = -5
 CP_ERR_DEVICE_BOUNDS = -6
 CP_ERR_WORKSPACE = -7
 CP_ERR_ARCH = -8
+CP_NOALLOC_SCRATCH_BYTES = 8 << 20
 CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1
 CP_SEQ_TO_HEAD = 0
@@ -77,6 +78,7 @@ def _L():
     lib.ulysses_reshard.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
     lib.cp_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.cp_attn_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
     lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
@@ -87,7 +89,7 @@ def _L():
 
 
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
-            "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_bwd", "cp_merge_lse", "cp_get_status", "cp_strerror"]
+            "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_noalloc", "cp_attn_bwd", "cp_merge_lse", "cp_get_status", "cp_strerror"]
 
 
 class CPError(RuntimeError):
@@ -196,6 +198,13 @@ def cp_attn_fwd(plan: Plan, q, k, v, o, lse, workspace=None, workspace_bytes=Non
 def cp_attn_fwd_local(plan: Plan, q, k, v, o, lse, stream=None):
     _check(_L().cp_attn_fwd_local(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)),
            "cp_attn_fwd_local")
+
+
+def cp_attn_fwd_noalloc(plan: Plan, q, k, v, o, lse, stream=None):
+    """cp_attn_fwd for an emit-partials plan, with the partials kept in the
+    library's static device scratch instead of an allocated workspace."""
+    _check(_L().cp_attn_fwd_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)),
+           "cp_attn_fwd_noalloc")
 
 
 def cp_attn_bwd(plan: Plan, q, k, v, o, lse, dO, dq, dk, dv, workspace=None, workspace_bytes=None, stream=None):

@@ -467,3 +467,68 @@ const char* cp_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free emit-partials forward (cp_attn_fwd_noalloc).
+//
+// For callers that cannot allocate device memory (see the header): the
+// per-ring-step partials live in this file-scope device array instead of a
+// caller workspace.  Host code may not use the array's name as an address
+// (in host code it is only a stand-in for the symbol), so its device address
+// is resolved once per device with cudaGetSymbolAddress while that device is
+// current, and that address is what the kernels receive.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (set-up on the
+// first call per device; nullptr if it could not be resolved).
+void* noalloc_scratch_addr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_addr[dev] = ptr;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int cp_attn_fwd_noalloc(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o,
+                                   float* lse, cudaStream_t stream) {
+  if (!p || !q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!p->desc.emit_partials || p->desc.ulysses_degree != 1) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return CP_ERR_ALIGNMENT;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const cp_plan_desc_t& d = p->desc;
+  const size_t R = d.ring_degree, L = d.L;
+  const size_t o_bytes = align256(R * L * d.Hq * d.d * 4);
+  const size_t lse_bytes = align256(R * L * d.Hq * 4);
+  if (o_bytes + lse_bytes > CP_NOALLOC_SCRATCH_BYTES) return CP_ERR_WORKSPACE;
+  char* scratch = static_cast<char*>(noalloc_scratch_addr());
+  if (!scratch) return CP_ERR_CUDA;
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = d.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.o_part = reinterpret_cast<float*>(scratch);
+  a.lse_part = reinterpret_cast<float*>(scratch + o_bytes);
+  a.items = p->d_items_steps;
+  a.n_items = p->n_items_steps;
+  rc = cpattn::launch_attn_fwd(a, stream);
+  if (rc != CP_OK) return rc;
+  return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse, stream);
+}

@@ -190,6 +190,35 @@ int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void 
 int cp_merge_lse(int n_parts, int rows, int H, int d, const float *o_parts,
                  const float *lse_parts, void *o_out, float *lse_out, cudaStream_t stream);
 
+/* Allocation-free variant of the emit-partials forward (no counterpart in
+ * the paper: it exists for callers, not for the method).
+ *
+ * Some callers cannot call cudaMalloc at all: a plugin running inside a host
+ * framework that owns the device allocator, a runtime whose device-memory
+ * budget is fixed at start-up, or a latency-critical loop that must not
+ * take cudaMalloc's implicit device synchronisation.  This entry point
+ * computes exactly what cp_attn_fwd computes for a plan created with
+ * emit_partials = 1 (per-ring-step partials, then their merge), but keeps the
+ * partials in a static device array of CP_NOALLOC_SCRATCH_BYTES compiled into
+ * the library instead of a caller-provided workspace, and calls no
+ * allocating function.  The caller still passes q, k, v, o, lse (same
+ * layouts as cp_attn_fwd).
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The first call on a device resolves the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    (different streams, no ordering between them) race on it.  Every
+ *    partial a call reads was written earlier by the same call, so nothing
+ *    needs clearing between calls.
+ *  - Returns CP_ERR_WORKSPACE if the partials need more than
+ *    CP_NOALLOC_SCRATCH_BYTES (R * L * Hq * (d + 1) * 4 bytes, each part
+ *    rounded up to 256), CP_ERR_INVALID_ARG if the plan was not created with
+ *    emit_partials = 1. */
+#define CP_NOALLOC_SCRATCH_BYTES (8u << 20)
+int cp_attn_fwd_noalloc(const cp_plan_t *plan, const void *q, const void *k, const void *v,
+                        void *o, float *lse, cudaStream_t stream);
+
 /* Synchronise `stream`, then read and clear the device status word:
  * *dev_code = 0 or the first CP_ERR_DEVICE_* code any kernel recorded since
  * the last call.  Returns CP_OK or CP_ERR_CUDA. */
