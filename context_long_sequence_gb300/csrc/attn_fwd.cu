@@ -37,6 +37,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace cpattn {
 namespace {
@@ -386,41 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D bf16 map over a [rows][cols] row-major matrix, box 64 cols x 128 rows,
-// 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 int launch_d(const FwdArgs& a, cudaStream_t stream) {
   const AttnGeom& g = a.g;
   const uint64_t rows = static_cast<uint64_t>(g.R) * g.U * g.T;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
-      !make_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, rows) ||
-      !make_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, rows))
+  if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
+      !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, rows) ||
+      !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, rows))
     return CP_ERR_CUDA;
   const uint32_t smem = FwdSmem<D>::kBytes;
   static bool attr_set = false;

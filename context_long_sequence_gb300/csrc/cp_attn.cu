@@ -28,10 +28,13 @@ struct cp_plan {
   bool on_device;
   int device;
   int32_t* d_doc_start;          // [L] or null
+  int32_t* d_doc_end;            // [L] or null
   WorkItem* d_items_fused;
   int n_items_fused;
   WorkItem* d_items_steps;       // emit-partials: one item per (query tile, ring step)
   int n_items_steps;
+  WorkItem* d_items_kv;          // backward: key tiles
+  int n_items_kv;
 };
 
 namespace {
@@ -74,6 +77,7 @@ AttnGeom geom(const cp_plan* p) {
   g.chunk = p->chunk;
   g.scale = p->scale;
   g.doc_start = p->d_doc_start;
+  g.doc_end = p->d_doc_end;
   return g;
 }
 
@@ -123,6 +127,49 @@ std::vector<WorkItem> build_items(const cp_plan* p, bool per_step) {
   std::stable_sort(v.begin(), v.end(), [](const Keyed& x, const Keyed& y) { return x.work > y.work; });
   std::vector<WorkItem> out(v.size());
   for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].it;
+  return out;
+}
+
+int doc_end_host(const cp_plan* p, int pos) {
+  if (p->offsets.empty()) return p->desc.L;
+  return *std::upper_bound(p->offsets.begin(), p->offsets.end(), pos);
+}
+
+// Number of (query tile, query head) steps the backward's key-tile kernel
+// walks for a key tile (the kernel's walk, evaluated on the host).
+int visited_q_tiles(const cp_plan* p, const AttnGeom& g, int src, int k0, int len) {
+  const int kpos0 = cpattn::slot_pos(g, src, k0);
+  const int hi_max = doc_end_host(p, kpos0 + len - 1) - 1;
+  int count = 0;
+  for (int s = 0; s < g.R; ++s) {
+    const int rr = (src + s) % g.R;
+    for (int ch = 0; ch < p->nchunks; ++ch) {
+      const int cpos0 = cpattn::slot_pos(g, rr, ch * g.chunk);
+      const int lo = std::max(cpos0, kpos0);
+      const int hi = std::min(cpos0 + g.chunk - 1, hi_max);
+      if (lo > hi) continue;
+      count += (hi - cpos0) / kTile - (lo - cpos0) / kTile + 1;
+    }
+  }
+  return count;
+}
+
+// Key tiles of every ring rank, ordered by descending work.
+std::vector<WorkItem> build_kv_items(const cp_plan* p) {
+  const AttnGeom g = geom(p);
+  std::vector<std::pair<int, WorkItem>> v;
+  for (int src = 0; src < g.R; ++src)
+    for (int ch = 0; ch < p->nchunks; ++ch)
+      for (int t0 = 0; t0 < p->chunk; t0 += kTile) {
+        const int k0 = ch * p->chunk + t0;
+        const int len = std::min(kTile, p->chunk - t0);
+        v.push_back({visited_q_tiles(p, g, src, k0, len), WorkItem{src, k0, len, -1}});
+      }
+  std::stable_sort(v.begin(), v.end(), [](const std::pair<int, WorkItem>& x, const std::pair<int, WorkItem>& y) {
+    return x.first > y.first;
+  });
+  std::vector<WorkItem> out(v.size());
+  for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].second;
   return out;
 }
 
@@ -224,9 +271,9 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->chunk = T / p->nchunks;
   p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p->on_device = false;
-  p->d_doc_start = nullptr;
-  p->d_items_fused = p->d_items_steps = nullptr;
-  p->n_items_fused = p->n_items_steps = 0;
+  p->d_doc_start = p->d_doc_end = nullptr;
+  p->d_items_fused = p->d_items_steps = p->d_items_kv = nullptr;
+  p->n_items_fused = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
   // maps, workspace sizes -- works without one).
@@ -245,10 +292,14 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     p->device = dev;
     int rc = CP_OK;
     if (!p->offsets.empty()) {
-      std::vector<int32_t> ds(d.L);
+      std::vector<int32_t> ds(d.L), de(d.L);
       for (int i = 0; i < d.num_docs; ++i)
-        for (int x = p->offsets[i]; x < p->offsets[i + 1]; ++x) ds[x] = p->offsets[i];
+        for (int x = p->offsets[i]; x < p->offsets[i + 1]; ++x) {
+          ds[x] = p->offsets[i];
+          de[x] = p->offsets[i + 1];
+        }
       rc = upload(ds, &p->d_doc_start);
+      if (rc == CP_OK) rc = upload(de, &p->d_doc_end);
     }
     std::vector<WorkItem> fused = build_items(p, false);
     p->n_items_fused = static_cast<int>(fused.size());
@@ -258,10 +309,17 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       p->n_items_steps = static_cast<int>(steps.size());
       rc = upload(steps, &p->d_items_steps);
     }
+    if (rc == CP_OK && U == 1) {
+      std::vector<WorkItem> kv = build_kv_items(p);
+      p->n_items_kv = static_cast<int>(kv.size());
+      rc = upload(kv, &p->d_items_kv);
+    }
     if (rc != CP_OK) {
       cudaFree(p->d_doc_start);
+      cudaFree(p->d_doc_end);
       cudaFree(p->d_items_fused);
       cudaFree(p->d_items_steps);
+      cudaFree(p->d_items_kv);
       delete p;
       return rc;
     }
@@ -275,8 +333,10 @@ void cp_plan_destroy(cp_plan_t* p) {
   if (!p) return;
   if (p->on_device) {
     cudaFree(p->d_doc_start);
+    cudaFree(p->d_doc_end);
     cudaFree(p->d_items_fused);
     cudaFree(p->d_items_steps);
+    cudaFree(p->d_items_kv);
   }
   delete p;
 }
@@ -424,8 +484,10 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.dk = dk;
   a.dv = dv;
   a.delta = static_cast<float*>(workspace);
-  a.items = p->d_items_fused;
-  a.n_items = p->n_items_fused;
+  a.items_q = p->d_items_fused;
+  a.n_items_q = p->n_items_fused;
+  a.items_kv = p->d_items_kv;
+  a.n_items_kv = p->n_items_kv;
   a.d = p->desc.d;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;

@@ -24,6 +24,7 @@ struct AttnGeom {
   int chunk;               // contiguous-position chunk length: T or T/2
   float scale;             // softmax scale
   const int32_t* doc_start;  // [L] start of the document holding each position, or null
+  const int32_t* doc_end;    // [L] one past the end of that document, or null
 };
 
 // Global position of slot t of ring rank r.
@@ -50,14 +51,18 @@ struct FwdArgs {
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// Backward (U == 1).  items_q: query tiles (all ring steps), as the forward's
+// fused list; items_kv: key tiles {a = owner rank, q0 = first slot, len, -1}.
 struct BwdArgs {
   AttnGeom g;
   const void* q;  const void* k;  const void* v;
   const void* o;  const float* lse;  const void* dO;
   float* dq;  float* dk;  float* dv;
   float* delta;   // [R][Hq][T] workspace: rowsum(dO * O)
-  const WorkItem* items;   // fused-mode work list (all ring steps)
-  int n_items;
+  const WorkItem* items_q;
+  int n_items_q;
+  const WorkItem* items_kv;
+  int n_items_kv;
   int d;
   int32_t* status;
 };

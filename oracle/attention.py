@@ -195,6 +195,62 @@ def attention_bwd(q, k, v, do, offsets=None, causal=True, scale=None):
     return O, LSE, dq, dk, dv
 
 
+def attention_bwd_rows(q, k, v, do, q_rows=(), key_rows=(), offsets=None, causal=True, scale=None,
+                       q_heads=None, kv_heads=None):
+    """Selected gradient rows, fp64, from the same definition as
+    attention_bwd: dQ at query rows ``q_rows`` for ``q_heads`` and dK, dV at
+    key rows ``key_rows`` for ``kv_heads`` (global order, positions 0..L-1).
+
+    Each needed query row's O and LSE come from attention_rows; then, per
+    query head h and KV head j = floor(h/G), with P = exp(S - LSE) over the
+    visible pairs, dP = dO V^T, D = rowsum(dO * O), dS = P (dP - D):
+    dQ_i = scale sum_k dS_ik K_k,  dV_k = sum_h sum_i P_ik dO_i,
+    dK_k = scale sum_h sum_i dS_ik Q_i.  The queries that see a key are
+    all later positions of its document, so key rows near a document's end
+    are cheap.  Returns (dq [nq, len(q_heads), d], dk, dv [nk, len(kv_heads), d]).
+    """
+    L, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    sc = _scale_of(d, scale)
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    key_rows = np.asarray(key_rows, dtype=np.int64)
+    q_heads = list(range(Hq)) if q_heads is None else [int(h) for h in q_heads]
+    kv_heads = list(range(Hkv)) if kv_heads is None else [int(j) for j in kv_heads]
+    dq = np.zeros((len(q_rows), len(q_heads), d))
+    dk = np.zeros((len(key_rows), len(kv_heads), d))
+    dv = np.zeros((len(key_rows), len(kv_heads), d))
+    all_pos = np.arange(L)
+
+    def row_terms(rows, h):
+        """P, dS over all keys for query rows `rows` of head h."""
+        j = h // G
+        O, LSE = attention_rows(q, k, v, rows=rows, offsets=offsets, causal=causal, scale=scale, heads=[h])
+        Kj, Vj = _f64(k[:, j, :]), _f64(v[:, j, :])
+        Qr, dOr = _f64(q[rows, h, :]), _f64(do[rows, h, :])
+        M = visible(rows, all_pos, offsets, causal)
+        S = sc * (Qr @ Kj.T)
+        P = np.where(M, np.exp(S - LSE[0][:, None]), 0.0)
+        dP = dOr @ Vj.T
+        D = (dOr * O[:, 0, :]).sum(axis=1)
+        dS = P * (dP - D[:, None])
+        return P, dS, Qr, dOr, Kj
+
+    if len(q_rows):
+        for hi, h in enumerate(q_heads):
+            _, dS, _, _, Kj = row_terms(q_rows, h)
+            dq[:, hi, :] = sc * (dS @ Kj)
+    if len(key_rows):
+        vis = visible(all_pos, key_rows, offsets, causal)          # [L, nk]: query sees key
+        need = np.nonzero(vis.any(axis=1))[0]
+        for ji, j in enumerate(kv_heads):
+            for h in range(j * G, (j + 1) * G):
+                P, dS, Qr, dOr, _ = row_terms(need, h)
+                dv[:, ji, :] += P[:, key_rows].T @ dOr
+                dk[:, ji, :] += sc * (dS[:, key_rows].T @ Qr)
+    return dq, dk, dv
+
+
 # --------------------------------------------------------------------------
 # Context-parallel restatement: index maps, merge, reshard, ring, USP
 # --------------------------------------------------------------------------

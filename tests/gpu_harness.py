@@ -57,3 +57,50 @@ def assert_close(O, LSE, O_ref, LSE_ref, what=""):
     assert mx <= O_MAX_ABS and mean <= O_MEAN_ABS and lmx <= LSE_MAX_ABS, \
         f"{what}: O max {mx:.3e} mean {mean:.3e}, LSE max {lmx:.3e}"
     return mx, mean, lmx
+
+
+def grad_tolerance(ref: np.ndarray):
+    """Gradient bounds (the workload spec gives none; derivation in the design doc).
+
+    dV = P^T dO, dK = scale dS^T Q and dQ = scale dS K are unnormalised sums
+    whose operands P and dS are rounded to bf16 (unit roundoff 2^-8) before
+    the tensor-core products, so the error grows with the tensor's own
+    magnitude: max-abs <= 1e-2 * max(1, max|ref|) and
+    mean-abs <= 1e-3 * max(1, RMS(ref))."""
+    rms = float(np.sqrt(np.mean(np.square(ref))))
+    return 1e-2 * max(1.0, float(np.abs(ref).max())), 1e-3 * max(1.0, rms)
+
+
+def bwd(plan: cpa.Plan, q_g, k_g, v_g, do_g, device="cuda"):
+    """Forward then backward through the C ABI on global-order CPU inputs;
+    returns global-order (dQ, dK, dV) float32 CPU tensors and the GPU's O, LSE."""
+    idx = torch.from_numpy(plan.index_map().astype(np.int64))
+    q = to_slots(q_g, idx).to(device)
+    k = to_slots(k_g, idx).to(device)
+    v = to_slots(v_g, idx).to(device)
+    do = to_slots(do_g, idx).to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty(plan.P, plan.Hq, plan.n, dtype=torch.float32, device=device)
+    cpa.cp_attn_fwd(plan, q, k, v, o, lse, cpa.alloc_workspace(plan))
+    dq = torch.empty(q.shape, dtype=torch.float32, device=device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=device)
+    cpa.cp_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, cpa.alloc_workspace(plan, cpa.CP_OP_BWD))
+    assert cpa.cp_get_status() == 0
+    out = []
+    for t in (dq, dk, dv):
+        g = torch.empty(t.shape, dtype=torch.float32)
+        g[idx] = t.cpu()
+        out.append(g)
+    return out
+
+
+def assert_grads_close(got, ref, what=""):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = np.asarray(g, dtype=np.float64)
+        e = np.abs(g - r)
+        mx_tol, mean_tol = grad_tolerance(r)
+        at = np.unravel_index(np.argmax(e), e.shape)
+        assert e.max() <= mx_tol and e.mean() <= mean_tol, \
+            (f"{what} {name}: max {e.max():.3e} (tol {mx_tol:.1e}) at {at} ref {r[at]:.4f}, "
+             f"max|ref| {np.abs(r).max():.3f}, mean {e.mean():.3e} (tol {mean_tol:.1e})")

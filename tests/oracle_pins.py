@@ -330,3 +330,29 @@ def pin_backward_autograd(orc):
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+def pin_backward_rows_autograd(orc):
+    """Selected gradient rows against torch autograd (fp64 SDPA, explicit mask)."""
+    L, Hq, Hkv, d = 23, 4, 2, 8
+    offs = [0, 10, 23]
+    q, k, v = _rand((L, Hq, d), 34), _rand((L, Hkv, d), 35), _rand((L, Hkv, d), 36)
+    do = _rand((L, Hq, d), 37)
+    G = Hq // Hkv
+    qt = torch.from_numpy(q).requires_grad_()
+    kt = torch.from_numpy(k).requires_grad_()
+    vt = torch.from_numpy(v).requires_grad_()
+    m = torch.from_numpy(_explicit_mask(L, offs))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt.permute(1, 0, 2)[None], kt.repeat_interleave(G, 1).permute(1, 0, 2)[None],
+        vt.repeat_interleave(G, 1).permute(1, 0, 2)[None], attn_mask=m, scale=1 / math.sqrt(d))
+    (o[0].permute(1, 0, 2) * torch.from_numpy(do)).sum().backward()
+    qr, kr = [0, 5, 9, 10, 22], [0, 3, 9, 12, 21, 22]
+    dq, dk, dv = orc.attention_bwd_rows(q, k, v, do, q_rows=qr, key_rows=kr, offsets=offs, q_heads=[1, 3],
+                                        kv_heads=[1])
+    np.testing.assert_allclose(dq, qt.grad.numpy()[qr][:, [1, 3]], rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, kt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, vt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -23,7 +23,9 @@ MUTATIONS = {
     "zigzag_chunk": ("(2 * R - 1 - r) * c + np.arange(c)", "(2 * R - 2 - r) * c + np.arange(c)"),
     "reshard_transposed": ("y[u, s * n:(s + 1) * n] = x[s, :, u * Hl:(u + 1) * Hl]", "y[u, s * n:(s + 1) * n] = x[u, :, s * Hl:(s + 1) * Hl]"),
     "doc_boundary": ('idx = np.searchsorted(offsets, pos, side="right") - 1', 'idx = np.searchsorted(offsets, pos, side="left") - 1'),
-    "bwd_sign": ("dS = P * (dP - D[:, None])", "dS = P * (dP + D[:, None])"),
+    "bwd_sign": ("dS = P * (dP - D[:, None])\n        dq[:, h, :]", "dS = P * (dP + D[:, None])\n        dq[:, h, :]"),
+    "bwd_rows_sign": ("dS = P * (dP - D[:, None])\n        return", "dS = P * (dP + D[:, None])\n        return"),
+    "bwd_rows_dv_operand": ("dv[:, ji, :] += P[:, key_rows].T @ dOr", "dv[:, ji, :] += P[:, key_rows].T @ Qr"),
     "bwd_gqa_overwrite": ("dk[:, j, :] += sc * (dS.T @ q[:, h, :])", "dk[:, j, :] = sc * (dS.T @ q[:, h, :])"),
     "bwd_dropped_scale": ("dq[:, h, :] = sc * (dS @ k[:, j, :])", "dq[:, h, :] = (dS @ k[:, j, :])"),
     "lse_reshard_back": ("out[s, u * Hl:(u + 1) * Hl, :] = lse[u, :, s * n:(s + 1) * n]", "out[s, u * Hl:(u + 1) * Hl, :] = lse[s, :, u * n:(u + 1) * n]"),
