@@ -174,6 +174,21 @@ def cpu_inputs(w, device_inputs=None):
     return workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device="cpu", k_scale=w.k_scale)
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (the job is as slow as its
+    slowest replica).  The only collective besides the barriers."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_value(flops_per_step_per_rank: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job useful TFLOP/s: every rank's work over the slowest rank's time."""
+    return world * flops_per_step_per_rank / (ms_per_step_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------- main
 
 
@@ -327,16 +342,12 @@ def main():
         kern["reshard_head_to_seq"] = {"ms": t_out, "gbs": bytes_out / t_out / 1e6, "bytes": bytes_out}
 
     peaks, peak_src = load_peaks()
-    # Max over ranks of the timed totals.
-    times = torch.tensor([total_ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms_max, attn_ms_max = times.tolist()
+    total_ms, e2e_ms_max, attn_ms_max = max_over_ranks([total_ms, e2e_ms, attn_ms], dist, dev)
 
     result = None
     if rank == 0:
         ms_per_step = total_ms / args.steps
-        value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+        value = aggregate_value(flops_step, world, ms_per_step)
         launches_per_step = (6 if U > 1 else 1) + (1 if w.emit_partials else 0)
         achieved = flops_step / (attn_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
