@@ -53,6 +53,7 @@ class cp_plan_desc_t(ctypes.Structure):
         ("doc_offsets", ctypes.POINTER(ctypes.c_int32)),
         ("softmax_scale", ctypes.c_float),
         ("emit_partials", ctypes.c_int32),
+        ("out_fp32", ctypes.c_int32),
     ]
 
 
@@ -129,7 +130,7 @@ class Plan:
     """Owns a cp_plan_t (cp_plan_create / cp_plan_destroy)."""
 
     def __init__(self, L, Hq, Hkv, d, ulysses_degree=1, ring_degree=1, layout=CP_LAYOUT_CONTIGUOUS,
-                 doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True):
+                 doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True, out_fp32=False):
         self._h = None
         desc = cp_plan_desc_t()
         desc.version = CP_ATTN_PLAN_VERSION
@@ -147,6 +148,7 @@ class Plan:
             desc.doc_offsets = None
         desc.softmax_scale = float(softmax_scale)
         desc.emit_partials = 1 if emit_partials else 0
+        desc.out_fp32 = 1 if out_fp32 else 0
         h = _vp()
         _check(_L().cp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "cp_plan_create")
         self._h = h
@@ -156,6 +158,12 @@ class Plan:
         self.n = self.L // self.P
         self.layout = desc.layout
         self.emit_partials = bool(emit_partials)
+        self.out_fp32 = bool(out_fp32)
+
+    @property
+    def o_dtype(self):
+        import torch
+        return torch.float32 if self.out_fp32 else torch.bfloat16
 
     @property
     def handle(self):

@@ -75,8 +75,11 @@ __device__ __forceinline__ void store_row32_packed(uint32_t tile, int row, int c
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
-template <int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
+
+template <int D, typename OT>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dO,
                                                         float* __restrict__ delta, long long rows, int H, int T) {
   constexpr int E = D / 32;  // elements per lane
@@ -86,11 +89,11 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   for (long long wi = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < total; wi += nwarps) {
     const long long row = wi / H;
     const int h = static_cast<int>(wi - row * H);
-    const __nv_bfloat16* po = o + wi * D + lane * E;
+    const OT* po = o + wi * D + lane * E;
     const __nv_bfloat16* pd = dO + wi * D + lane * E;
     float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc = fmaf(__bfloat162float(po[e]), __bfloat162float(pd[e]), acc);
+    for (int e = 0; e < E; ++e) acc = fmaf(to_f32(po[e]), __bfloat162float(pd[e]), acc);
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
@@ -662,8 +665,12 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     const long long warps = rows * g.Hq_loc;
     long long grid = (warps * 32 + 255) / 256;
     if (grid > sms * 16LL) grid = sms * 16LL;
-    if (grid > 0)
-      bwd_delta_kernel<D><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+    if (grid > 0 && a.o_fp32)
+      bwd_delta_kernel<D, float><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+          static_cast<const float*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
+          static_cast<long long>(rows), g.Hq_loc, g.T);
+    else if (grid > 0)
+      bwd_delta_kernel<D, __nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
           static_cast<long long>(rows), g.Hq_loc, g.T);
   }

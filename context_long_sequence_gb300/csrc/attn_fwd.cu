@@ -1,39 +1,47 @@
 // attn_fwd.cu -- causal context-parallel attention forward on sm_103a.
 //
-// One CTA computes one 128-row query tile of one head of one attention rank.
-// It walks the KV chunks of the ring in ring order -- at step s the chunk of
-// ring rank (r - s) mod R ([MTX] nougat.kr "MaxText long-context training and
-// KV parallelism", section "Split heads or rotate KV": P2P keeps token
-// sharding and computes a partial with each visiting KV chunk) -- and, per
-// 128-key tile that has at least one visible (query, key) pair:
+// One CTA computes a block of up to 256 query rows (two 128-row tiles, Q0
+// and Q1, of the same head and the same contiguous-position chunk) of one
+// attention rank.  It walks the KV chunks of the ring in ring order -- at
+// step s the chunk of ring rank (r - s) mod R ([MTX] nougat.kr "MaxText
+// long-context training and KV parallelism", section "Split heads or rotate
+// KV": P2P keeps token sharding and computes a partial with each visiting KV
+// chunk) -- and, per 128-key tile visible from either query tile:
 //
-//   S = Q K^T             tcgen05.mma, bf16 operands in shared memory (TMA,
-//                         128-byte swizzle), fp32 accumulator in TMEM
-//   mask, online softmax  one thread per query row (TMEM lane = row), exp2
-//   O += P V              tcgen05.mma, P staged in shared memory as bf16
+//   S_t = Q_t K^T          tcgen05.mma, Q and K in shared memory (TMA,
+//                          128-byte swizzle), fp32 accumulator in TMEM
+//   mask, online softmax   one thread per query row (TMEM lane = row);
+//                          P_t = exp2(...) written back over S_t in TMEM
+//                          as packed bf16
+//   O_t += P_t V           tcgen05.mma with A read from TMEM, V in shared
+//                          memory
 //
-// Tiles with no visible pair are never visited; tiles wholly inside the
-// causal and document window skip the mask.  The merge of the ring partials
-// is fused: the online softmax simply continues across ring steps, which is
-// the exact merge evaluated incrementally.  In emit-partials mode a CTA
-// covers one ring step and writes that step's normalised partial (O, LSE) in
-// fp32 for the separate merge kernel.
+// The two query tiles ping-pong: while one softmax warpgroup works on S_0,
+// the tensor core runs the other tile's PV and QK^T, so neither waits for
+// the other.  Tiles with no visible pair are never visited; tiles wholly
+// inside the causal and document window skip the mask.  The merge of the
+// ring partials is fused: the online softmax continues across ring steps,
+// which is the exact merge evaluated incrementally.  In emit-partials mode
+// a CTA covers one ring step and writes that step's normalised partial
+// (O, LSE) in fp32 for the separate merge kernel.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator
-// and MMA issuer, warps 2..5 = softmax / correction / epilogue (thread t of
-// warp w owns query row 32*(w%4)+t, the TMEM lanes that warp may access).
+// Warp roles (320 threads): warp 0 = TMA producer; warp 1 = TMEM allocator
+// and MMA issuer; warps 2..5 = softmax / correction / epilogue of Q0 and
+// warps 6..9 of Q1 (thread t of warp w owns row 32*(w%4)+t, the TMEM lanes
+// that warp may access).  K and V have two shared-memory stages each.
 //
-// Pipeline: K and V have two shared-memory stages each; S is double-buffered
-// in TMEM so QK^T of tile j+1 runs while the softmax of tile j runs.  The
-// running max is only raised when it grows by more than 2^8 (log2 units), so
-// O is rescaled in TMEM rarely; the final normalisation uses the same max,
-// which keeps the result exact.
+// The running max is only raised when it grows by more than 2^8 (log2
+// units), so O is rescaled in TMEM rarely; the final normalisation uses the
+// same max, which keeps the result exact.  Issue order on the tensor core
+// per key tile j: QK0_j, PV1_{j-1}, QK1_j, PV0_j.  PV_t of one tile is
+// always issued before QK_t of the next, and tcgen05.mma ops from one thread
+// execute in issue order, so the next S_t never overwrites a P_t still
+// being read.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <cstdio>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -46,7 +54,7 @@ constexpr int BM = 128;                      // query rows per tile
 constexpr int BN = 128;                      // keys per tile
 constexpr uint32_t HALF_BYTES = 128 * 128;   // one 64-column (128-byte) swizzled half of a 128-row tile
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 
 enum Bar {
   BAR_Q = 0,
@@ -54,10 +62,9 @@ enum Bar {
   BAR_K_EMPTY = 3,  // +stage
   BAR_V_FULL = 5,   // +stage
   BAR_V_EMPTY = 7,  // +stage
-  BAR_S_FULL = 9,   // +buffer
-  BAR_S_EMPTY = 11, // +buffer
-  BAR_P_FULL = 13,
-  BAR_O_FULL = 14,
+  BAR_S_FULL = 9,   // +query tile
+  BAR_P_FULL = 11,  // +query tile
+  BAR_O_DONE = 13,  // +query tile
   BAR_DRAIN = 15,
   NUM_BARS = 16
 };
@@ -66,12 +73,10 @@ template <int D>
 struct FwdSmem {
   static constexpr uint32_t kQ = BM * D * 2;
   static constexpr uint32_t kKV = BN * D * 2;
-  static constexpr uint32_t kP = BM * BN * 2;
-  static constexpr uint32_t offQ = 0;
-  static constexpr uint32_t offK = offQ + kQ;
-  static constexpr uint32_t offV = offK + 2 * kKV;
-  static constexpr uint32_t offP = offV + 2 * kKV;
-  static constexpr uint32_t offBar = offP + kP;
+  static constexpr uint32_t offQ = 0;                 // two query tiles
+  static constexpr uint32_t offK = offQ + 2 * kQ;     // two stages
+  static constexpr uint32_t offV = offK + 2 * kKV;    // two stages
+  static constexpr uint32_t offBar = offV + 2 * kKV;
   static constexpr uint32_t offMisc = offBar + NUM_BARS * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   // 1 KB alignment slack; D=64 is padded so that one CTA (and one 512-column
@@ -79,10 +84,10 @@ struct FwdSmem {
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
 };
 
-// Visit, in ring order, every 128-key tile that may hold a visible key for a
-// query tile with positions [qpos0, qpos_last] and document starts >= lo_min.
-// f(kv_row, kpos0, klen): first row of the tile in the [R*U*T] row space, the
-// tile's first position, and its number of valid keys.
+// Visit, in ring order, every 128-key tile that may hold a visible key for
+// query positions <= qpos_last whose documents start at or after lo_min.
+// f(kv_row, kpos0, klen): first row of the tile in the [R*U*T] row space,
+// the tile's first position, and its number of valid keys.
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end,
                                                  int lo_min, int qpos_last, F&& f) {
@@ -103,6 +108,18 @@ __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u
   }
 }
 
+// One query tile's window: positions [qp0, qp_last], document starts in
+// [lo_min, lo_max]; len == 0 marks an absent tile.
+struct QWin {
+  int qp0, qp_last, lo_min, lo_max, len;
+  __device__ __forceinline__ bool sees(int kpos0, int klen) const {
+    return len > 0 && kpos0 <= qp_last && kpos0 + klen - 1 >= lo_min;
+  }
+  __device__ __forceinline__ bool full(int kpos0, int klen) const {
+    return klen == BN && kpos0 + BN - 1 <= qp0 && lo_max <= kpos0;
+  }
+};
+
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
 
 template <int D>
@@ -114,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + SM::offQ, sK = s_base + SM::offK, sV = s_base + SM::offV, sP = s_base + SM::offP;
+  const uint32_t sQ = s_base + SM::offQ, sK = s_base + SM::offK, sV = s_base + SM::offV;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
@@ -126,13 +143,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.x % g.Hq_loc;
   const WorkItem it = args.items[item_idx];
   const int a = it.a, r = a / g.U, u = a % g.U;
-  const int qpos0 = slot_pos(g, r, it.q0);
-  const int qpos_last = qpos0 + it.len - 1;
-  const int lo_min = g.doc_start ? g.doc_start[qpos0] : 0;
-  const int lo_max = g.doc_start ? g.doc_start[qpos_last] : 0;
   const int s_begin = it.step < 0 ? 0 : it.step;
   const int s_end = it.step < 0 ? g.R : it.step + 1;
   const int hkv = h / g.G;
+
+  // The two query tiles' windows (positions are contiguous within the block).
+  auto make_win = [&](int t) {
+    QWin w;
+    w.len = max(0, min(BM, it.len - t * BM));
+    w.qp0 = slot_pos(g, r, it.q0) + t * BM;
+    w.qp_last = w.qp0 + w.len - 1;
+    w.lo_min = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp0] : 0;
+    w.lo_max = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp_last] : 0;
+    return w;
+  };
+  const QWin win0 = make_win(0), win1 = make_win(1);
+  const int blk_lo_min = win0.lo_min;
+  const int blk_qp_last = win0.qp0 + it.len - 1;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
@@ -142,10 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_V_FULL + i), 1);
       mbar_init(bar(BAR_V_EMPTY + i), 1);
       mbar_init(bar(BAR_S_FULL + i), 1);
-      mbar_init(bar(BAR_S_EMPTY + i), 4);
+      mbar_init(bar(BAR_P_FULL + i), 4);
+      mbar_init(bar(BAR_O_DONE + i), 1);
     }
-    mbar_init(bar(BAR_P_FULL), 4);
-    mbar_init(bar(BAR_O_FULL), 1);
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -163,16 +189,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+  // S_t = tmem + 128 t (128 fp32 columns; P_t as packed bf16 in its first
+  // 64) and O_t = tmem + 256 + D t.
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(BAR_Q), SM::kQ);
+      mbar_arrive_expect_tx(bar(BAR_Q), 2 * SM::kQ);
       const int qrow = a * g.T + it.q0;
-      for (int hh = 0; hh < NH; ++hh) tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow);
+      for (int t = 0; t < 2; ++t)
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
       int nk = 0, nv = 0;
-      for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row, int, int) {
+      for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row, int, int) {
         if (*abort_flag) return;
         const int st = nk & 1;
         const uint32_t ph = ((nk >> 1) & 1) ^ 1;
@@ -199,48 +228,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(bar(BAR_P_FULL), i & 1, abort_flag, status)) return false;
-        if (!mbar_wait(bar(BAR_V_FULL + st), (i >> 1) & 1, abort_flag, status)) return false;
+      int npv[2] = {0, 0};      // PVs issued per query tile
+      int pend_st = -1;         // V stage of a PV1 still to issue
+      uint32_t pend_ph = 0;
+      auto issue_qk = [&](int t, uint32_t kb) {
+        const uint32_t qb = sQ + t * SM::kQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 128 * t, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc_qk,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_S_FULL + t));
+      };
+      // O_t += P_t V: A = P_t in TMEM (8 columns per 16 keys), B = V [keys x d]
+      // read as N=d x K=keys, MN-major (16 keys = 16 rows of 128 bytes; the two
+      // 64-column halves of d are HALF_BYTES apart).
+      auto issue_pv = [&](int t, int st, uint32_t ph, bool release_v) -> bool {
+        if (!mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status)) return false;
+        if (!mbar_wait(bar(BAR_V_FULL + st), ph, abort_flag, status)) return false;
         tc_fence_after();
         const uint32_t vb = sV + st * SM::kKV;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P [128 x 128 keys], K-major: 16 keys = 32 bytes inside a 64-key half.
-          const uint64_t ad = smem_desc_sw128(sP + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-          // B = V [keys x d] read as N=d x K=keys, MN-major: 16 keys = 16 rows of 128 bytes;
-          // the two 64-column halves of d are HALF_BYTES apart (leading offset).
-          const uint64_t bd = smem_desc_sw128(vb + kk * 2048, HALF_BYTES, 1024);
-          mma_bf16_ss(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(BAR_O_FULL));
-        mma_commit(bar(BAR_V_EMPTY + st));
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + 256 + D * t, tmem + 128 * t + kk * 8, smem_desc_sw128(vb + kk * 2048, HALF_BYTES, 1024),
+                      idesc_pv, (npv[t] > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(BAR_O_DONE + t));
+        if (release_v) mma_commit(bar(BAR_V_EMPTY + st));
+        ++npv[t];
         return true;
       };
       int j = 0;
-      if (mbar_wait(bar(BAR_Q), 0, abort_flag, status)) {
-        for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) {
-          if (*abort_flag) return;
+      bool ok = mbar_wait(bar(BAR_Q), 0, abort_flag, status);
+      if (ok) {
+        for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int, int kpos0, int klen) {
+          if (!ok || *abort_flag) return;
+          const bool v0 = win0.sees(kpos0, klen), v1 = win1.sees(kpos0, klen);
           const int st = j & 1;
           const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait(bar(BAR_K_FULL + st), ph, abort_flag, status)) return;
-          if (!mbar_wait(bar(BAR_S_EMPTY + st), ph ^ 1, abort_flag, status)) return;
+          if (!(ok = mbar_wait(bar(BAR_K_FULL + st), ph, abort_flag, status))) return;
           tc_fence_after();
           const uint32_t kb = sK + st * SM::kKV;
-          const uint32_t tS = st ? tS1 : tS0;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc_qk,
-                        kk > 0 ? 1u : 0u);
+          if (v0) issue_qk(0, kb);
+          if (pend_st >= 0) {
+            if (!(ok = issue_pv(1, pend_st, pend_ph, true))) return;
+            pend_st = -1;
           }
-          mma_commit(bar(BAR_S_FULL + st));
+          if (v1) issue_qk(1, kb);
           mma_commit(bar(BAR_K_EMPTY + st));
-          if (j > 0 && !issue_pv(j - 1)) return;
+          if (v0 && !(ok = issue_pv(0, st, ph, !v1))) return;
+          if (v1) {
+            pend_st = st;
+            pend_ph = ph;
+          }
           ++j;
         });
-        if (j > 0 && !*abort_flag) issue_pv(j - 1);
+        if (ok && pend_st >= 0 && !*abort_flag) issue_pv(1, pend_st, pend_ph, true);
       }
       // Every MMA issued so far completes before TMEM and shared memory are released.
       mma_commit(bar(BAR_DRAIN));
@@ -248,44 +291,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
+    const int t = (warp - 2) >> 2;  // query tile of this warpgroup
+    const QWin w = t ? win1 : win0;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const bool row_valid = row < it.len;
-    const int my_pos = row_valid ? qpos0 + row : -1;
+    const uint32_t tSt = tmem + 128 * t + lane_off, tOt = tmem + 256 + D * t + lane_off;
+    const bool row_valid = row < w.len;
+    const int my_pos = row_valid ? w.qp0 + row : -1;
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
     const float sl2 = g.scale * 1.4426950408889634f;
     float m = -INFINITY, l = 0.f;
-    int j = 0;
+    int k = 0;
     bool ok = true;
-    for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int kpos0, int klen) {
-      if (!ok) return;
-      const int b = j & 1;
-      ok = warp_all(mbar_wait(bar(BAR_S_FULL + b), (j >> 1) & 1, abort_flag, status));
+    for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int, int kpos0, int klen) {
+      if (!ok || !w.sees(kpos0, klen)) return;
+      ok = warp_all(mbar_wait(bar(BAR_S_FULL + t), k & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
+      const bool full = w.full(kpos0, klen);
+      const int c_lo = my_lo - kpos0;
+      const int c_hi = min(my_pos - kpos0, klen - 1);
+      // S row -> registers: four 32-column loads in flight, one wait.
       uint32_t sr[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32((b ? tS1 : tS0) + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_ld32(tSt + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY + b));
-      float* s = reinterpret_cast<float*>(sr);
-      const bool full = (klen == BN) && (kpos0 + BN - 1 <= qpos0) && (lo_max <= kpos0);
+      float* x = reinterpret_cast<float*>(sr);
       if (!full) {
-        const int c_lo = my_lo - kpos0;
-        const int c_hi = min(my_pos - kpos0, klen - 1);
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c < c_lo || c > c_hi) s[c] = -INFINITY;
+        for (int e = 0; e < BN; ++e)
+          if (e < c_lo || e > c_hi) x[e] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // Row max: 3-input max in 8 independent chains.
+      float m8[8];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(x[i], x[8 + i]);
+#pragma unroll
+      for (int e = 16; e < BN; e += 16)  // covers x[16 .. 127]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[e + i], x[e + 8 + i]);
+      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_new = fmaxf(m, mx * sl2);
       float alpha = 1.f;
       if (m_new > m + kRescaleThreshold) {
@@ -293,49 +342,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       const float mb = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      // P = exp2(S*scale*log2e - m) -> packed bf16 into the first 64 columns
+      // of S (already read into registers).
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const float p = ex2_approx(fmaf(s[c], sl2, -mb));
-        s[c] = p;
-        rs += p;
-      }
-      l = l * alpha + rs;
-      if (j > 0) {
-        // PV of the previous tile must be done: it reads P and writes O.
-        ok = warp_all(mbar_wait(bar(BAR_O_FULL), (j - 1) & 1, abort_flag, status));
-        if (!ok) return;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + lane_off + c * 32, ov);
-            tmem_wait_ld();
-            reg_fence(ov);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, ov);
-          }
-          tmem_wait_st();
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2_approx(fmaf(x[c * 32 + e], sl2, -mb));
+          const float p1 = ex2_approx(fmaf(x[c * 32 + e + 1], sl2, -mb));
+          rs4[(e >> 1) & 3] += p0 + p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
         }
+        tmem_st16(tSt + c * 16, pk);
       }
-      // P -> shared memory, bf16, K-major with 128-byte swizzle.
-      const uint32_t prow = sP + row * 128;
+      tmem_wait_st();
+      l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      // O is stable here: this tile's S_FULL commit came after the previous PV_t.
+      if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tOt + c * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const uint32_t addr = prow + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (row & 7)) << 4);
-        st_shared_v4(addr, pack_bf16x2(s[8 * ch + 0], s[8 * ch + 1]), pack_bf16x2(s[8 * ch + 2], s[8 * ch + 3]),
-                     pack_bf16x2(s[8 * ch + 4], s[8 * ch + 5]), pack_bf16x2(s[8 * ch + 6], s[8 * ch + 7]));
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tOt + c * 32, ov);
+        }
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
-      ++j;
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
+      ++k;
     });
-    if (ok && j > 0) {
-      ok = warp_all(mbar_wait(bar(BAR_O_FULL), (j - 1) & 1, abort_flag, status));
+    if (ok && k > 0) {
+      ok = warp_all(mbar_wait(bar(BAR_O_DONE + t), (k - 1) & 1, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
@@ -343,26 +387,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = has ? 1.f / l : 0.f;
       const float lse = has ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
       const bool partial = args.o_part != nullptr;
-      const int s_idx = s_begin;
+      const int q_slot = it.q0 + t * BM + row;
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
-        if (j > 0) {
-          tmem_ld32(tO + lane_off + c * 32, ov);
+        if (k > 0) {
+          tmem_ld32(tOt + c * 32, ov);
           tmem_wait_ld();
           reg_fence(ov);
         }
         if (!row_valid) continue;
         float o[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = (j > 0) ? __uint_as_float(ov[e]) * inv_l : 0.f;
+        for (int e = 0; e < 32; ++e) o[e] = (k > 0) ? __uint_as_float(ov[e]) * inv_l : 0.f;
         if (partial) {
           float* dst = args.o_part +
-                       ((static_cast<size_t>(r * g.R + s_idx) * g.T + it.q0 + row) * g.Hq_loc + h) * D + c * 32;
+                       ((static_cast<size_t>(r * g.R + s_begin) * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        } else if (args.o_fp32) {
+          float* dst = reinterpret_cast<float*>(args.o) + (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         } else {
           __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) +
-                               (static_cast<size_t>(a * g.T + it.q0 + row) * g.Hq_loc + h) * D + c * 32;
+                               (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 8)
             *reinterpret_cast<uint4*>(dst + e) =
@@ -372,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row_valid) {
         if (partial)
-          args.lse_part[(static_cast<size_t>(r * g.R + s_idx) * g.Hq_loc + h) * g.T + it.q0 + row] = lse;
+          args.lse_part[(static_cast<size_t>(r * g.R + s_begin) * g.Hq_loc + h) * g.T + q_slot] = lse;
         else
-          args.lse[(static_cast<size_t>(a) * g.Hq_loc + h) * g.T + it.q0 + row] = lse;
+          args.lse[(static_cast<size_t>(a) * g.Hq_loc + h) * g.T + q_slot] = lse;
       }
     }
   }

@@ -29,9 +29,11 @@ struct cp_plan {
   int device;
   int32_t* d_doc_start;          // [L] or null
   int32_t* d_doc_end;            // [L] or null
-  WorkItem* d_items_fused;
+  WorkItem* d_items_fused;       // forward: 256-row query blocks, all ring steps
   int n_items_fused;
-  WorkItem* d_items_steps;       // emit-partials: one item per (query tile, ring step)
+  WorkItem* d_items_q;           // backward dQ: 128-row query tiles
+  int n_items_q;
+  WorkItem* d_items_steps;       // emit-partials: one item per (256-row query block, ring step)
   int n_items_steps;
   WorkItem* d_items_kv;          // backward: key tiles
   int n_items_kv;
@@ -101,8 +103,9 @@ int visited_tiles(const cp_plan* p, const AttnGeom& g, int r, int q0, int len, i
   return count;
 }
 
-// Query tiles ordered by descending work (longest first onto the SMs).
-std::vector<WorkItem> build_items(const cp_plan* p, bool per_step) {
+// Query blocks of `rows` slots, ordered by descending work (longest first
+// onto the SMs).
+std::vector<WorkItem> build_items(const cp_plan* p, bool per_step, int rows) {
   const AttnGeom g = geom(p);
   struct Keyed {
     int work;
@@ -113,9 +116,9 @@ std::vector<WorkItem> build_items(const cp_plan* p, bool per_step) {
   for (int a = 0; a < A; ++a) {
     const int r = a / g.U;
     for (int ch = 0; ch < p->nchunks; ++ch)
-      for (int t0 = 0; t0 < p->chunk; t0 += kTile) {
+      for (int t0 = 0; t0 < p->chunk; t0 += rows) {
         const int q0 = ch * p->chunk + t0;
-        const int len = std::min(kTile, p->chunk - t0);
+        const int len = std::min(rows, p->chunk - t0);
         if (per_step) {
           for (int s = 0; s < g.R; ++s)
             v.push_back({visited_tiles(p, g, r, q0, len, s, s + 1), WorkItem{a, q0, len, s}});
@@ -208,7 +211,7 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
     w.qh = take(L * d.Hq * d.d * 2);
     w.kh = take(L * d.Hkv * d.d * 2);
     w.vh = take(L * d.Hkv * d.d * 2);
-    w.oh = take(L * d.Hq * d.d * 2);
+    w.oh = take(L * d.Hq * d.d * (d.out_fp32 ? 4 : 2));
     w.lseh = take(L * d.Hq * 4);
   }
   if (d.emit_partials) {
@@ -235,6 +238,8 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   if (d.Hq % d.Hkv) return CP_ERR_INVALID_ARG;
   if (d.layout != CP_LAYOUT_CONTIGUOUS && d.layout != CP_LAYOUT_ZIGZAG) return CP_ERR_INVALID_ARG;
   if (d.num_docs < 0) return CP_ERR_INVALID_ARG;
+  if (d.out_fp32 != 0 && d.out_fp32 != 1) return CP_ERR_INVALID_ARG;
+  if (d.emit_partials != 0 && d.emit_partials != 1) return CP_ERR_INVALID_ARG;
   if (!(d.softmax_scale >= 0.f) || std::isinf(d.softmax_scale)) return CP_ERR_INVALID_ARG;
   if (d.d != 64 && d.d != 128) return CP_ERR_UNSUPPORTED;
   if (d.causal != 1) return CP_ERR_UNSUPPORTED;
@@ -272,8 +277,8 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
-  p->d_items_fused = p->d_items_steps = p->d_items_kv = nullptr;
-  p->n_items_fused = p->n_items_steps = p->n_items_kv = 0;
+  p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = nullptr;
+  p->n_items_fused = p->n_items_q = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
   // maps, workspace sizes -- works without one).
@@ -301,11 +306,16 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       rc = upload(ds, &p->d_doc_start);
       if (rc == CP_OK) rc = upload(de, &p->d_doc_end);
     }
-    std::vector<WorkItem> fused = build_items(p, false);
+    std::vector<WorkItem> fused = build_items(p, false, 2 * kTile);
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
+    if (rc == CP_OK && U == 1) {
+      std::vector<WorkItem> qt = build_items(p, false, kTile);
+      p->n_items_q = static_cast<int>(qt.size());
+      rc = upload(qt, &p->d_items_q);
+    }
     if (rc == CP_OK && d.emit_partials) {
-      std::vector<WorkItem> steps = build_items(p, true);
+      std::vector<WorkItem> steps = build_items(p, true, 2 * kTile);
       p->n_items_steps = static_cast<int>(steps.size());
       rc = upload(steps, &p->d_items_steps);
     }
@@ -318,6 +328,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       cudaFree(p->d_doc_start);
       cudaFree(p->d_doc_end);
       cudaFree(p->d_items_fused);
+      cudaFree(p->d_items_q);
       cudaFree(p->d_items_steps);
       cudaFree(p->d_items_kv);
       delete p;
@@ -335,6 +346,7 @@ void cp_plan_destroy(cp_plan_t* p) {
     cudaFree(p->d_doc_start);
     cudaFree(p->d_doc_end);
     cudaFree(p->d_items_fused);
+    cudaFree(p->d_items_q);
     cudaFree(p->d_items_steps);
     cudaFree(p->d_items_kv);
   }
@@ -396,6 +408,7 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   cpattn::FwdArgs a{};
   a.g = geom(p);
   a.d = d.d;
+  a.o_fp32 = d.out_fp32;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;
   if (d.ulysses_degree == 1) {
@@ -411,7 +424,8 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
       a.n_items = p->n_items_steps;
       rc = cpattn::launch_attn_fwd(a, stream);
       if (rc != CP_OK) return rc;
-      return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse, stream);
+      return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse,
+                                  d.out_fp32, stream);
     }
     a.items = p->d_items_fused;
     a.n_items = p->n_items_fused;
@@ -435,7 +449,9 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.items = p->d_items_fused;
   a.n_items = p->n_items_fused;
   if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
-  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 2, oh, o, stream))) return rc;
+  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o,
+                                   stream)))
+    return rc;
   return cpattn::launch_reshard(R, U, p->n, d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse, stream);
 }
 
@@ -448,6 +464,7 @@ int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const vo
   cpattn::FwdArgs a{};
   a.g = geom(p);
   a.d = p->desc.d;
+  a.o_fp32 = p->desc.out_fp32;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;
   a.q = q;
@@ -480,12 +497,13 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.o = o;
   a.lse = lse;
   a.dO = dO;
+  a.o_fp32 = p->desc.out_fp32;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
   a.delta = static_cast<float*>(workspace);
-  a.items_q = p->d_items_fused;
-  a.n_items_q = p->n_items_fused;
+  a.items_q = p->d_items_q;
+  a.n_items_q = p->n_items_q;
   a.items_kv = p->d_items_kv;
   a.n_items_kv = p->n_items_kv;
   a.d = p->desc.d;
@@ -500,7 +518,7 @@ int cp_merge_lse(int n_parts, int rows, int H, int d, const float* o_parts, cons
   if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
   if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o_out) || !aligned16(lse_out))
     return CP_ERR_ALIGNMENT;
-  return cpattn::launch_merge(1, n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream);
+  return cpattn::launch_merge(1, n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, 0, stream);
 }
 
 int cp_get_status(cudaStream_t stream, int32_t* dev_code) {
@@ -579,6 +597,7 @@ extern "C" int cp_attn_fwd_noalloc(const cp_plan_t* p, const void* q, const void
   cpattn::FwdArgs a{};
   a.g = geom(p);
   a.d = d.d;
+  a.o_fp32 = d.out_fp32;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;
   a.q = q;
@@ -592,5 +611,6 @@ extern "C" int cp_attn_fwd_noalloc(const cp_plan_t* p, const void* q, const void
   a.n_items = p->n_items_steps;
   rc = cpattn::launch_attn_fwd(a, stream);
   if (rc != CP_OK) return rc;
-  return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse, stream);
+  return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse,
+                              d.out_fp32, stream);
 }

@@ -39,7 +39,8 @@ struct FwdArgs {
   const void* q;  // [R*U*T][Hq_loc][d] bf16
   const void* k;  // [R*U*T][Hkv_loc][d] bf16
   const void* v;
-  void* o;        // [R*U*T][Hq_loc][d] bf16     (fused mode)
+  void* o;        // [R*U*T][Hq_loc][d] bf16 or fp32 (o_fp32)  (fused mode)
+  int o_fp32;
   float* lse;     // [R*U][Hq_loc][T]            (fused mode)
   float* o_part;  // [R][R][T][Hq][d] fp32       (emit-partials mode, U == 1)
   float* lse_part;// [R][R][Hq][T]
@@ -57,6 +58,7 @@ struct BwdArgs {
   AttnGeom g;
   const void* q;  const void* k;  const void* v;
   const void* o;  const float* lse;  const void* dO;
+  int o_fp32;     // o is fp32 instead of bf16
   float* dq;  float* dk;  float* dv;
   float* delta;   // [R][Hq][T] workspace: rowsum(dO * O)
   const WorkItem* items_q;
@@ -75,6 +77,6 @@ int launch_reshard(int R, int U, int n, int H, int row_bytes_total, int directio
 
 // Merge of `n_parts` partials, `batch` independent groups laid out back to back.
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts,
-                 const float* lse_parts, void* o_out, float* lse_out, cudaStream_t stream);
+                 const float* lse_parts, void* o_out, float* lse_out, int out_fp32, cudaStream_t stream);
 
 }  // namespace cpattn

@@ -31,8 +31,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(int n_parts, long long rows, int H, const float* __restrict__ o_parts,
-                                                    const float* __restrict__ lse_parts, __nv_bfloat16* __restrict__ o_out,
-                                                    float* __restrict__ lse_out, long long batch) {
+                                                    const float* __restrict__ lse_parts, void* __restrict__ o_out,
+                                                    float* __restrict__ lse_out, long long batch, int out_fp32) {
   constexpr int TPR = D / 4;  // threads per (row, head)
   const long long per_batch = rows * H;
   const long long total = batch * per_batch * TPR;
@@ -63,8 +63,11 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, long long rows,
         acc.w = fmaf(wgt, x.w, acc.w);
       }
     }
-    uint2 packed = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(o_out + (b * per_batch + w) * D + c4 * 4) = packed;
+    const long long oi = (b * per_batch + w) * D + c4 * 4;
+    if (out_fp32)
+      *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc;
+    else
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oi) = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
     if (c4 == 0) lse_out[b * per_batch + static_cast<long long>(h) * rows + row] = lse;
   }
 }
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, long long rows,
 }  // namespace
 
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts,
-                 void* o_out, float* lse_out, cudaStream_t stream) {
+                 void* o_out, float* lse_out, int out_fp32, cudaStream_t stream) {
   const long long work = static_cast<long long>(batch) * rows * H * (d / 4);
   if (work == 0) return CP_OK;
   int dev = 0, sms = 148;
@@ -81,13 +84,12 @@ int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_
   long long grid = (work + threads - 1) / threads;
   const long long cap = static_cast<long long>(sms) * 8;
   if (grid > cap) grid = cap;
-  auto* o = static_cast<__nv_bfloat16*>(o_out);
   if (d == 128)
-    merge_kernel<128><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o,
-                                                                      lse_out, batch);
+    merge_kernel<128><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
+                                                                      lse_out, batch, out_fp32);
   else if (d == 64)
-    merge_kernel<64><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o,
-                                                                     lse_out, batch);
+    merge_kernel<64><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
+                                                                     lse_out, batch, out_fp32);
   else
     return CP_ERR_UNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;

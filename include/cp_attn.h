@@ -102,6 +102,10 @@ typedef struct {
                                  into the workspace and merges them in ring order with the same
                                  kernel as cp_merge_lse(); 0 => the merge is fused (online softmax
                                  continued across ring steps).  Requires U == 1. */
+  int32_t out_fp32;           /* 0 => O is bf16 (round to nearest even); 1 => O is fp32 (the
+                                 normalised accumulator, unrounded).  Applies to the o output of
+                                 cp_attn_fwd, cp_attn_fwd_local and cp_attn_fwd_noalloc and to the
+                                 o input of cp_attn_bwd; cp_merge_lse always writes bf16. */
 } cp_plan_desc_t;
 
 typedef struct cp_plan cp_plan_t;   /* opaque; immutable after creation; usable from any stream */
@@ -143,7 +147,7 @@ int ulysses_reshard(const cp_plan_t *plan, int direction, int tensor_kind, int H
 /* Causal CP attention forward for all P emulated ranks.
  *   q  [P][n][Hq][d]  bf16, sequence-sharded (slot order of cp_index_map)
  *   k,v[P][n][Hkv][d] bf16
- *   o  [P][n][Hq][d]  bf16 out
+ *   o  [P][n][Hq][d]  bf16 out (fp32 if the plan's out_fp32 is set)
  *   lse[P][Hq][n]     fp32 out (natural log; -inf for a row with no visible key)
  * With U > 1 the call reshards Q, K, V to head-sharded layout in the
  * workspace, runs ring attention per head group and reshards O and LSE back
@@ -161,7 +165,7 @@ int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void 
  * rotate KV": each chip computes its heads over the whole group sequence;
  * the ring runs over r for each head group u).
  *   q  [R][U][T][Hq/U][d] bf16,  k, v [R][U][T][Hkv/U][d] bf16, T = L/R
- *   o  [R][U][T][Hq/U][d] bf16 out,  lse [R][U][Hq/U][T] fp32 out
+ *   o  [R][U][T][Hq/U][d] bf16 (fp32 if out_fp32) out,  lse [R][U][Hq/U][T] fp32 out
  * With U == 1 this is cp_attn_fwd with the fused merge.  No workspace. */
 int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                       void *o, float *lse, cudaStream_t stream);
@@ -171,7 +175,8 @@ int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const
  * cost"): with P = exp(scale*QK^T - LSE),
  *   D = rowsum(dO * O); dV = P^T dO; dS = P * (dO V^T - D);
  *   dQ = scale dS K;  dK = scale dS^T Q;  query heads sum into their KV head.
- * q, o, dO [P][n][Hq][d] bf16; k, v [P][n][Hkv][d] bf16; lse [P][Hq][n] fp32;
+ * q, dO [P][n][Hq][d] bf16; o the same (fp32 if out_fp32); k, v [P][n][Hkv][d] bf16;
+ * lse [P][Hq][n] fp32;
  * dq [P][n][Hq][d], dk, dv [P][n][Hkv][d] fp32 out (overwritten).
  * Gradients of a KV chunk land on the rank that owns the chunk.
  * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes. */

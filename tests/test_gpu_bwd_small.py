@@ -55,3 +55,15 @@ def test_bwd_deterministic(cpa):
     b = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_bwd_with_fp32_o(cpa):
+    """The backward reads an fp32 O (plan out_fp32) for D = rowsum(dO * O)."""
+    import gpu_harness as gh
+    inp = workloads.make_inputs(768, 4, 2, 128, 21, with_do=True)
+    plan = cpa.Plan(768, 4, 2, 128, ring_degree=3, layout=1, doc_offsets=[0, 300, 768], out_fp32=True)
+    got = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
+    _, _, dq, dk, dv = oracle.attention_bwd(inp["q"].double().numpy(), inp["k"].double().numpy(),
+                                            inp["v"].double().numpy(), inp["do"].double().numpy(),
+                                            offsets=[0, 300, 768])
+    gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], "fp32 O")

@@ -47,16 +47,17 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("out_fp32", [True, False], ids=["o_fp32", "o_bf16"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_fwd_matches_oracle(cpa, case):
+def test_fwd_matches_oracle(cpa, case, out_fp32):
     import gpu_harness as gh
     name, L, Hq, Hkv, d, U, R, layout, docs, partials = case
     inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(name.encode()) % 1000)
     plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=layout, doc_offsets=docs,
-                    emit_partials=partials)
+                    emit_partials=partials, out_fp32=out_fp32)
     O, LSE = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
     O_ref, LSE_ref = oracle.attention(inp["q"], inp["k"], inp["v"], offsets=docs)
-    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name)
+    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name, bf16_out=not out_fp32)
 
 
 def test_fwd_deterministic(cpa):

@@ -44,14 +44,14 @@ def _boundaries(w, offsets):
     return b
 
 
-def _run_fwd(cpa, w, dev="cuda"):
+def _run_fwd(cpa, w, dev="cuda", out_fp32=False):
     offsets = workloads.workload_doc_offsets(w)
     plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
-                    doc_offsets=offsets, emit_partials=w.emit_partials)
+                    doc_offsets=offsets, emit_partials=w.emit_partials, out_fp32=out_fp32)
     g = workloads.workload_inputs(w, device=dev)
     idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
     q, k, v = (g[n][idx].contiguous() for n in ("q", "k", "v"))
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=plan.o_dtype, device=dev)
     lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device=dev)
     ws = cpa.alloc_workspace(plan, device=dev)
     cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws)
@@ -62,11 +62,12 @@ def _run_fwd(cpa, w, dev="cuda"):
     return plan, offsets, g, (q, k, v, o, lse), slot_of
 
 
+@pytest.mark.parametrize("out_fp32", [False, True], ids=["o_bf16", "o_fp32"])
 @pytest.mark.parametrize("wi", [0, 1, 2, 3, 4], ids=[w.name for w in workloads.WORKLOADS])
-def test_workload_forward_sampled(cpa, wi):
+def test_workload_forward_sampled(cpa, wi, out_fp32):
     import gpu_harness as gh
     w = workloads.WORKLOADS[wi]
-    plan, offsets, g, (q, k, v, o, lse), slot_of = _run_fwd(cpa, w)
+    plan, offsets, g, (q, k, v, o, lse), slot_of = _run_fwd(cpa, w, out_fp32=out_fp32)
     per_head = 256 if w.L <= 65536 else 48
     rows = workloads.sample_rows(w.L, _boundaries(w, offsets), per_head, seed=w.seed)
     if w.L <= 1024:
@@ -82,7 +83,7 @@ def test_workload_forward_sampled(cpa, wi):
     del g
     torch.cuda.empty_cache()
     O_ref, LSE_ref = oracle.attention_rows(cpu["q"], cpu["k"], cpu["v"], rows=rows, offsets=offsets, heads=heads)
-    gh.assert_close(O, LSE, O_ref, LSE_ref, w.name)
+    gh.assert_close(O, LSE, O_ref, LSE_ref, w.name, bf16_out=not out_fp32)
 
 
 def test_workload_backward_sampled(cpa):
