@@ -16,6 +16,7 @@ same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -33,6 +34,8 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
+METRIC = "CP causal attn fwd TFLOPS & tokens/s, L=1K-1M, % of GB300 bf16 dense peak"
+BWD_FLOP_RATIO = 2.5   # backward useful FLOPs per forward FLOP (dV, dP, dQ, dK products + recompute of S excluded)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -200,14 +203,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--L", type=int, default=0,
+                    help="override the workload's sequence length (small cases for profiling); 0 keeps it")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = workloads.WORKLOAD_BY_NAME[args.workload]
+    if args.L:
+        w = dataclasses.replace(w, L=args.L)
     offsets = workloads.workload_doc_offsets(w)
-    flops_step = useful_flops(w, offsets)
+    flops_fwd = useful_flops(w, offsets)
+    flops_step = int(flops_fwd * (1 + BWD_FLOP_RATIO)) if w.backward else flops_fwd
     warmup = max(3, args.warmup)
 
     if args.impl == "reference":
@@ -228,17 +236,32 @@ def main():
                     doc_offsets=offsets, emit_partials=w.emit_partials)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
     # each rank draws its own sequence.
-    g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale)
+    g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale,
+                                     with_do=w.backward)
     idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
     q, k, v = (g_inputs[n][idx].contiguous() for n in ("q", "k", "v"))
     o = torch.empty_like(q)
     lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device=dev)
     ws = cpa.alloc_workspace(plan, device=dev)
+    if w.backward:
+        do = g_inputs["do"][idx].contiguous()
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        ws_bwd = cpa.alloc_workspace(plan, cpa.CP_OP_BWD, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def fwd():
         cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws, stream=stream)
+
+    def bwd():
+        cpa.cp_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws_bwd, stream=stream)
+
+    def step():
+        fwd()
+        if w.backward:
+            bwd()
 
     for _ in range(warmup):
         step()
@@ -276,13 +299,18 @@ def main():
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
+    ins = [(q, q_h), (k, k_h), (v, v_h)]
+    outs = [(o, o_h), (lse, lse_h)]
+    if w.backward:
+        ins.append((do, do.cpu().pin_memory()))
+        outs += [(t, torch.empty(t.shape, dtype=t.dtype).pin_memory()) for t in (dq, dk, dv)]
+
     def e2e_step():
-        q.copy_(q_h, non_blocking=True)
-        k.copy_(k_h, non_blocking=True)
-        v.copy_(v_h, non_blocking=True)
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
         step()
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        for src, dst in outs:
+            dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -295,8 +323,8 @@ def main():
     ee1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
-    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
 
     # ---- per-kernel breakdown (the dominant kernel's roofline)
     kern = {}
@@ -324,7 +352,11 @@ def main():
 
     reps = max(3, min(args.steps, 10))
     attn_ms = timed(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
-    kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_step / attn_ms / 1e9}
+    kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9}
+    if w.backward:
+        bwd_ms = timed(bwd, reps)
+        kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,
+                            "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"}
     if U > 1:
         def rin():
             cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh, stream=stream)
@@ -348,11 +380,11 @@ def main():
     if rank == 0:
         ms_per_step = total_ms / args.steps
         value = aggregate_value(flops_step, world, ms_per_step)
-        launches_per_step = (6 if U > 1 else 1) + (1 if w.emit_partials else 0)
-        achieved = flops_step / (attn_ms * 1e-3) / 1e12
+        launches_per_step = (6 if U > 1 else 1) + (1 if w.emit_partials else 0) + (3 if w.backward else 0)
+        achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         result = {
-            "metric": "CP causal attention forward, useful TFLOP/s",
+            "metric": METRIC,
             "value": round(value, 3),
             "unit": "TFLOP/s",
             "n_gpus": world,
@@ -368,6 +400,7 @@ def main():
                        "layout": "zigzag" if w.layout else "contiguous", "docs": bool(offsets is not None),
                        "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
                        "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",
+                       "step": "forward + backward" if w.backward else "forward",
                        "l2": "flushed (256 MiB write) before every timed step"},
             "tokens_per_s": round(world * w.L / (ms_per_step * 1e-3), 1),
             "useful_flops_per_step": flops_step,
@@ -377,7 +410,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"bf16 dense burst, {peak_src}",
-                         "traffic": profiled_traffic(w.name)},
+                         "traffic": None if args.L else profiled_traffic(w.name)},
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
             "hbm_peak_gbs": peaks["hbm_gbs"],
@@ -424,7 +457,7 @@ def run_reference(args, w, offsets, flops_step, warmup, world):
     cores = len(os.sched_getaffinity(0))
     sample = f"per step {rows} seeded random query rows x {len(heads)} heads of {w.name} (fp64 numpy oracle)"
     line = {
-        "impl": "reference", "metric": "CP causal attention forward, useful TFLOP/s", "value": value,
+        "impl": "reference", "metric": METRIC, "value": value,
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
         "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",

@@ -28,7 +28,12 @@
 // Warp roles (320 threads): warp 0 = TMA producer; warp 1 = TMEM allocator
 // and MMA issuer; warps 2..5 = softmax / correction / epilogue of Q0 and
 // warps 6..9 of Q1 (thread t of warp w owns row 32*(w%4)+t, the TMEM lanes
-// that warp may access).  K and V have two shared-memory stages each.
+// that warp may access).
+//
+// K and V tiles stream through one ring of five shared-memory slots in load
+// order K_0, V_0, K_1, V_1, ... (load n of the sequence uses slot n mod 5), so
+// a tile's loads are issued about two tiles ahead of their use: a TMA load
+// from L2 takes a few microseconds under load, more than one tile's work.
 //
 // The running max is only raised when it grows by more than 2^8 (log2
 // units), so O is rescaled in TMEM rarely; the final normalisation uses the
@@ -56,17 +61,17 @@ constexpr uint32_t HALF_BYTES = 128 * 128;   // one 64-column (128-byte) swizzle
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kThreads = 320;
 
+constexpr int kSlots = 5;                    // K/V ring slots
+
 enum Bar {
   BAR_Q = 0,
-  BAR_K_FULL = 1,   // +stage
-  BAR_K_EMPTY = 3,  // +stage
-  BAR_V_FULL = 5,   // +stage
-  BAR_V_EMPTY = 7,  // +stage
-  BAR_S_FULL = 9,   // +query tile
-  BAR_P_FULL = 11,  // +query tile
-  BAR_O_DONE = 13,  // +query tile
-  BAR_DRAIN = 15,
-  NUM_BARS = 16
+  BAR_KV_FULL = 1,               // +slot
+  BAR_KV_EMPTY = 1 + kSlots,     // +slot
+  BAR_S_FULL = 1 + 2 * kSlots,   // +query tile
+  BAR_P_FULL = 3 + 2 * kSlots,   // +query tile
+  BAR_O_DONE = 5 + 2 * kSlots,   // +query tile
+  BAR_DRAIN = 7 + 2 * kSlots,
+  NUM_BARS = 8 + 2 * kSlots
 };
 
 template <int D>
@@ -74,9 +79,8 @@ struct FwdSmem {
   static constexpr uint32_t kQ = BM * D * 2;
   static constexpr uint32_t kKV = BN * D * 2;
   static constexpr uint32_t offQ = 0;                 // two query tiles
-  static constexpr uint32_t offK = offQ + 2 * kQ;     // two stages
-  static constexpr uint32_t offV = offK + 2 * kKV;    // two stages
-  static constexpr uint32_t offBar = offV + 2 * kKV;
+  static constexpr uint32_t offKV = offQ + 2 * kQ;    // kSlots K/V slots
+  static constexpr uint32_t offBar = offKV + kSlots * kKV;
   static constexpr uint32_t offMisc = offBar + NUM_BARS * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   // 1 KB alignment slack; D=64 is padded so that one CTA (and one 512-column
@@ -131,7 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + SM::offQ, sK = s_base + SM::offK, sV = s_base + SM::offV;
+  const uint32_t sQ = s_base + SM::offQ, sKV = s_base + SM::offKV;
+  // Load n of the K/V sequence (K of tile j is load 2j, V of tile j is 2j+1).
+  auto slot_of = [](int n) { return n % kSlots; };
+  auto parity_of = [](int n) { return static_cast<uint32_t>((n / kSlots) & 1); };
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
@@ -163,11 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar(BAR_KV_FULL + i), 1);
+      mbar_init(bar(BAR_KV_EMPTY + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_K_FULL + i), 1);
-      mbar_init(bar(BAR_K_EMPTY + i), 1);
-      mbar_init(bar(BAR_V_FULL + i), 1);
-      mbar_init(bar(BAR_V_EMPTY + i), 1);
       mbar_init(bar(BAR_S_FULL + i), 1);
       mbar_init(bar(BAR_P_FULL + i), 4);
       mbar_init(bar(BAR_O_DONE + i), 1);
@@ -200,27 +207,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
-      int nk = 0, nv = 0;
+      int n = 0;  // loads issued
+      auto load = [&](const CUtensorMap* map, int kv_row) -> bool {
+        const int sl = slot_of(n);
+        if (!mbar_wait(bar(BAR_KV_EMPTY + sl), parity_of(n) ^ 1, abort_flag, status)) return false;
+        mbar_arrive_expect_tx(bar(BAR_KV_FULL + sl), SM::kKV);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sKV + sl * SM::kKV + hh * HALF_BYTES, map, bar(BAR_KV_FULL + sl), hkv * D + hh * 64, kv_row);
+        ++n;
+        return true;
+      };
       for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row, int, int) {
         if (*abort_flag) return;
-        const int st = nk & 1;
-        const uint32_t ph = ((nk >> 1) & 1) ^ 1;
-        if (!mbar_wait(bar(BAR_K_EMPTY + st), ph, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(BAR_K_FULL + st), SM::kKV);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sK + st * SM::kKV + hh * HALF_BYTES, &tm_k, bar(BAR_K_FULL + st), hkv * D + hh * 64, kv_row);
-        ++nk;
-        if (!mbar_wait(bar(BAR_V_EMPTY + st), ph, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(BAR_V_FULL + st), SM::kKV);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sV + st * SM::kKV + hh * HALF_BYTES, &tm_v, bar(BAR_V_FULL + st), hkv * D + hh * 64, kv_row);
-        ++nv;
+        if (load(&tm_k, kv_row)) load(&tm_v, kv_row);
       });
       if (*abort_flag) {
         // Let every copy still in flight land before the CTA exits.
         mbar_wait(bar(BAR_Q), 0, nullptr, status);
-        for (int i = max(0, nk - 2); i < nk; ++i) mbar_wait(bar(BAR_K_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
-        for (int i = max(0, nv - 2); i < nv; ++i) mbar_wait(bar(BAR_V_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
+        for (int i = max(0, n - kSlots); i < n; ++i) mbar_wait(bar(BAR_KV_FULL + slot_of(i)), parity_of(i), nullptr, status);
       }
     }
   } else if (warp == 1) {
@@ -229,61 +233,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
       int npv[2] = {0, 0};      // PVs issued per query tile
-      int pend_st = -1;         // V stage of a PV1 still to issue
+      int pend_sl = -1;         // V slot of a PV1 still to issue
       uint32_t pend_ph = 0;
-      auto issue_qk = [&](int t, uint32_t kb) {
-        const uint32_t qb = sQ + t * SM::kQ;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 128 * t, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc_qk,
-                      kk > 0 ? 1u : 0u);
-        }
+      bool pend_ready = false;  // that V load was already waited for
+      // Descriptors are built once; each MMA only adds a compile-time offset
+      // to the start-address field (addresses stay below 256 KB, so the
+      // 14-bit field never carries).  This thread shares its scheduler with
+      // softmax warps, so every instruction it saves shortens the critical
+      // path of the tensor core.
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sQ + SM::kQ, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sKV, 16, 1024);          // slot 0 read as K (K-major)
+      const uint64_t dv0 = smem_desc_sw128(sKV, HALF_BYTES, 1024);  // slot 0 read as V (MN-major)
+      constexpr uint64_t kSlotStep = SM::kKV >> 4;
+      auto issue_qk = [&](int t, int slot) {
+        const uint64_t a0 = t ? dq1 : dq0;
+        const uint64_t b0 = dk0 + static_cast<uint64_t>(slot) * kSlotStep;
+        if constexpr (D == 128)
+          mma_bf16_ss_k128<HALF_BYTES>(tmem + 128 * t, a0, b0, idesc_qk, 0u);
+        else
+          mma_bf16_ss_k64(tmem + 128 * t, a0, b0, idesc_qk, 0u);
         mma_commit(bar(BAR_S_FULL + t));
       };
       // O_t += P_t V: A = P_t in TMEM (8 columns per 16 keys), B = V [keys x d]
       // read as N=d x K=keys, MN-major (16 keys = 16 rows of 128 bytes; the two
       // 64-column halves of d are HALF_BYTES apart).
-      auto issue_pv = [&](int t, int st, uint32_t ph, bool release_v) -> bool {
+      // V slot of the load a PV reads; `v_ready` skips the wait when the other
+      // tile's PV of the same key tile already saw that load land.
+      auto issue_pv = [&](int t, int sl, uint32_t ph, bool v_ready, bool release_v) -> bool {
         if (!mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status)) return false;
-        if (!mbar_wait(bar(BAR_V_FULL + st), ph, abort_flag, status)) return false;
+        if (!v_ready && !mbar_wait(bar(BAR_KV_FULL + sl), ph, abort_flag, status)) return false;
         tc_fence_after();
-        const uint32_t vb = sV + st * SM::kKV;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + 256 + D * t, tmem + 128 * t + kk * 8, smem_desc_sw128(vb + kk * 2048, HALF_BYTES, 1024),
-                      idesc_pv, (npv[t] > 0 || kk > 0) ? 1u : 0u);
+        const uint64_t b0 = dv0 + static_cast<uint64_t>(sl) * kSlotStep;
+        mma_bf16_ts_k128(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
         mma_commit(bar(BAR_O_DONE + t));
-        if (release_v) mma_commit(bar(BAR_V_EMPTY + st));
+        if (release_v) mma_commit(bar(BAR_KV_EMPTY + sl));
         ++npv[t];
         return true;
       };
       int j = 0;
+      int ring_slot = 0;        // slot of the next K load
+      uint32_t ring_ph = 0;     // its phase parity
       bool ok = mbar_wait(bar(BAR_Q), 0, abort_flag, status);
       if (ok) {
         for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int, int kpos0, int klen) {
           if (!ok || *abort_flag) return;
           const bool v0 = win0.sees(kpos0, klen), v1 = win1.sees(kpos0, klen);
-          const int st = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!(ok = mbar_wait(bar(BAR_K_FULL + st), ph, abort_flag, status))) return;
+          // K of tile j is load 2j, V is load 2j+1 (slots advance by one per load).
+          const int kslot = ring_slot, vslot = ring_slot + 1 == kSlots ? 0 : ring_slot + 1;
+          const uint32_t kph = ring_ph, vph = ring_slot + 1 == kSlots ? ring_ph ^ 1u : ring_ph;
+          ring_slot = vslot + 1 == kSlots ? 0 : vslot + 1;
+          ring_ph = vslot + 1 == kSlots ? vph ^ 1u : vph;
+          if (!(ok = mbar_wait(bar(BAR_KV_FULL + kslot), kph, abort_flag, status))) return;
           tc_fence_after();
-          const uint32_t kb = sK + st * SM::kKV;
-          if (v0) issue_qk(0, kb);
-          if (pend_st >= 0) {
-            if (!(ok = issue_pv(1, pend_st, pend_ph, true))) return;
-            pend_st = -1;
+          if (v0) issue_qk(0, kslot);
+          if (pend_sl >= 0) {
+            if (!(ok = issue_pv(1, pend_sl, pend_ph, pend_ready, true))) return;
+            pend_sl = -1;
           }
-          if (v1) issue_qk(1, kb);
-          mma_commit(bar(BAR_K_EMPTY + st));
-          if (v0 && !(ok = issue_pv(0, st, ph, !v1))) return;
+          if (v1) issue_qk(1, kslot);
+          mma_commit(bar(BAR_KV_EMPTY + kslot));
+          if (v0 && !(ok = issue_pv(0, vslot, vph, false, !v1))) return;
           if (v1) {
-            pend_st = st;
-            pend_ph = ph;
+            pend_sl = vslot;
+            pend_ph = vph;
+            pend_ready = v0;
           }
           ++j;
         });
-        if (ok && pend_st >= 0 && !*abort_flag) issue_pv(1, pend_st, pend_ph, true);
+        if (ok && pend_sl >= 0 && !*abort_flag) issue_pv(1, pend_sl, pend_ph, pend_ready, true);
       }
       // Every MMA issued so far completes before TMEM and shared memory are released.
       mma_commit(bar(BAR_DRAIN));
