@@ -362,21 +362,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mb = (m == -INFINITY) ? 0.f : m;
       // P = exp2(S*scale*log2e - m) -> packed bf16 into the first 64 columns
       // of S (already read into registers).
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      // Pairs of columns go through packed fp32x2 fma/add (half the issue
+      // slots of scalar code); exp2 stays per element on the MUFU pipe.
+      const f32x2 sl2x2 = make_f32x2(sl2, sl2), nmbx2 = make_f32x2(-mb, -mb);
+      f32x2 rs2[4] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(x[c * 32 + e], sl2, -mb));
-          const float p1 = ex2_approx(fmaf(x[c * 32 + e + 1], sl2, -mb));
-          rs4[(e >> 1) & 3] += p0 + p1;
+          float a0, a1;
+          split_f32x2(fma_f32x2(make_f32x2(x[c * 32 + e], x[c * 32 + e + 1]), sl2x2, nmbx2), a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          rs2[(e >> 1) & 3] = add_f32x2(rs2[(e >> 1) & 3], make_f32x2(p0, p1));
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tSt + c * 16, pk);
       }
       tmem_wait_st();
-      l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      float rs_lo[4], rs_hi[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) split_f32x2(rs2[i], rs_lo[i], rs_hi[i]);
+      l = l * alpha + (((rs_lo[0] + rs_hi[0]) + (rs_lo[1] + rs_hi[1])) + ((rs_lo[2] + rs_hi[2]) + (rs_lo[3] + rs_hi[3])));
       // O is stable here: this tile's S_FULL commit came after the previous PV_t.
       if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1

@@ -8,10 +8,12 @@
 // Both layouts are sequences of contiguous blocks:
 //   token-major: a block is one token's H/U heads (H/U * E elements),
 //   head-major (LSE): a block is one head's n tokens.
-// The kernel walks the OUTPUT in order, one 16-byte (or 4-byte) vector per
-// thread and several vectors in flight per thread, so every write is fully
-// coalesced and every read is a contiguous run of at least one block.  It is
-// bandwidth-bound; the grid is a multiple of the SM count.
+// The kernel walks the OUTPUT in order.  One warp copies one block at a time
+// (lanes take consecutive 16-byte vectors, or 4-byte words when a block is
+// not a multiple of 16 bytes), so reads and writes are both contiguous and
+// fully coalesced; the block's source offset is computed once per block, not
+// per vector.  Each warp keeps four blocks in flight.  HBM-bound; the grid
+// is a multiple of the SM count.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,76 +25,77 @@ namespace cpattn {
 namespace {
 
 struct ReshardGeom {
-  long long R, U, n, H, Hl;  // Hl = H / U
-  long long blk;             // block size in vectors
+  uint32_t U, n, H, Hl;  // Hl = H / U
+  uint32_t blk;          // block size in vectors
+  uint32_t nblocks;      // output blocks
   int dir, kind;
 };
 
-// Input vector offset of output block `ob` (in units of vectors).
-__device__ __forceinline__ long long in_block(const ReshardGeom& g, long long ob) {
-  const long long U = g.U, n = g.n, H = g.H, Hl = g.Hl;
+// Source block index of output block `ob`.
+__device__ __forceinline__ uint32_t in_block(const ReshardGeom& g, uint32_t ob) {
+  const uint32_t U = g.U, n = g.n, H = g.H, Hl = g.Hl;
   if (g.kind == CP_TOKEN_MAJOR) {
     if (g.dir == CP_SEQ_TO_HEAD) {
       // out [r][u][s*n+t] (block = Hl heads)  <-  in [r][s][t][u*Hl ..]
-      const long long t = ob % n;
-      long long x = ob / n;
-      const long long s = x % U;
+      const uint32_t t = ob % n;
+      uint32_t x = ob / n;
+      const uint32_t s = x % U;
       x /= U;
-      const long long u = x % U;
-      const long long r = x / U;
-      return (((r * U + s) * n + t) * U + u) * g.blk;  // in row has H = U*Hl heads = U blocks
-    } else {
-      // out [r][s][t][u*Hl ..] (block index (r,s,t,u))  <-  in [r][u][s*n+t]
-      const long long u = ob % U;
-      long long x = ob / U;
-      const long long t = x % n;
-      x /= n;
-      const long long s = x % U;
-      const long long r = x / U;
-      return ((r * U + u) * U * n + s * n + t) * g.blk;
+      const uint32_t u = x % U;
+      const uint32_t r = x / U;
+      return ((r * U + s) * n + t) * U + u;  // an input row holds U blocks
     }
-  } else {
-    if (g.dir == CP_SEQ_TO_HEAD) {
-      // out [r][u][h'][s*n .. +n]  (block index (r,u,h',s))  <-  in [r][s][u*Hl+h'][0..n)
-      const long long s = ob % U;
-      long long x = ob / U;
-      const long long hl = x % Hl;
-      x /= Hl;
-      const long long u = x % U;
-      const long long r = x / U;
-      return ((r * U + s) * H + u * Hl + hl) * g.blk;
-    } else {
-      // out [r][s][h = u*Hl+h'][0..n)  (block index (r,s,h))  <-  in [r][u][h'][s*n ..]
-      const long long h = ob % H;
-      long long x = ob / H;
-      const long long s = x % U;
-      const long long r = x / U;
-      const long long u = h / Hl, hl = h % Hl;
-      return (((r * U + u) * Hl + hl) * U + s) * g.blk;
-    }
+    // out [r][s][t][u*Hl ..] (block (r,s,t,u))  <-  in [r][u][s*n+t]
+    const uint32_t u = ob % U;
+    uint32_t x = ob / U;
+    const uint32_t t = x % n;
+    x /= n;
+    const uint32_t s = x % U;
+    const uint32_t r = x / U;
+    return (r * U + u) * U * n + s * n + t;
   }
+  if (g.dir == CP_SEQ_TO_HEAD) {
+    // out [r][u][h'][s*n .. +n]  (block (r,u,h',s))  <-  in [r][s][u*Hl+h'][0..n)
+    const uint32_t s = ob % U;
+    uint32_t x = ob / U;
+    const uint32_t hl = x % Hl;
+    x /= Hl;
+    const uint32_t u = x % U;
+    const uint32_t r = x / U;
+    return (r * U + s) * H + u * Hl + hl;
+  }
+  // out [r][s][h = u*Hl+h'][0..n)  (block (r,s,h))  <-  in [r][u][h'][s*n ..]
+  const uint32_t h = ob % H;
+  uint32_t x = ob / H;
+  const uint32_t s = x % U;
+  const uint32_t r = x / U;
+  const uint32_t u = h / Hl, hl = h % Hl;
+  return ((r * U + u) * Hl + hl) * U + s;
 }
 
-template <typename V, int ILP>
-__global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, V* __restrict__ out,
-                                                      ReshardGeom g, long long total) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x * ILP;
-  for (long long base = (static_cast<long long>(blockIdx.x) * blockDim.x * ILP) + threadIdx.x; base < total;
-       base += stride) {
-    V v[ILP];
-    long long dst[ILP];
+constexpr int kBlocksInFlight = 4;
+
+template <typename V>
+__global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, V* __restrict__ out, ReshardGeom g) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t w0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  for (uint32_t base = w0 * kBlocksInFlight; base < g.nblocks; base += warps * kBlocksInFlight) {
+    uint64_t src[kBlocksInFlight];
 #pragma unroll
-    for (int i = 0; i < ILP; ++i) {
-      const long long o = base + static_cast<long long>(i) * blockDim.x;
-      dst[i] = o;
-      if (o < total) {
-        const long long ob = o / g.blk, w = o - ob * g.blk;
-        v[i] = __ldg(in + in_block(g, ob) + w);
-      }
+    for (int i = 0; i < kBlocksInFlight; ++i) {
+      const uint32_t ob = base + i;
+      src[i] = ob < g.nblocks ? static_cast<uint64_t>(in_block(g, ob)) * g.blk : 0;
     }
+    for (uint32_t v0 = lane; v0 < g.blk; v0 += 32) {
+      V val[kBlocksInFlight];
 #pragma unroll
-    for (int i = 0; i < ILP; ++i)
-      if (dst[i] < total) out[dst[i]] = v[i];
+      for (int i = 0; i < kBlocksInFlight; ++i)
+        if (base + i < g.nblocks) val[i] = __ldg(in + src[i] + v0);
+#pragma unroll
+      for (int i = 0; i < kBlocksInFlight; ++i)
+        if (base + i < g.nblocks) out[static_cast<uint64_t>(base + i) * g.blk + v0] = val[i];
+    }
   }
 }
 
@@ -111,33 +114,32 @@ int sm_count() {
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind, int elem_bytes,
                    const void* in, void* out, cudaStream_t stream) {
   ReshardGeom g;
-  g.R = R;
   g.U = U;
   g.n = n;
   g.H = H;
   g.Hl = H / U;
   g.dir = direction;
   g.kind = kind;
-  const long long block_bytes = (kind == CP_TOKEN_MAJOR) ? g.Hl * row_elems * elem_bytes
+  const long long block_bytes = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(g.Hl) * row_elems * elem_bytes
                                                          : static_cast<long long>(n) * elem_bytes;
-  const long long total_bytes = static_cast<long long>(R) * U * n * H * row_elems * elem_bytes;
-  if (total_bytes == 0) return CP_OK;
-  const int blocks_per_sm = 8, threads = 256;
-  const long long grid_cap = static_cast<long long>(sm_count()) * blocks_per_sm;
+  const long long nblocks = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(R) * U * n * U
+                                                     : static_cast<long long>(R) * U * H;
+  if (nblocks == 0 || block_bytes == 0) return CP_OK;
+  if (nblocks >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  g.nblocks = static_cast<uint32_t>(nblocks);
+  const int threads = 256, warps_per_cta = threads / 32;
+  const long long need = (nblocks + warps_per_cta * kBlocksInFlight - 1) / (warps_per_cta * kBlocksInFlight);
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  const int grid = static_cast<int>(need < cap ? need : cap);
   if (block_bytes % 16 == 0) {
-    g.blk = block_bytes / 16;
-    const long long total = total_bytes / 16;
-    const long long need = (total + threads * 4 - 1) / (threads * 4);
-    const int grid = static_cast<int>(need < grid_cap ? need : grid_cap);
-    reshard_kernel<uint4, 4><<<grid, threads, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), g,
-                                                           total);
+    if (block_bytes / 16 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+    g.blk = static_cast<uint32_t>(block_bytes / 16);
+    reshard_kernel<uint4><<<grid, threads, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
   } else if (block_bytes % 4 == 0) {
-    g.blk = block_bytes / 4;
-    const long long total = total_bytes / 4;
-    const long long need = (total + threads * 4 - 1) / (threads * 4);
-    const int grid = static_cast<int>(need < grid_cap ? need : grid_cap);
-    reshard_kernel<uint32_t, 4><<<grid, threads, 0, stream>>>(static_cast<const uint32_t*>(in),
-                                                              static_cast<uint32_t*>(out), g, total);
+    if (block_bytes / 4 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+    g.blk = static_cast<uint32_t>(block_bytes / 4);
+    reshard_kernel<uint32_t><<<grid, threads, 0, stream>>>(static_cast<const uint32_t*>(in),
+                                                           static_cast<uint32_t*>(out), g);
   } else {
     return CP_ERR_UNSUPPORTED;
   }
