@@ -23,6 +23,10 @@
 // nougat.kr "MaxText long-context training and KV parallelism", "Split heads
 // or rotate KV": the chunk's partial results travel with it).
 //
+// The kernels read the head-sharded layout of the Ulysses exchange (rank
+// a = r*U + u holds ring rank r's slots for head group u; U == 1 is plain
+// sequence sharding); the ring runs over r within each head group.
+//
 // Warp roles as in the forward: warp 0 TMA producer, warp 1 TMEM allocator
 // and MMA issuer, warps 2..5 element-wise (one TMEM lane = one row each).
 #include <cuda.h>
@@ -73,6 +77,15 @@ __device__ __forceinline__ void store_row32_packed(uint32_t tile, int row, int c
   }
 }
 
+// Q K^T-type product over d: A and B both K-major, 128-byte swizzled.
+template <int D>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+  if constexpr (D == 128)
+    mma_bf16_ss_k128<HALF_BYTES>(d_tmem, a, b, idesc, 0u);
+  else
+    mma_bf16_ss_k64(d_tmem, a, b, idesc, 0u);
+}
+
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -120,7 +133,7 @@ struct DqSmem {
 };
 
 template <typename F>
-__device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int lo_min, int qpos_last, F&& f) {
+__device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int lo_min, int qpos_last, F&& f) {
   const int nchunks = (g.layout == CP_LAYOUT_CONTIGUOUS) ? 1 : 2;
   for (int s = 0; s < g.R; ++s) {
     const int src = (r - s + g.R) % g.R;
@@ -132,7 +145,7 @@ __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int l
       if (lo > hi) continue;
       const int t1 = (hi - cpos0) / BN;
       for (int t = (lo - cpos0) / BN; t <= t1; ++t)
-        f(src * g.T + cslot0 + t * BN, cpos0 + t * BN, min(BN, g.chunk - t * BN));
+        f((src * g.U + u) * g.T + cslot0 + t * BN, cpos0 + t * BN, min(BN, g.chunk - t * BN));
     }
   }
 }
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hq = g.Hq_loc;
   const WorkItem it = args.items_q[blockIdx.x / Hq];
   const int h = blockIdx.x % Hq;
-  const int r = it.a;  // U == 1
+  const int a = it.a, r = a / g.U, u = a % g.U;  // rank a = ring rank r, Ulysses member u
   const int qpos0 = slot_pos(g, r, it.q0);
   const int qpos_last = qpos0 + it.len - 1;
   const int lo_min = g.doc_start ? g.doc_start[qpos0] : 0;
@@ -195,13 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(DQ_QD_FULL), 2 * SM::kT);
-      const int qrow = r * g.T + it.q0;
+      const int qrow = a * g.T + it.q0;
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
         tma_load_2d(sDO + hh * HALF_BYTES, &tm_do, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
       }
       int nk = 0, nv = 0;
-      for_each_kv_tile(g, r, lo_min, qpos_last, [&](int kv_row, int, int) {
+      for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int kv_row, int, int) {
         if (*abort_flag) return;
         const int st = nk & 1;
         const uint32_t ph = ((nk >> 1) & 1) ^ 1;
@@ -226,9 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, D, 1);
+      // Descriptors built once; stage st adds st * tile bytes (>> 4).
+      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024), dDS = smem_desc_sw128(sDS, 16, 1024);
       int n = 0;
       if (mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status)) {
-        for_each_kv_tile(g, r, lo_min, qpos_last, [&](int, int, int) {
+        for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int, int) {
           if (*abort_flag) return;
           const int st = n & 1;
           const uint32_t ph = (n >> 1) & 1;
@@ -236,30 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(DQ_V_FULL + st), ph, abort_flag, status)) return;
           if (!mbar_wait(bar(DQ_SP_EMPTY), (n & 1) ^ 1, abort_flag, status)) return;
           tc_fence_after();
-          const uint32_t kb = sK + st * SM::kT, vb = sV + st * SM::kT;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc_s,
-                        kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tdP, smem_desc_sw128(sDO + off, 16, 1024), smem_desc_sw128(vb + off, 16, 1024), idesc_s,
-                        kk > 0 ? 1u : 0u);
-          }
+          const uint64_t step = static_cast<uint64_t>(st) * (SM::kT >> 4);
+          mma_qk<D>(tS, dQ0, dK0 + step, idesc_s);
+          mma_qk<D>(tdP, dDO0, dV0 + step, idesc_s);
           mma_commit(bar(DQ_SP_FULL));
           mma_commit(bar(DQ_V_EMPTY + st));
           if (!mbar_wait(bar(DQ_DS_FULL), n & 1, abort_flag, status)) return;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // A = dS [queries x keys] K-major; B = K [keys x d] read as N=d x K=keys (MN-major).
-            const uint64_t ad = smem_desc_sw128(sDS + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kb + kk * 2048, HALF_BYTES, 1024);
-            mma_bf16_ss(tdQ, ad, bd, idesc_dq, (n > 0 || kk > 0) ? 1u : 0u);
-          }
+          // A = dS [queries x keys] K-major; B = K [keys x d] read as N=d x K=keys (MN-major).
+          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + step, idesc_dq, n > 0 ? 1u : 0u);
           mma_commit(bar(DQ_K_EMPTY + st));
           mma_commit(bar(DQ_DONE));
           ++n;
@@ -275,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = row < it.len;
     const int my_pos = row_valid ? qpos0 + row : -1;
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
-    const size_t lrow = (static_cast<size_t>(r) * Hq + h) * g.T + it.q0 + row;
+    const size_t lrow = (static_cast<size_t>(a) * Hq + h) * g.T + it.q0 + row;
     const float lse2 = row_valid ? args.lse[lrow] * kLog2e : INFINITY;
     const float dlt = row_valid ? args.delta[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
     int n = 0;
     bool ok = true;
-    for_each_kv_tile(g, r, lo_min, qpos_last, [&](int, int kpos0, int klen) {
+    for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int kpos0, int klen) {
       if (!ok) return;
       ok = warp_all(mbar_wait(bar(DQ_SP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      float* dst = args.dq + (static_cast<size_t>(r * g.T + it.q0 + row) * Hq + h) * D;
+      float* dst = args.dq + (static_cast<size_t>(a * g.T + it.q0 + row) * Hq + h) * D;
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t v[32];
         if (n > 0) {
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hkv = g.Hkv_loc, Hq = g.Hq_loc;
   const WorkItem it = args.items_kv[blockIdx.x / Hkv];
   const int jh = blockIdx.x % Hkv;
-  const int src = it.a;
+  const int a = it.a, src = a / g.U, u = a % g.U;  // key tile of rank a = ring rank src, member u
   const int kpos0 = slot_pos(g, src, it.q0);
   const int kpos_last = kpos0 + it.len - 1;
   const int hi_max = g.doc_end ? g.doc_end[kpos_last] - 1 : g.L - 1;
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(KV_FULL), 2 * SM::kT);
-      const int krow = src * g.T + it.q0;
+      const int krow = a * g.T + it.q0;
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = ((nq >> 1) & 1) ^ 1;
         if (!mbar_wait(bar(KV_QD_EMPTY + st), ph, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(KV_QD_FULL + st), 2 * SM::kT);
-        const int qrow = rr * g.T + qslot0;
+        const int qrow = (rr * g.U + u) * g.T + qslot0;
         for (int hh = 0; hh < NH; ++hh) {
           tma_load_2d(sQ + st * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_QD_FULL + st), h * D + hh * 64, qrow);
           tma_load_2d(sDO + st * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_QD_FULL + st), h * D + hh * 64, qrow);
@@ -473,6 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(BM, D, 1);
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dQmn0 = smem_desc_sw128(sQ, HALF_BYTES, 1024), dDOmn0 = smem_desc_sw128(sDO, HALF_BYTES, 1024);
+      const uint64_t dPB = smem_desc_sw128(sPB, 16, 1024);
       int n = 0;
       if (mbar_wait(bar(KV_FULL), 0, abort_flag, status)) {
         for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int, int, int, int, int) {
@@ -481,38 +487,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(KV_QD_FULL + st), (n >> 1) & 1, abort_flag, status)) return;
           if (!mbar_wait(bar(KV_ST_EMPTY), (n & 1) ^ 1, abort_flag, status)) return;
           tc_fence_after();
-          const uint32_t qb = sQ + st * SM::kT, db = sDO + st * SM::kT;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tSt, smem_desc_sw128(sK + off, 16, 1024), smem_desc_sw128(qb + off, 16, 1024), idesc_s,
-                        kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tdPt, smem_desc_sw128(sV + off, 16, 1024), smem_desc_sw128(db + off, 16, 1024), idesc_s,
-                        kk > 0 ? 1u : 0u);
-          }
+          const uint64_t step = static_cast<uint64_t>(st) * (SM::kT >> 4);
+          mma_qk<D>(tSt, dK0, dQ0 + step, idesc_s);
+          mma_qk<D>(tdPt, dV0, dDO0 + step, idesc_s);
           mma_commit(bar(KV_ST_FULL));
           if (!mbar_wait(bar(KV_PT_FULL), n & 1, abort_flag, status)) return;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            // A = P^T [keys x queries] K-major; B = dO [queries x d] as N=d x K=queries (MN-major).
-            const uint64_t ad = smem_desc_sw128(sPB + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tdV, ad, smem_desc_sw128(db + kk * 2048, HALF_BYTES, 1024), idesc_acc,
-                        (n > 0 || kk > 0) ? 1u : 0u);
-          }
+          // A = P^T [keys x queries] K-major; B = dO [queries x d] as N=d x K=queries (MN-major).
+          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + step, idesc_acc, n > 0 ? 1u : 0u);
           mma_commit(bar(KV_PB_FREE));
           if (!mbar_wait(bar(KV_DS_FULL), n & 1, abort_flag, status)) return;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sPB + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tdK, ad, smem_desc_sw128(qb + kk * 2048, HALF_BYTES, 1024), idesc_acc,
-                        (n > 0 || kk > 0) ? 1u : 0u);
-          }
+          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + step, idesc_acc, n > 0 ? 1u : 0u);
           mma_commit(bar(KV_QD_EMPTY + st));
           mma_commit(bar(KV_ACC_DONE));
           ++n;
@@ -538,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // barriers on every tile, also after an abort, so they stay balanced.
       named_bar_sync(1, 128);  // everyone finished reading the previous tile's values
       {
-        const size_t li = (static_cast<size_t>(rr) * Hq + h) * g.T + qslot0 + etid;
+        const size_t li = (static_cast<size_t>(rr * g.U + u) * Hq + h) * g.T + qslot0 + etid;
         sLse[etid] = etid < qlen ? args.lse[li] * kLog2e : INFINITY;
         sDel[etid] = etid < qlen ? args.delta[li] : 0.f;
       }
@@ -605,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      const size_t orow = (static_cast<size_t>(src * g.T + it.q0 + row) * Hkv + jh) * D;
+      const size_t orow = (static_cast<size_t>(a * g.T + it.q0 + row) * Hkv + jh) * D;
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t v[32], k[32];
         if (n > 0) {
@@ -643,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const AttnGeom& g = a.g;
-  const uint64_t rows = static_cast<uint64_t>(g.R) * g.T;
+  const uint64_t rows = static_cast<uint64_t>(g.R) * g.U * g.T;
   CUtensorMap mq, mdo, mk, mv;
   if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
       !make_tile_map(&mdo, a.dO, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
@@ -689,7 +675,6 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
-  if (a.g.U != 1) return CP_ERR_UNSUPPORTED;
   if (a.d == 128) return launch_bwd_d<128>(a, stream);
   if (a.d == 64) return launch_bwd_d<64>(a, stream);
   return CP_ERR_UNSUPPORTED;

@@ -157,16 +157,16 @@ int visited_q_tiles(const cp_plan* p, const AttnGeom& g, int src, int k0, int le
   return count;
 }
 
-// Key tiles of every ring rank, ordered by descending work.
+// Key tiles of every attention rank a = src * U + u, ordered by descending work.
 std::vector<WorkItem> build_kv_items(const cp_plan* p) {
   const AttnGeom g = geom(p);
   std::vector<std::pair<int, WorkItem>> v;
-  for (int src = 0; src < g.R; ++src)
+  for (int a = 0; a < g.R * g.U; ++a)
     for (int ch = 0; ch < p->nchunks; ++ch)
       for (int t0 = 0; t0 < p->chunk; t0 += kTile) {
         const int k0 = ch * p->chunk + t0;
         const int len = std::min(kTile, p->chunk - t0);
-        v.push_back({visited_q_tiles(p, g, src, k0, len), WorkItem{src, k0, len, -1}});
+        v.push_back({visited_q_tiles(p, g, a / g.U, k0, len), WorkItem{a, k0, len, -1}});
       }
   std::stable_sort(v.begin(), v.end(), [](const std::pair<int, WorkItem>& x, const std::pair<int, WorkItem>& y) {
     return x.first > y.first;
@@ -222,8 +222,36 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
   return w;
 }
 
-size_t bwd_workspace(const cp_plan* p) {
-  return align256(static_cast<size_t>(p->desc.L) * p->desc.Hq * 4);  // delta = rowsum(dO * O)
+struct BwdWorkspace {
+  size_t delta, qh, kh, vh, oh, doh, lseh, dqh, dkh, dvh, total;
+};
+
+// delta = rowsum(dO * O) always; with U > 1 also the head-sharded copies of
+// the inputs and gradients.
+BwdWorkspace bwd_workspace(const cp_plan* p) {
+  const cp_plan_desc_t& d = p->desc;
+  const size_t L = d.L;
+  BwdWorkspace w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  w.delta = take(L * d.Hq * 4);
+  if (d.ulysses_degree > 1) {
+    w.qh = take(L * d.Hq * d.d * 2);
+    w.kh = take(L * d.Hkv * d.d * 2);
+    w.vh = take(L * d.Hkv * d.d * 2);
+    w.oh = take(L * d.Hq * d.d * (d.out_fp32 ? 4 : 2));
+    w.doh = take(L * d.Hq * d.d * 2);
+    w.lseh = take(L * d.Hq * 4);
+    w.dqh = take(L * d.Hq * d.d * 4);
+    w.dkh = take(L * d.Hkv * d.d * 4);
+    w.dvh = take(L * d.Hkv * d.d * 4);
+  }
+  w.total = off;
+  return w;
 }
 
 }  // namespace
@@ -309,7 +337,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     std::vector<WorkItem> fused = build_items(p, false, 2 * kTile);
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
-    if (rc == CP_OK && U == 1) {
+    if (rc == CP_OK) {
       std::vector<WorkItem> qt = build_items(p, false, kTile);
       p->n_items_q = static_cast<int>(qt.size());
       rc = upload(qt, &p->d_items_q);
@@ -319,7 +347,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       p->n_items_steps = static_cast<int>(steps.size());
       rc = upload(steps, &p->d_items_steps);
     }
-    if (rc == CP_OK && U == 1) {
+    if (rc == CP_OK) {
       std::vector<WorkItem> kv = build_kv_items(p);
       p->n_items_kv = static_cast<int>(kv.size());
       rc = upload(kv, &p->d_items_kv);
@@ -368,7 +396,7 @@ int cp_workspace_size(const cp_plan_t* p, int op, size_t* bytes) {
   if (op == CP_OP_FWD)
     *bytes = fwd_workspace(p).total;
   else if (op == CP_OP_BWD)
-    *bytes = bwd_workspace(p);
+    *bytes = bwd_workspace(p).total;
   else
     return CP_ERR_INVALID_ARG;
   return CP_OK;
@@ -484,11 +512,11 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (workspace && !aligned16(workspace)))
     return CP_ERR_ALIGNMENT;
-  if (p->desc.ulysses_degree != 1) return CP_ERR_UNSUPPORTED;
   int rc = check_device(p);
   if (rc != CP_OK) return rc;
-  const size_t need = bwd_workspace(p);
-  if (!workspace || workspace_bytes < need) return CP_ERR_WORKSPACE;
+  const BwdWorkspace w = bwd_workspace(p);
+  if (!workspace || workspace_bytes < w.total) return CP_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   cpattn::BwdArgs a{};
   a.g = geom(p);
   a.q = q;
@@ -501,7 +529,7 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.delta = static_cast<float*>(workspace);
+  a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.items_q = p->d_items_q;
   a.n_items_q = p->n_items_q;
   a.items_kv = p->d_items_kv;
@@ -509,7 +537,34 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.d = p->desc.d;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;
-  return cpattn::launch_attn_bwd(a, stream);
+  const cp_plan_desc_t& d = p->desc;
+  if (d.ulysses_degree == 1) return cpattn::launch_attn_bwd(a, stream);
+  // Ulysses / USP: the forward's exchanges run in reverse for the gradients.
+  // Inputs (q, k, v, o, dO, LSE) go to the head-sharded layout, the ring
+  // backward runs per head group, and dQ, dK, dV come back token-sharded.
+  const int R = d.ring_degree, U = d.ulysses_degree, n = p->n;
+  const int ob = d.out_fp32 ? 4 : 2;
+  if ((rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh, stream)))
+    return rc;
+  a.q = ws + w.qh;
+  a.k = ws + w.kh;
+  a.v = ws + w.vh;
+  a.o = ws + w.oh;
+  a.dO = ws + w.doh;
+  a.lse = reinterpret_cast<const float*>(ws + w.lseh);
+  a.dq = reinterpret_cast<float*>(ws + w.dqh);
+  a.dk = reinterpret_cast<float*>(ws + w.dkh);
+  a.dv = reinterpret_cast<float*>(ws + w.dvh);
+  if ((rc = cpattn::launch_attn_bwd(a, stream))) return rc;
+  if ((rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq, stream)) ||
+      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk, stream)))
+    return rc;
+  return cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv, stream);
 }
 
 int cp_merge_lse(int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts, void* o_out,

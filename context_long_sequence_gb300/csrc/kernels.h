@@ -52,15 +52,17 @@ struct FwdArgs {
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
-// Backward (U == 1).  items_q: query tiles (all ring steps), as the forward's
-// fused list; items_kv: key tiles {a = owner rank, q0 = first slot, len, -1}.
+// Backward on the head-sharded layout of cp_attn_fwd_local (rank a = r*U+u;
+// with U == 1 that is the sequence-sharded layout).  items_q: 128-row query
+// tiles (all ring steps); items_kv: key tiles {a = owner rank, q0 = first
+// slot, len, -1}.
 struct BwdArgs {
   AttnGeom g;
   const void* q;  const void* k;  const void* v;
   const void* o;  const float* lse;  const void* dO;
   int o_fp32;     // o is fp32 instead of bf16
   float* dq;  float* dk;  float* dv;
-  float* delta;   // [R][Hq][T] workspace: rowsum(dO * O)
+  float* delta;   // [R*U][Hq_loc][T] workspace: rowsum(dO * O)
   const WorkItem* items_q;
   int n_items_q;
   const WorkItem* items_kv;
@@ -72,7 +74,7 @@ struct BwdArgs {
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // Block-permutation copy behind ulysses_reshard.
-int launch_reshard(int R, int U, int n, int H, int row_bytes_total, int direction, int kind,
+int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind,
                    int elem_bytes, const void* in, void* out, cudaStream_t stream);
 
 // Merge of `n_parts` partials, `batch` independent groups laid out back to back.

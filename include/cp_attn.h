@@ -170,16 +170,21 @@ int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void 
 int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                       void *o, float *lse, cudaStream_t stream);
 
-/* Causal CP attention backward (U == 1) from the forward's O and LSE
- * (activation recompute, [L3P] "Long context changes more than attention
- * cost"): with P = exp(scale*QK^T - LSE),
+/* Causal CP attention backward from the forward's O and LSE (activation
+ * recompute, [L3P] "Long context changes more than attention cost"): with
+ * P = exp(scale*QK^T - LSE),
  *   D = rowsum(dO * O); dV = P^T dO; dS = P * (dO V^T - D);
  *   dQ = scale dS K;  dK = scale dS^T Q;  query heads sum into their KV head.
  * q, dO [P][n][Hq][d] bf16; o the same (fp32 if out_fp32); k, v [P][n][Hkv][d] bf16;
  * lse [P][Hq][n] fp32;
  * dq [P][n][Hq][d], dk, dv [P][n][Hkv][d] fp32 out (overwritten).
- * Gradients of a KV chunk land on the rank that owns the chunk.
- * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes. */
+ * Gradients of a KV chunk land on the rank that owns the chunk.  With U > 1
+ * (Ulysses, USP) the forward's exchanges run in reverse: q, k, v, o, dO and
+ * LSE are resharded to head sharding ([MTX] "Split heads or rotate KV"),
+ * the ring backward runs per head group, and dq, dk, dv are resharded back
+ * to token sharding.  Deterministic: no atomics, fixed summation order.
+ * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes (with U > 1 it holds
+ * the head-sharded copies: about 2x the inputs and gradients). */
 int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                 const void *o, const float *lse, const void *dO,
                 float *dq, float *dk, float *dv, void *workspace, size_t workspace_bytes,

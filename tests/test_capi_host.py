@@ -72,6 +72,10 @@ def test_workspace_sizes(cpa):
     p = cpa.Plan(16384, 32, 8, 128, ulysses_degree=4)
     L = 16384
     assert p.workspace_size(cpa.CP_OP_FWD) == al(L * 32 * 256) * 2 + al(L * 8 * 256) * 2 + al(L * 32 * 4)
+    # delta, then head-sharded q, k, v, o, dO (bf16), LSE, dq, dk, dv (fp32).
+    assert p.workspace_size(cpa.CP_OP_BWD) == (al(L * 32 * 4) + al(L * 32 * 256) * 3 + al(L * 8 * 256) * 2
+                                              + al(L * 32 * 4) + al(L * 32 * 512) + al(L * 8 * 512) * 2)
+    p = cpa.Plan(16384, 32, 8, 128, ring_degree=4)
     assert p.workspace_size(cpa.CP_OP_BWD) == al(L * 32 * 4)
     p = cpa.Plan(1024, 4, 4, 64, ring_degree=4, emit_partials=True)
     assert p.workspace_size(cpa.CP_OP_FWD) == al(4 * 1024 * 4 * 64 * 4) + al(4 * 1024 * 4 * 4)

@@ -1,6 +1,7 @@
 """GPU parity of the backward (dQ, dK, dV) against the fp64 oracle,
 element by element: GQA, zigzag and contiguous rings, ragged chunks, packed
 documents whose boundaries fall inside tiles, K scaled by 0.5; and
+Ulysses and USP plans (gradients resharded back through the exchanges);
 run-to-run determinism (no atomics)."""
 import os
 import sys
@@ -27,20 +28,24 @@ def cpa():
 
 
 CASES = [
-    # name, L, Hq, Hkv, d, R, layout, docs, k_scale
-    ("gqa_zigzag_d128", 1024, 4, 2, 128, 2, 1, None, 1.0),
-    ("ragged_docs_d64", 1000, 4, 1, 64, 2, 1, [0, 300, 301, 1000], 1.0),
-    ("contig_R3_docs_d128", 768, 2, 2, 128, 3, 0, [0, 200, 700, 768], 1.0),
-    ("ring_R8_zigzag_kscale", 2048, 8, 2, 128, 8, 1, None, 0.5),
+    # name, L, Hq, Hkv, d, U, R, layout, docs, k_scale
+    ("gqa_zigzag_d128", 1024, 4, 2, 128, 1, 2, 1, None, 1.0),
+    ("ragged_docs_d64", 1000, 4, 1, 64, 1, 2, 1, [0, 300, 301, 1000], 1.0),
+    ("contig_R3_docs_d128", 768, 2, 2, 128, 1, 3, 0, [0, 200, 700, 768], 1.0),
+    ("ring_R8_zigzag_kscale", 2048, 8, 2, 128, 1, 8, 1, None, 0.5),
+    # Ulysses and USP: gradients pass back through the exchanges.
+    ("ulysses_U4_gqa_d128", 1024, 8, 4, 128, 4, 1, 0, None, 1.0),
+    ("usp_U2xR2_zigzag_docs_d64", 1536, 8, 2, 64, 2, 2, 1, [0, 500, 520, 1536], 1.0),
+    ("usp_U2xR3_ragged_d128", 1440, 4, 2, 128, 2, 3, 0, [0, 711, 1440], 0.5),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_bwd_matches_oracle(cpa, case):
     import gpu_harness as gh
-    name, L, Hq, Hkv, d, R, layout, docs, ks = case
+    name, L, Hq, Hkv, d, U, R, layout, docs, ks = case
     inp = workloads.make_inputs(L, Hq, Hkv, d, zlib.crc32(name.encode()) % 1000, k_scale=ks, with_do=True)
-    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=R, layout=layout, doc_offsets=docs)
+    plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=layout, doc_offsets=docs)
     got = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
     _, _, dq, dk, dv = oracle.attention_bwd(inp["q"].double().numpy(), inp["k"].double().numpy(),
                                             inp["v"].double().numpy(), inp["do"].double().numpy(), offsets=docs)
@@ -67,3 +72,18 @@ def test_bwd_with_fp32_o(cpa):
                                             inp["v"].double().numpy(), inp["do"].double().numpy(),
                                             offsets=[0, 300, 768])
     gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], "fp32 O")
+
+
+def test_bwd_usp_deterministic_fp32_o(cpa):
+    """USP backward with an fp32 O: matches the oracle and repeats bit for bit."""
+    import gpu_harness as gh
+    docs = [0, 100, 1024]
+    inp = workloads.make_inputs(1024, 8, 4, 128, 31, with_do=True)
+    plan = cpa.Plan(1024, 8, 4, 128, ulysses_degree=2, ring_degree=2, layout=1, doc_offsets=docs, out_fp32=True)
+    a = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
+    b = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    _, _, dq, dk, dv = oracle.attention_bwd(inp["q"].double().numpy(), inp["k"].double().numpy(),
+                                            inp["v"].double().numpy(), inp["do"].double().numpy(), offsets=docs)
+    gh.assert_grads_close([g.numpy() for g in a], [dq, dk, dv], "usp fp32 O")

@@ -44,11 +44,12 @@ def _boundaries(w, offsets):
     return b
 
 
-def _run_fwd(cpa, w, dev="cuda", out_fp32=False):
+def _run_fwd(cpa, w, dev="cuda", out_fp32=False, with_do=False):
     offsets = workloads.workload_doc_offsets(w)
     plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
                     doc_offsets=offsets, emit_partials=w.emit_partials, out_fp32=out_fp32)
-    g = workloads.workload_inputs(w, device=dev)
+    g = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device=dev, k_scale=w.k_scale,
+                              with_do=w.backward or with_do)
     idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
     q, k, v = (g[n][idx].contiguous() for n in ("q", "k", "v"))
     o = torch.empty(q.shape, dtype=plan.o_dtype, device=dev)
@@ -86,10 +87,14 @@ def test_workload_forward_sampled(cpa, wi, out_fp32):
     gh.assert_close(O, LSE, O_ref, LSE_ref, w.name, bf16_out=not out_fp32)
 
 
-def test_workload_backward_sampled(cpa):
+@pytest.mark.parametrize("wi", [1, 2], ids=[workloads.WORKLOADS[i].name for i in (1, 2)])
+def test_workload_backward_sampled(cpa, wi):
+    """The ring backward at the ring workload's size, and the Ulysses
+    workload's shapes run backward through the exchanges (its dO drawn after
+    V like the ring workload's)."""
     import gpu_harness as gh
-    w = workloads.WORKLOADS[2]
-    plan, offsets, g, (q, k, v, o, lse), slot_of = _run_fwd(cpa, w)
+    w = workloads.WORKLOADS[wi]
+    plan, offsets, g, (q, k, v, o, lse), slot_of = _run_fwd(cpa, w, with_do=True)
     idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(q.device)
     do = g["do"][idx].contiguous()
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
@@ -107,7 +112,7 @@ def test_workload_backward_sampled(cpa):
     do_abs = do.double().abs().sum(dim=0).reshape(w.Hkv, G, w.d).sum(dim=1)
     assert ((dv_sum - do_sum).abs() <= 2.0 ** -8 * do_abs + 1e-3).all()
 
-    heads = _heads(w.Hq, 1)
+    heads = _heads(w.Hq, w.ulysses)
     kv_heads = sorted({h // G for h in heads})
     q_rows = workloads.sample_rows(w.L, _boundaries(w, offsets), 64, seed=w.seed + 1)
     key_rows = np.arange(w.L - 160, w.L, 3)
