@@ -203,6 +203,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="add the backward to every step (the ring fwd+bwd workload always has it)")
     ap.add_argument("--L", type=int, default=0,
                     help="override the workload's sequence length (small cases for profiling); 0 keeps it")
     args = ap.parse_args()
@@ -213,6 +215,8 @@ def main():
     w = workloads.WORKLOAD_BY_NAME[args.workload]
     if args.L:
         w = dataclasses.replace(w, L=args.L)
+    if args.backward:
+        w = dataclasses.replace(w, backward=True)
     offsets = workloads.workload_doc_offsets(w)
     flops_fwd = useful_flops(w, offsets)
     flops_step = int(flops_fwd * (1 + BWD_FLOP_RATIO)) if w.backward else flops_fwd
@@ -356,7 +360,8 @@ def main():
     if w.backward:
         bwd_ms = timed(bwd, reps)
         kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,
-                            "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"}
+                            "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"
+                                       + (" and 9 Ulysses reshards" if U > 1 else "")}
     if U > 1:
         def rin():
             cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh, stream=stream)
@@ -373,6 +378,18 @@ def main():
         kern["reshard_seq_to_head"] = {"ms": t_in, "gbs": bytes_in / t_in / 1e6, "bytes": bytes_in}
         kern["reshard_head_to_seq"] = {"ms": t_out, "gbs": bytes_out / t_out / 1e6, "bytes": bytes_out}
 
+    # Standalone LSE merge at one ring rank's shape of the 64K ring workload
+    # (8 ring-step partials of 8192 rows x 32 heads x 128): HBM-bound.
+    mp, mr, mh, md = 8, 8192, 32, 128
+    o_parts = torch.randn(mp, mr, mh, md, dtype=torch.float32, device=dev)
+    lse_parts = torch.randn(mp, mh, mr, dtype=torch.float32, device=dev)
+    o_m = torch.empty(mr, mh, md, dtype=torch.bfloat16, device=dev)
+    lse_m = torch.empty(mh, mr, dtype=torch.float32, device=dev)
+    t_merge = timed(lambda: cpa.cp_merge_lse(mp, mr, mh, md, o_parts, lse_parts, o_m, lse_m, stream=stream), reps)
+    merge_bytes = mp * mr * mh * (4 * md + 4) + mr * mh * (2 * md + 4)
+    kern["merge_8x8192x32x128"] = {"ms": t_merge, "gbs": merge_bytes / t_merge / 1e6, "bytes": merge_bytes}
+    del o_parts, lse_parts, o_m, lse_m
+
     peaks, peak_src = load_peaks()
     total_ms, e2e_ms_max, attn_ms_max = max_over_ranks([total_ms, e2e_ms, attn_ms], dist, dev)
 
@@ -380,7 +397,10 @@ def main():
     if rank == 0:
         ms_per_step = total_ms / args.steps
         value = aggregate_value(flops_step, world, ms_per_step)
-        launches_per_step = (6 if U > 1 else 1) + (1 if w.emit_partials else 0) + (3 if w.backward else 0)
+        # forward: 3 reshards in, attention, 2 reshards out (U > 1); merge with
+        # partials.  backward: delta, dkv, dq, plus 6 reshards in and 3 out (U > 1).
+        launches_per_step = ((6 if U > 1 else 1) + (1 if w.emit_partials else 0)
+                             + ((3 + (9 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         result = {
