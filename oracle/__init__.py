@@ -4,4 +4,5 @@ from .attention import (attention, attention_rows, attention_bwd, merge, merge_p
                         ring_forward, usp_forward, ring_positions, shard, unshard,
                         ulysses_seq_to_head, ulysses_head_to_seq, ulysses_lse_head_to_seq,
                         visible, doc_start_of, visible_pairs, rank_visible_pairs,
-                        LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG)  # noqa: F401
+                        chunk_work, balanced_chunks,
+                        LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG, LAYOUT_BALANCED)  # noqa: F401

@@ -257,16 +257,64 @@ def attention_bwd_rows(q, k, v, do, q_rows=(), key_rows=(), offsets=None, causal
 
 LAYOUT_CONTIGUOUS = 0
 LAYOUT_ZIGZAG = 1
+LAYOUT_BALANCED = 2
 
 
-def ring_positions(L: int, R: int, layout: int) -> np.ndarray:
+def chunk_work(L: int, n_chunks: int, offsets=None) -> np.ndarray:
+    """Attention work of each of n_chunks equal position chunks: the number
+    of visible (query, key) pairs whose query lies in the chunk.  A query at
+    position i sees i - doc_start(i) + 1 keys (causal, same document)."""
+    c = L // n_chunks
+    pos = np.arange(L, dtype=np.int64)
+    per_query = pos - doc_start_of(pos, offsets) + 1
+    return per_query.reshape(n_chunks, c).sum(axis=1)
+
+
+def balanced_chunks(L: int, R: int, chunks_per_rank: int, offsets=None):
+    """Chunk lists of the work-balanced layout ([L3P] "Long context changes
+    more than attention cost": split by actual attention work, not by
+    position; [MTX] "Split heads or rotate KV": causal load balancing).
+
+    Reading: the sequence is cut into C = m*R equal chunks (m =
+    chunks_per_rank).  Taking the chunks from most to least work (equal work:
+    lower chunk index first), each goes to the rank with the least work so
+    far among the ranks that still hold fewer than m chunks (equal work:
+    lower rank first).  Each rank keeps its chunks in position order.
+    Returns a list of R lists of chunk indices.
+    """
+    m = chunks_per_rank
+    C = m * R
+    if m < 1 or L % C:
+        raise ValueError("chunks_per_rank * R must divide L")
+    work = chunk_work(L, C, offsets)
+    order = sorted(range(C), key=lambda j: (-int(work[j]), j))
+    load = [0] * R
+    held = [[] for _ in range(R)]
+    for j in order:
+        best = None
+        for r in range(R):
+            if len(held[r]) < m and (best is None or load[r] < load[best]):
+                best = r
+        held[best].append(j)
+        load[best] += int(work[j])
+    return [sorted(h) for h in held]
+
+
+def ring_positions(L: int, R: int, layout: int, offsets=None, chunks_per_rank: int = 4) -> np.ndarray:
     """Global position of every slot, rank-major: out[r*(L/R) + t].
 
     Contiguous: rank r holds positions [r*L/R, (r+1)*L/R).
     Zigzag (the reading of [MTX] "Split heads or rotate KV" / [L3P] "Long
     context": balance by actual attention work): the sequence is cut into 2R
     chunks of c = L/(2R); rank r holds chunk r followed by chunk 2R-1-r.
+    Balanced: the chunks of ``balanced_chunks`` (which reads the document
+    offsets), concatenated in each rank's order.
     """
+    if layout == LAYOUT_BALANCED:
+        lists = balanced_chunks(L, R, chunks_per_rank, offsets)
+        c = L // (chunks_per_rank * R)
+        return np.concatenate([np.arange(j * c, (j + 1) * c, dtype=np.int64)
+                               for chunks in lists for j in chunks])
     if layout == LAYOUT_CONTIGUOUS:
         if L % R:
             raise ValueError("R must divide L")
@@ -390,7 +438,7 @@ def ring_partials(q_r, k_ranks, v_ranks, q_pos, k_pos_ranks, r, offsets=None,
 
 
 def ring_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True,
-                 scale=None, return_partials=False):
+                 scale=None, return_partials=False, chunks_per_rank=4):
     """Ring (P2P) CP forward over R ranks on global-order inputs.
 
     Returns per-rank O [R][n][Hq][d] and LSE [R][Hq][n] in slot order (and the
@@ -398,7 +446,7 @@ def ring_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True
     """
     L = q.shape[0]
     n = L // R
-    pos = ring_positions(L, R, layout)
+    pos = ring_positions(L, R, layout, offsets, chunks_per_rank)
     qs, ks, vs = shard(q, pos), shard(k, pos), shard(v, pos)
     k_ranks = [ks[r * n:(r + 1) * n] for r in range(R)]
     v_ranks = [vs[r * n:(r + 1) * n] for r in range(R)]
@@ -417,7 +465,7 @@ def ring_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True
 
 
 def usp_forward(q, k, v, U, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True,
-                scale=None):
+                scale=None, chunks_per_rank=4):
     """USP = Ulysses groups x ring ([MTX] "Split heads or rotate KV").
 
     Rank g = r*U + u (Ulysses innermost).  Member u of ring rank r holds the
@@ -432,7 +480,7 @@ def usp_forward(q, k, v, U, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=Tr
         raise ValueError("Ulysses degree must divide the KV-head count")
     T = L // R                      # ring shard length
     n = T // U                      # per-rank tokens
-    pos = ring_positions(L, R, layout)
+    pos = ring_positions(L, R, layout, offsets, chunks_per_rank)
     qs, ks, vs = shard(q, pos), shard(k, pos), shard(v, pos)
 
     def group(x, r):                # [U][n][H][d] of ring rank r
@@ -466,9 +514,9 @@ def visible_pairs(L: int, offsets=None, causal=True) -> int:
     return int((lens * (lens + 1) // 2).sum()) if causal else int((lens * lens).sum())
 
 
-def rank_visible_pairs(L, R, layout, offsets=None):
+def rank_visible_pairs(L, R, layout, offsets=None, chunks_per_rank=4):
     """Visible pairs whose query sits on each ring rank (the rank's work)."""
-    pos = ring_positions(L, R, layout)
+    pos = ring_positions(L, R, layout, offsets, chunks_per_rank)
     n = L // R
     ds = doc_start_of(np.arange(L), offsets)
     out = []

@@ -277,6 +277,58 @@ def pin_index_maps(orc):
     assert orc.visible_pairs(10, [0, 4, 10]) == 10 + 21
 
 
+def pin_balanced_layout_golden(orc):
+    """The work-balanced layout on hand-worked examples (tests/golden)."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "balanced_layout_examples.json")
+    for ex in json.load(open(path))["examples"]:
+        L, R, m, offs = ex["L"], ex["R"], ex["chunks_per_rank"], ex["offsets"]
+        assert orc.chunk_work(L, m * R, offs).tolist() == ex["chunk_work"]
+        assert orc.balanced_chunks(L, R, m, offs) == ex["rank_chunks"]
+        assert orc.rank_visible_pairs(L, R, 2, offs, m) == ex["rank_work"]
+        if "zigzag_rank_work" in ex:
+            assert orc.rank_visible_pairs(L, R, 1, offs) == ex["zigzag_rank_work"]
+
+
+def pin_balanced_layout_structure(orc):
+    """Balanced maps are permutations made of whole chunks, m per rank, in
+    position order within a rank; the ranks' work adds up to the total
+    visible pairs; with two chunks per rank and no documents the greedy rule
+    reproduces zigzag exactly (chunk work grows with the chunk index, so the
+    last R chunks go to ranks 0..R-1 in order and the first R come back in
+    reverse)."""
+    for L, R in [(64, 4), (48, 3), (4096, 8), (24, 1)]:
+        assert np.array_equal(orc.ring_positions(L, R, 2, None, 2), orc.ring_positions(L, R, 1))
+    for L, R, m, offs in [(96, 4, 3, [0, 7, 50, 51, 96]), (120, 5, 2, [0, 60, 120]), (64, 2, 8, None)]:
+        p = orc.ring_positions(L, R, 2, offs, m)
+        assert sorted(p.tolist()) == list(range(L))
+        c = L // (m * R)
+        chunks = orc.balanced_chunks(L, R, m, offs)
+        assert all(len(x) == m for x in chunks)
+        for r in range(R):
+            starts = p[r * m * c:(r + 1) * m * c:c]
+            assert list(starts) == [j * c for j in chunks[r]]
+            assert list(starts) == sorted(starts)
+            assert np.array_equal(p[r * m * c:(r + 1) * m * c].reshape(m, c) - starts[:, None],
+                                  np.tile(np.arange(c), (m, 1)))
+        assert sum(orc.rank_visible_pairs(L, R, 2, offs, m)) == orc.visible_pairs(L, offs)
+
+
+def pin_ring_balanced_equals_full(orc):
+    """Ring and USP CP on the balanced layout equal full attention."""
+    L, Hq, Hkv, d = 48, 4, 2, 4
+    q, k, v = _rand((L, Hq, d), 40), _rand((L, Hkv, d), 41), _rand((L, Hkv, d), 42)
+    for offs in (None, [0, 5, 29, 48]):
+        O, LSE = orc.attention(q, k, v, offsets=offs)
+        for R, m in [(2, 3), (3, 4), (4, 2)]:
+            o, lse = orc.ring_forward(q, k, v, R, 2, offsets=offs, chunks_per_rank=m)
+            pos = orc.ring_positions(L, R, 2, offs, m)
+            np.testing.assert_allclose(o.reshape(L, Hq, d), O[pos], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(np.concatenate(list(lse), axis=1), LSE[:, pos], rtol=1e-12, atol=1e-12)
+        o, lse = orc.usp_forward(q, k, v, 2, 2, 2, offsets=offs, chunks_per_rank=3)
+        pos = orc.ring_positions(L, 2, 2, offs, 3)
+        np.testing.assert_allclose(o.reshape(L, Hq, d), O[pos], rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- backward
 
 

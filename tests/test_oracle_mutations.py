@@ -28,6 +28,9 @@ MUTATIONS = {
     "bwd_rows_dv_operand": ("dv[:, ji, :] += P[:, key_rows].T @ dOr", "dv[:, ji, :] += P[:, key_rows].T @ Qr"),
     "bwd_gqa_overwrite": ("dk[:, j, :] += sc * (dS.T @ q[:, h, :])", "dk[:, j, :] = sc * (dS.T @ q[:, h, :])"),
     "bwd_dropped_scale": ("dq[:, h, :] = sc * (dS @ k[:, j, :])", "dq[:, h, :] = (dS @ k[:, j, :])"),
+    "balanced_ascending": ("key=lambda j: (-int(work[j]), j)", "key=lambda j: (int(work[j]), j)"),
+    "balanced_most_loaded": ("load[r] < load[best]", "load[r] > load[best]"),
+    "balanced_ignores_docs": ("per_query = pos - doc_start_of(pos, offsets) + 1", "per_query = pos + 1"),
     "lse_reshard_back": ("out[s, u * Hl:(u + 1) * Hl, :] = lse[u, :, s * n:(s + 1) * n]", "out[s, u * Hl:(u + 1) * Hl, :] = lse[s, :, u * n:(u + 1) * n]"),
 }
 
