@@ -57,6 +57,15 @@ def row_visible(pos: np.ndarray, offsets) -> np.ndarray:
     return pos - start + 1
 
 
+def rank_work_spread(index_map, R: int, offsets) -> float:
+    """max / mean over ring ranks of the visible (query, key) pairs whose
+    query the rank holds: a query at position i sees i - doc_start(i) + 1 keys."""
+    pos = np.asarray(index_map, dtype=np.int64)
+    row_keys = row_visible(pos, offsets)
+    work = row_keys.reshape(R, -1).sum(axis=1).astype(np.float64)
+    return round(float(work.max() / work.mean()), 4)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if not os.path.exists(path):
@@ -203,6 +212,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", choices=["workload", "contiguous", "zigzag", "balanced"], default="workload",
+                    help="token layout of the ring shards (default: the workload's own)")
+    ap.add_argument("--chunks-per-rank", type=int, default=8, help="chunks per ring rank of the balanced layout")
     ap.add_argument("--backward", action="store_true",
                     help="add the backward to every step (the ring fwd+bwd workload always has it)")
     ap.add_argument("--L", type=int, default=0,
@@ -217,6 +229,8 @@ def main():
         w = dataclasses.replace(w, L=args.L)
     if args.backward:
         w = dataclasses.replace(w, backward=True)
+    if args.layout != "workload":
+        w = dataclasses.replace(w, layout={"contiguous": 0, "zigzag": 1, "balanced": 2}[args.layout])
     offsets = workloads.workload_doc_offsets(w)
     flops_fwd = useful_flops(w, offsets)
     flops_step = int(flops_fwd * (1 + BWD_FLOP_RATIO)) if w.backward else flops_fwd
@@ -237,7 +251,7 @@ def main():
     dev = torch.device("cuda", local_rank)
 
     plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
-                    doc_offsets=offsets, emit_partials=w.emit_partials)
+                    doc_offsets=offsets, emit_partials=w.emit_partials, chunks_per_rank=args.chunks_per_rank)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
     # each rank draws its own sequence.
     g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale,
@@ -417,7 +431,9 @@ def main():
             "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": U, "ring": R,
-                       "layout": "zigzag" if w.layout else "contiguous", "docs": bool(offsets is not None),
+                       "layout": ["contiguous", "zigzag", f"balanced (m={args.chunks_per_rank})"][w.layout],
+                       "rank_work_spread": rank_work_spread(plan.index_map(), w.ring, offsets),
+                       "docs": bool(offsets is not None),
                        "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
                        "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",
                        "step": "forward + backward" if w.backward else "forward",

@@ -30,6 +30,7 @@ CP_ERR_ARCH = -8
 CP_NOALLOC_SCRATCH_BYTES = 8 << 20
 CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1
+CP_LAYOUT_BALANCED = 2
 CP_SEQ_TO_HEAD = 0
 CP_HEAD_TO_SEQ = 1
 CP_TOKEN_MAJOR = 0
@@ -54,6 +55,7 @@ class cp_plan_desc_t(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("emit_partials", ctypes.c_int32),
         ("out_fp32", ctypes.c_int32),
+        ("chunks_per_rank", ctypes.c_int32),
     ]
 
 
@@ -130,7 +132,8 @@ class Plan:
     """Owns a cp_plan_t (cp_plan_create / cp_plan_destroy)."""
 
     def __init__(self, L, Hq, Hkv, d, ulysses_degree=1, ring_degree=1, layout=CP_LAYOUT_CONTIGUOUS,
-                 doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True, out_fp32=False):
+                 doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True, out_fp32=False,
+                 chunks_per_rank=8):
         self._h = None
         desc = cp_plan_desc_t()
         desc.version = CP_ATTN_PLAN_VERSION
@@ -149,6 +152,7 @@ class Plan:
         desc.softmax_scale = float(softmax_scale)
         desc.emit_partials = 1 if emit_partials else 0
         desc.out_fp32 = 1 if out_fp32 else 0
+        desc.chunks_per_rank = int(chunks_per_rank)
         h = _vp()
         _check(_L().cp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "cp_plan_create")
         self._h = h
@@ -157,6 +161,7 @@ class Plan:
         self.P = self.U * self.R
         self.n = self.L // self.P
         self.layout = desc.layout
+        self.chunks_per_rank = desc.chunks_per_rank
         self.emit_partials = bool(emit_partials)
         self.out_fp32 = bool(out_fp32)
 

@@ -134,7 +134,7 @@ struct DqSmem {
 
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int lo_min, int qpos_last, F&& f) {
-  const int nchunks = (g.layout == CP_LAYOUT_CONTIGUOUS) ? 1 : 2;
+  const int nchunks = g.nchunks;
   for (int s = 0; s < g.R; ++s) {
     const int src = (r - s + g.R) % g.R;
     for (int ch = 0; ch < nchunks; ++ch) {
@@ -371,7 +371,7 @@ struct DkvSmem {
 // every query head of KV head jh that may see the key tile [kpos0, hi_max].
 template <typename F>
 __device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int kpos0, int hi_max, int jh, F&& f) {
-  const int nchunks = (g.layout == CP_LAYOUT_CONTIGUOUS) ? 1 : 2;
+  const int nchunks = g.nchunks;
   for (int s = 0; s < g.R; ++s) {
     const int rr = (src + s) % g.R;
     for (int ch = 0; ch < nchunks; ++ch) {

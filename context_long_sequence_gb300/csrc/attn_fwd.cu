@@ -95,7 +95,7 @@ struct FwdSmem {
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end,
                                                  int lo_min, int qpos_last, F&& f) {
-  const int nchunks = (g.layout == CP_LAYOUT_CONTIGUOUS) ? 1 : 2;
+  const int nchunks = g.nchunks;
   for (int s = s_begin; s < s_end; ++s) {
     const int src = (r - s + g.R) % g.R;
     const int a_src = src * g.U + u;

@@ -27,6 +27,8 @@ struct cp_plan {
   float scale;
   bool on_device;
   int device;
+  std::vector<int32_t> chunk_pos;  // balanced layout: [R][nchunks] first position of each chunk
+  int32_t* d_chunk_pos;          // device copy, or null
   int32_t* d_doc_start;          // [L] or null
   int32_t* d_doc_end;            // [L] or null
   WorkItem* d_items_fused;       // forward: 256-row query blocks, all ring steps
@@ -65,7 +67,9 @@ int doc_start_host(const cp_plan* p, int pos) {
   return *(it - 1);
 }
 
-AttnGeom geom(const cp_plan* p) {
+// Geometry for the kernels (device tables) or for host-side walks of the
+// same index arithmetic (host copy of the chunk table).
+AttnGeom geom(const cp_plan* p, bool on_host = false) {
   AttnGeom g;
   const cp_plan_desc_t& d = p->desc;
   g.L = d.L;
@@ -77,6 +81,8 @@ AttnGeom geom(const cp_plan* p) {
   g.G = d.Hq / d.Hkv;
   g.layout = d.layout;
   g.chunk = p->chunk;
+  g.nchunks = p->nchunks;
+  g.chunk_pos = p->chunk_pos.empty() ? nullptr : (on_host ? p->chunk_pos.data() : p->d_chunk_pos);
   g.scale = p->scale;
   g.doc_start = p->d_doc_start;
   g.doc_end = p->d_doc_end;
@@ -106,7 +112,7 @@ int visited_tiles(const cp_plan* p, const AttnGeom& g, int r, int q0, int len, i
 // Query blocks of `rows` slots, ordered by descending work (longest first
 // onto the SMs).
 std::vector<WorkItem> build_items(const cp_plan* p, bool per_step, int rows) {
-  const AttnGeom g = geom(p);
+  const AttnGeom g = geom(p, true);
   struct Keyed {
     int work;
     WorkItem it;
@@ -131,6 +137,42 @@ std::vector<WorkItem> build_items(const cp_plan* p, bool per_step, int rows) {
   std::vector<WorkItem> out(v.size());
   for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].it;
   return out;
+}
+
+// Work-balanced layout ([L3P] "Long context changes more than attention
+// cost": split by actual attention work; [MTX] "Split heads or rotate KV":
+// causal load balancing).  m*R equal chunks; a query at position i costs
+// i - doc_start(i) + 1 visible keys.  Chunks go, from most to least work
+// (equal work: lower chunk first), to the least-loaded rank that still holds
+// fewer than m chunks (equal load: lower rank first); each rank keeps its
+// chunks in position order.  Fills p->chunk_pos[r * m + k].
+void balanced_chunk_table(cp_plan* p) {
+  const int R = p->desc.ring_degree, m = p->nchunks, C = R * m, c = p->chunk;
+  std::vector<long long> work(C, 0);
+  for (int j = 0; j < C; ++j) {
+    int ds = doc_start_host(p, j * c);
+    for (int i = j * c; i < (j + 1) * c; ++i) {
+      if (!p->offsets.empty() && std::binary_search(p->offsets.begin(), p->offsets.end(), i)) ds = i;
+      work[j] += i - ds + 1;
+    }
+  }
+  std::vector<int> order(C);
+  for (int j = 0; j < C; ++j) order[j] = j;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work[x] > work[y]; });
+  std::vector<long long> load(R, 0);
+  std::vector<std::vector<int>> held(R);
+  for (int j : order) {
+    int best = -1;
+    for (int r = 0; r < R; ++r)
+      if (static_cast<int>(held[r].size()) < m && (best < 0 || load[r] < load[best])) best = r;
+    held[best].push_back(j);
+    load[best] += work[j];
+  }
+  p->chunk_pos.assign(static_cast<size_t>(C), 0);
+  for (int r = 0; r < R; ++r) {
+    std::sort(held[r].begin(), held[r].end());
+    for (int k = 0; k < m; ++k) p->chunk_pos[static_cast<size_t>(r) * m + k] = held[r][k] * c;
+  }
 }
 
 int doc_end_host(const cp_plan* p, int pos) {
@@ -159,7 +201,7 @@ int visited_q_tiles(const cp_plan* p, const AttnGeom& g, int src, int k0, int le
 
 // Key tiles of every attention rank a = src * U + u, ordered by descending work.
 std::vector<WorkItem> build_kv_items(const cp_plan* p) {
-  const AttnGeom g = geom(p);
+  const AttnGeom g = geom(p, true);
   std::vector<std::pair<int, WorkItem>> v;
   for (int a = 0; a < g.R * g.U; ++a)
     for (int ch = 0; ch < p->nchunks; ++ch)
@@ -264,7 +306,9 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   if (d.version != CP_ATTN_PLAN_VERSION) return CP_ERR_INVALID_ARG;
   if (d.L <= 0 || d.Hq <= 0 || d.Hkv <= 0 || d.ulysses_degree <= 0 || d.ring_degree <= 0) return CP_ERR_INVALID_ARG;
   if (d.Hq % d.Hkv) return CP_ERR_INVALID_ARG;
-  if (d.layout != CP_LAYOUT_CONTIGUOUS && d.layout != CP_LAYOUT_ZIGZAG) return CP_ERR_INVALID_ARG;
+  if (d.layout != CP_LAYOUT_CONTIGUOUS && d.layout != CP_LAYOUT_ZIGZAG && d.layout != CP_LAYOUT_BALANCED)
+    return CP_ERR_INVALID_ARG;
+  if (d.layout == CP_LAYOUT_BALANCED && d.chunks_per_rank < 1) return CP_ERR_INVALID_ARG;
   if (d.num_docs < 0) return CP_ERR_INVALID_ARG;
   if (d.out_fp32 != 0 && d.out_fp32 != 1) return CP_ERR_INVALID_ARG;
   if (d.emit_partials != 0 && d.emit_partials != 1) return CP_ERR_INVALID_ARG;
@@ -273,7 +317,9 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   if (d.causal != 1) return CP_ERR_UNSUPPORTED;
   if (d.Hkv % d.ulysses_degree) return CP_ERR_UNSUPPORTED;  // KV heads cap the A2A degree
   const int R = d.ring_degree, U = d.ulysses_degree;
-  if (d.layout == CP_LAYOUT_CONTIGUOUS ? (d.L % R) : (d.L % (2 * R))) return CP_ERR_INVALID_ARG;
+  const int nchunks = d.layout == CP_LAYOUT_CONTIGUOUS ? 1 : d.layout == CP_LAYOUT_ZIGZAG ? 2 : d.chunks_per_rank;
+  if (static_cast<long long>(nchunks) * R > d.L || d.L % (static_cast<long long>(nchunks) * R))
+    return CP_ERR_INVALID_ARG;
   const int T = d.L / R;
   if (T % U) return CP_ERR_INVALID_ARG;
   if (d.emit_partials && U != 1) return CP_ERR_UNSUPPORTED;
@@ -300,8 +346,10 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->P = R * U;
   p->T = T;
   p->n = T / U;
-  p->nchunks = d.layout == CP_LAYOUT_CONTIGUOUS ? 1 : 2;
+  p->nchunks = nchunks;
   p->chunk = T / p->nchunks;
+  if (d.layout == CP_LAYOUT_BALANCED) balanced_chunk_table(p);
+  p->d_chunk_pos = nullptr;
   p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
@@ -334,6 +382,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       rc = upload(ds, &p->d_doc_start);
       if (rc == CP_OK) rc = upload(de, &p->d_doc_end);
     }
+    if (rc == CP_OK) rc = upload(p->chunk_pos, &p->d_chunk_pos);
     std::vector<WorkItem> fused = build_items(p, false, 2 * kTile);
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
@@ -353,6 +402,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       rc = upload(kv, &p->d_items_kv);
     }
     if (rc != CP_OK) {
+      cudaFree(p->d_chunk_pos);
       cudaFree(p->d_doc_start);
       cudaFree(p->d_doc_end);
       cudaFree(p->d_items_fused);
@@ -371,6 +421,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
 void cp_plan_destroy(cp_plan_t* p) {
   if (!p) return;
   if (p->on_device) {
+    cudaFree(p->d_chunk_pos);
     cudaFree(p->d_doc_start);
     cudaFree(p->d_doc_end);
     cudaFree(p->d_items_fused);
@@ -383,7 +434,7 @@ void cp_plan_destroy(cp_plan_t* p) {
 
 int cp_index_map(const cp_plan_t* p, int32_t* host_out) {
   if (!p || !host_out) return CP_ERR_INVALID_ARG;
-  const AttnGeom g = geom(p);
+  const AttnGeom g = geom(p, true);
   // Sequence-sharded slot order: rank g = r*U + u holds ring-local slots
   // [u*n, (u+1)*n) of ring rank r, so the slot order is ring rank major.
   for (int r = 0; r < g.R; ++r)

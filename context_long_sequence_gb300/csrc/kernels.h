@@ -21,7 +21,10 @@ struct AttnGeom {
   int L, R, U, T;          // T = L / R slots per attention rank
   int Hq_loc, Hkv_loc, G;  // G = Hq_loc / Hkv_loc
   int layout;              // CP_LAYOUT_*
-  int chunk;               // contiguous-position chunk length: T or T/2
+  int chunk;               // contiguous-position chunk length: T / nchunks
+  int nchunks;             // chunks per ring rank: 1 (contiguous), 2 (zigzag), m (balanced)
+  const int32_t* chunk_pos;  // balanced: [R][nchunks] first position of each chunk (host or
+                             // device copy, matching where slot_pos runs); else null
   float scale;             // softmax scale
   const int32_t* doc_start;  // [L] start of the document holding each position, or null
   const int32_t* doc_end;    // [L] one past the end of that document, or null
@@ -31,7 +34,9 @@ struct AttnGeom {
 __host__ __device__ inline int slot_pos(const AttnGeom& g, int r, int t) {
   if (g.layout == 0) return r * g.T + t;
   const int c = g.chunk;
-  return t < c ? r * c + t : (2 * g.R - 1 - r) * c + (t - c);
+  if (g.layout == 1) return t < c ? r * c + t : (2 * g.R - 1 - r) * c + (t - c);
+  const int j = t / c;
+  return g.chunk_pos[r * g.nchunks + j] + (t - j * c);
 }
 
 struct FwdArgs {

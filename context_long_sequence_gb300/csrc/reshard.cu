@@ -8,14 +8,16 @@
 // Both layouts are sequences of contiguous blocks:
 //   token-major: a block is one token's H/U heads (H/U * E elements),
 //   head-major (LSE): a block is one head's n tokens.
-// The kernel walks the OUTPUT in order.  One warp copies one block at a time
-// (lanes take consecutive 16-byte vectors, or 4-byte words when a block is
-// not a multiple of 16 bytes), so reads and writes are both contiguous and
-// fully coalesced; the block's source offset is computed once per block, not
-// per vector.  Each warp keeps four blocks in flight.  HBM-bound; the grid
-// is a multiple of the SM count.
+// The kernel walks the OUTPUT in order.  Blocks longer than 4 KB are cut into
+// 4 KB segments (LSE blocks are a whole rank's tokens of one head), and one
+// warp copies one segment at a time (lanes take consecutive 16-byte vectors,
+// or 4-byte words when a block is not a multiple of 16 bytes), so reads and
+// writes are both contiguous and fully coalesced; the source offset is
+// computed once per segment, not per vector.  Each warp keeps four segments
+// in flight.  HBM-bound; the grid is a multiple of the SM count.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "cp_attn.h"
@@ -28,6 +30,8 @@ struct ReshardGeom {
   uint32_t U, n, H, Hl;  // Hl = H / U
   uint32_t blk;          // block size in vectors
   uint32_t nblocks;      // output blocks
+  uint32_t seg, nseg;    // segment size in vectors, segments per block
+  uint32_t nunits;       // nblocks * nseg
   int dir, kind;
 };
 
@@ -80,21 +84,30 @@ __global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, 
   const int lane = threadIdx.x & 31;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   const uint32_t w0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  for (uint32_t base = w0 * kBlocksInFlight; base < g.nblocks; base += warps * kBlocksInFlight) {
-    uint64_t src[kBlocksInFlight];
+  for (uint32_t base = w0 * kBlocksInFlight; base < g.nunits; base += warps * kBlocksInFlight) {
+    uint64_t src[kBlocksInFlight], dst[kBlocksInFlight];
+    uint32_t len[kBlocksInFlight];
 #pragma unroll
     for (int i = 0; i < kBlocksInFlight; ++i) {
-      const uint32_t ob = base + i;
-      src[i] = ob < g.nblocks ? static_cast<uint64_t>(in_block(g, ob)) * g.blk : 0;
+      const uint32_t un = base + i;
+      len[i] = 0;
+      src[i] = dst[i] = 0;
+      if (un < g.nunits) {
+        const uint32_t ob = un / g.nseg;
+        const uint32_t v0 = (un - ob * g.nseg) * g.seg;
+        len[i] = min(g.seg, g.blk - v0);
+        src[i] = static_cast<uint64_t>(in_block(g, ob)) * g.blk + v0;
+        dst[i] = static_cast<uint64_t>(ob) * g.blk + v0;
+      }
     }
-    for (uint32_t v0 = lane; v0 < g.blk; v0 += 32) {
+    for (uint32_t v = lane; v < g.seg; v += 32) {
       V val[kBlocksInFlight];
 #pragma unroll
       for (int i = 0; i < kBlocksInFlight; ++i)
-        if (base + i < g.nblocks) val[i] = __ldg(in + src[i] + v0);
+        if (v < len[i]) val[i] = __ldg(in + src[i] + v);
 #pragma unroll
       for (int i = 0; i < kBlocksInFlight; ++i)
-        if (base + i < g.nblocks) out[static_cast<uint64_t>(base + i) * g.blk + v0] = val[i];
+        if (v < len[i]) out[dst[i] + v] = val[i];
     }
   }
 }
@@ -128,21 +141,26 @@ int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int
   if (nblocks >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
   g.nblocks = static_cast<uint32_t>(nblocks);
   const int threads = 256, warps_per_cta = threads / 32;
-  const long long need = (nblocks + warps_per_cta * kBlocksInFlight - 1) / (warps_per_cta * kBlocksInFlight);
+  const long long vec_bytes = (block_bytes % 16 == 0) ? 16 : 4;
+  const long long blk = block_bytes / vec_bytes;
+  if (block_bytes % 4 != 0) return CP_ERR_UNSUPPORTED;
+  if (blk >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  const long long seg = std::min<long long>(blk, 4096 / vec_bytes);
+  const long long nseg = (blk + seg - 1) / seg;
+  const long long nunits = nblocks * nseg;
+  if (nunits >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  g.blk = static_cast<uint32_t>(blk);
+  g.seg = static_cast<uint32_t>(seg);
+  g.nseg = static_cast<uint32_t>(nseg);
+  g.nunits = static_cast<uint32_t>(nunits);
+  const long long need = (nunits + warps_per_cta * kBlocksInFlight - 1) / (warps_per_cta * kBlocksInFlight);
   const long long cap = static_cast<long long>(sm_count()) * 8;
   const int grid = static_cast<int>(need < cap ? need : cap);
-  if (block_bytes % 16 == 0) {
-    if (block_bytes / 16 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
-    g.blk = static_cast<uint32_t>(block_bytes / 16);
+  if (vec_bytes == 16)
     reshard_kernel<uint4><<<grid, threads, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
-  } else if (block_bytes % 4 == 0) {
-    if (block_bytes / 4 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
-    g.blk = static_cast<uint32_t>(block_bytes / 4);
+  else
     reshard_kernel<uint32_t><<<grid, threads, 0, stream>>>(static_cast<const uint32_t*>(in),
                                                            static_cast<uint32_t*>(out), g);
-  } else {
-    return CP_ERR_UNSUPPORTED;
-  }
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 

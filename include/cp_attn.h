@@ -74,6 +74,13 @@ extern "C" {
  * [L3P] "Long context changes more than attention cost"). */
 #define CP_LAYOUT_CONTIGUOUS 0    /* ring rank r holds positions [r*L/R, (r+1)*L/R) */
 #define CP_LAYOUT_ZIGZAG     1    /* 2R chunks of c = L/(2R); rank r holds chunk r then chunk 2R-1-r */
+#define CP_LAYOUT_BALANCED   2    /* m*R chunks of c = L/(m*R), m = chunks_per_rank, dealt out by
+                                     attention work: a query at position i does i - doc_start(i) + 1
+                                     units; chunks are taken from most to least work (equal work:
+                                     lower chunk first) and each goes to the least-loaded rank that
+                                     holds fewer than m chunks (equal load: lower rank first); a
+                                     rank keeps its chunks in position order.  With m = 2 and one
+                                     document this is exactly the zigzag layout. */
 
 /* Reshard directions and tensor kinds for ulysses_reshard(). */
 #define CP_SEQ_TO_HEAD 0
@@ -93,7 +100,8 @@ typedef struct {
   int32_t d;                  /* head dimension: 64 or 128 */
   int32_t ulysses_degree;     /* U >= 1; U divides Hkv ([MTX] "Split heads or rotate KV": KV heads cap A2A) */
   int32_t ring_degree;        /* R >= 1; P = U*R emulated ranks */
-  int32_t layout;             /* CP_LAYOUT_*; R divides L (contiguous) or 2R divides L (zigzag); U divides L/R */
+  int32_t layout;             /* CP_LAYOUT_*; R divides L (contiguous), 2R divides L (zigzag) or
+                                 m*R divides L (balanced); U divides L/R */
   int32_t causal;             /* must be 1 (causal attention; [MTX] "Why KV comes back together") */
   int32_t num_docs;           /* 0 or 1: one document; >1: packed documents */
   const int32_t *doc_offsets; /* host; num_docs+1 entries, [0]=0, strictly increasing, [num_docs]=L; copied */
@@ -106,6 +114,7 @@ typedef struct {
                                  normalised accumulator, unrounded).  Applies to the o output of
                                  cp_attn_fwd, cp_attn_fwd_local and cp_attn_fwd_noalloc and to the
                                  o input of cp_attn_bwd; cp_merge_lse always writes bf16. */
+  int32_t chunks_per_rank;    /* CP_LAYOUT_BALANCED: m >= 1 chunks per ring rank; ignored otherwise */
 } cp_plan_desc_t;
 
 typedef struct cp_plan cp_plan_t;   /* opaque; immutable after creation; usable from any stream */

@@ -48,6 +48,21 @@ def test_index_map_matches_oracle(cpa, L, R, U, layout):
     assert np.array_equal(p.index_map(), oracle.ring_positions(L, R, layout))
 
 
+@pytest.mark.parametrize("L,R,U,m,docs", [
+    (24, 2, 1, 3, [0, 10, 24]), (16, 2, 1, 2, [0, 3, 16]), (12, 3, 1, 1, None), (65536, 8, 1, 2, None),
+    (4096, 4, 2, 4, [0, 100, 2000, 4096]), (1000, 5, 1, 4, [0, 1, 2, 999, 1000]), (131072, 16, 1, 8, "packed")])
+def test_balanced_index_map_matches_oracle(cpa, L, R, U, m, docs):
+    """The plan's work-balanced chunk assignment (C++) equals the oracle's,
+    bit for bit, including the packed-document workload's seeded documents."""
+    import oracle
+    import workloads
+    if docs == "packed":
+        docs = workloads.workload_doc_offsets(workloads.WORKLOADS[3])
+    p = cpa.Plan(L, 8, 4, 64, ulysses_degree=U, ring_degree=R, layout=cpa.CP_LAYOUT_BALANCED, doc_offsets=docs,
+                 chunks_per_rank=m)
+    assert np.array_equal(p.index_map(), oracle.ring_positions(L, R, oracle.LAYOUT_BALANCED, docs, m))
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(L=100, Hq=8, Hkv=4, d=64, ring_degree=3), -1),                 # R does not divide L
     (dict(L=96, Hq=8, Hkv=3, d=64), -1),                                 # Hkv does not divide Hq
@@ -59,6 +74,9 @@ def test_index_map_matches_oracle(cpa, L, R, U, layout):
     (dict(L=96, Hq=8, Hkv=4, d=64, doc_offsets=[0, 50, 95]), -1),        # does not end at L
     (dict(L=90, Hq=8, Hkv=4, d=64, ring_degree=4, layout=1), -1),        # 2R does not divide L
     (dict(L=96, Hq=8, Hkv=4, d=64, ulysses_degree=4, ring_degree=5), -1),
+    (dict(L=96, Hq=8, Hkv=4, d=64, ring_degree=2, layout=2, chunks_per_rank=0), -1),   # balanced needs m >= 1
+    (dict(L=96, Hq=8, Hkv=4, d=64, ring_degree=2, layout=2, chunks_per_rank=5), -1),   # m*R does not divide L
+    (dict(L=96, Hq=8, Hkv=4, d=64, layout=3), -1),                                    # unknown layout
 ])
 def test_plan_validation(cpa, kw, code):
     with pytest.raises(cpa.CPError) as e:

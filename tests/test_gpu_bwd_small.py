@@ -52,6 +52,21 @@ def test_bwd_matches_oracle(cpa, case):
     gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], name)
 
 
+@pytest.mark.parametrize("U,R,m,docs", [(1, 2, 3, [0, 200, 1100, 1536]), (2, 2, 4, [0, 900, 1536]),
+                                        (1, 3, 4, None)])
+def test_bwd_balanced_layout(cpa, U, R, m, docs):
+    """Backward on the work-balanced chunk layout."""
+    import gpu_harness as gh
+    L, Hq, Hkv, d = 1536, 8, 2, 128
+    inp = workloads.make_inputs(L, Hq, Hkv, d, 40 + U + R + m, with_do=True)
+    plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=cpa.CP_LAYOUT_BALANCED,
+                    doc_offsets=docs, chunks_per_rank=m)
+    got = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
+    _, _, dq, dk, dv = oracle.attention_bwd(inp["q"].double().numpy(), inp["k"].double().numpy(),
+                                            inp["v"].double().numpy(), inp["do"].double().numpy(), offsets=docs)
+    gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], f"balanced U{U} R{R} m{m}")
+
+
 def test_bwd_deterministic(cpa):
     import gpu_harness as gh
     inp = workloads.make_inputs(1024, 4, 2, 128, 5, with_do=True)

@@ -60,6 +60,31 @@ def test_fwd_matches_oracle(cpa, case, out_fp32):
     gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name, bf16_out=not out_fp32)
 
 
+BALANCED_CASES = [
+    # name, L, Hq, Hkv, d, U, R, chunks_per_rank, docs, emit_partials
+    ("balanced_docs_m3", 1536, 8, 2, 128, 1, 2, 3, [0, 200, 1100, 1536], False),
+    ("balanced_usp_m4_d64", 2048, 8, 4, 64, 2, 2, 4, [0, 1500, 2048], False),
+    ("balanced_partials_chunk100", 1200, 4, 4, 128, 1, 3, 4, [0, 50, 1200], True),
+    ("balanced_one_chunk_R4", 1024, 4, 2, 128, 1, 4, 1, None, False),
+    ("balanced_m8_ragged_docs", 2560, 4, 1, 128, 1, 2, 8, [0, 1, 700, 701, 2559, 2560], False),
+]
+
+
+@pytest.mark.parametrize("case", BALANCED_CASES, ids=[c[0] for c in BALANCED_CASES])
+def test_fwd_balanced_layout_matches_oracle(cpa, case):
+    """Work-balanced chunk layout: chunks of any length (down to below one
+    tile), several per rank in position order, with Ulysses, partials and
+    documents."""
+    import gpu_harness as gh
+    name, L, Hq, Hkv, d, U, R, m, docs, partials = case
+    inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(name.encode()) % 1000)
+    plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=cpa.CP_LAYOUT_BALANCED,
+                    doc_offsets=docs, emit_partials=partials, out_fp32=True, chunks_per_rank=m)
+    O, LSE = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
+    O_ref, LSE_ref = oracle.attention(inp["q"], inp["k"], inp["v"], offsets=docs)
+    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name)
+
+
 def test_fwd_deterministic(cpa):
     import gpu_harness as gh
     inp = _inputs(1536, 8, 2, 128, seed=7)

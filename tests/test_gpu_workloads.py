@@ -87,6 +87,38 @@ def test_workload_forward_sampled(cpa, wi, out_fp32):
     gh.assert_close(O, LSE, O_ref, LSE_ref, w.name, bf16_out=not out_fp32)
 
 
+def test_packed_documents_balanced_layout_sampled(cpa):
+    """The packed-document workload (L = 131072, R = 16, seeded documents)
+    on the work-balanced layout with 8 chunks per rank: sampled rows against
+    the oracle."""
+    import gpu_harness as gh
+    w = workloads.WORKLOADS[3]
+    offsets = workloads.workload_doc_offsets(w)
+    plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ring_degree=w.ring, layout=cpa.CP_LAYOUT_BALANCED, doc_offsets=offsets,
+                    chunks_per_rank=8, out_fp32=True)
+    g = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device="cuda", k_scale=w.k_scale)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64)).to("cuda")
+    q, k, v = (g[n][idx].contiguous() for n in ("q", "k", "v"))
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device="cuda")
+    cpa.cp_attn_fwd(plan, q, k, v, o, lse, cpa.alloc_workspace(plan))
+    assert cpa.cp_get_status() == 0
+    slot_of = torch.empty_like(idx)
+    slot_of[idx] = torch.arange(w.L, device="cuda")
+    c = w.L // (8 * w.ring)
+    rows = workloads.sample_rows(w.L, list(range(0, w.L, c)) + [int(x) for x in offsets], 48, seed=w.seed + 2)
+    heads = _heads(w.Hq, 1)
+    rows_t = torch.from_numpy(rows).to("cuda")
+    slots = slot_of[rows_t]
+    O = o[slots][:, heads].cpu().numpy()
+    LSE = lse.permute(1, 0, 2).reshape(w.Hq, w.L)[heads][:, slots].cpu().numpy()
+    cpu = {n: g[n].cpu() for n in ("q", "k", "v")}
+    del q, k, v, o, lse, g
+    torch.cuda.empty_cache()
+    O_ref, LSE_ref = oracle.attention_rows(cpu["q"], cpu["k"], cpu["v"], rows=rows, offsets=offsets, heads=heads)
+    gh.assert_close(O, LSE, O_ref, LSE_ref, "packed docs, balanced layout")
+
+
 @pytest.mark.parametrize("wi", [1, 2], ids=[workloads.WORKLOADS[i].name for i in (1, 2)])
 def test_workload_backward_sampled(cpa, wi):
     """The ring backward at the ring workload's size, and the Ulysses
