@@ -371,6 +371,13 @@ def main():
     reps = max(3, min(args.steps, 10))
     attn_ms = timed(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
     kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9}
+    if U == 1 and not w.emit_partials:
+        # Each ring rank's share alone (cp_attn_fwd_rank): the forward time of
+        # one GPU per rank, communication aside, is the slowest rank's.
+        per_rank = [timed(lambda r=r: cpa.cp_attn_fwd_rank(plan, r, q, k, v, o, lse, stream=stream), reps)
+                    for r in range(R)]
+        kern["attn_fwd_per_rank"] = {"ms": [round(t, 4) for t in per_rank], "max_ms": max(per_rank),
+                                     "max_over_mean": max(per_rank) / statistics.mean(per_rank)}
     if w.backward:
         bwd_ms = timed(bwd, reps)
         kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,

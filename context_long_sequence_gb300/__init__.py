@@ -81,6 +81,7 @@ def _L():
     lib.ulysses_reshard.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
     lib.cp_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.cp_attn_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_fwd_rank.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
@@ -92,7 +93,8 @@ def _L():
 
 
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
-            "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_noalloc", "cp_attn_bwd", "cp_merge_lse", "cp_get_status", "cp_strerror"]
+            "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
+            "cp_merge_lse", "cp_get_status", "cp_strerror"]
 
 
 class CPError(RuntimeError):
@@ -206,6 +208,11 @@ def cp_attn_fwd(plan: Plan, q, k, v, o, lse, workspace=None, workspace_bytes=Non
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L().cp_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
                             int(workspace_bytes), _stream(stream)), "cp_attn_fwd")
+
+
+def cp_attn_fwd_rank(plan: Plan, rank, q, k, v, o, lse, stream=None):
+    _check(_L().cp_attn_fwd_rank(plan.handle, int(rank), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                 _stream(stream)), "cp_attn_fwd_rank")
 
 
 def cp_attn_fwd_local(plan: Plan, q, k, v, o, lse, stream=None):

@@ -39,6 +39,8 @@ struct cp_plan {
   int n_items_steps;
   WorkItem* d_items_kv;          // backward: key tiles
   int n_items_kv;
+  WorkItem* d_items_rank;        // the fused list grouped by attention rank (cp_attn_fwd_rank)
+  std::vector<int> rank_item_off;  // [P + 1] offsets into d_items_rank
 };
 
 namespace {
@@ -353,7 +355,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
-  p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = nullptr;
+  p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = p->d_items_rank = nullptr;
   p->n_items_fused = p->n_items_q = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
@@ -387,6 +389,15 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
     if (rc == CP_OK) {
+      // The same items grouped by rank, each group keeping the longest-first order.
+      std::vector<WorkItem> by_rank(fused);
+      std::stable_sort(by_rank.begin(), by_rank.end(), [](const WorkItem& x, const WorkItem& y) { return x.a < y.a; });
+      p->rank_item_off.assign(p->P + 1, 0);
+      for (const WorkItem& it : by_rank) ++p->rank_item_off[it.a + 1];
+      for (int a = 0; a < p->P; ++a) p->rank_item_off[a + 1] += p->rank_item_off[a];
+      rc = upload(by_rank, &p->d_items_rank);
+    }
+    if (rc == CP_OK) {
       std::vector<WorkItem> qt = build_items(p, false, kTile);
       p->n_items_q = static_cast<int>(qt.size());
       rc = upload(qt, &p->d_items_q);
@@ -402,6 +413,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       rc = upload(kv, &p->d_items_kv);
     }
     if (rc != CP_OK) {
+      cudaFree(p->d_items_rank);
       cudaFree(p->d_chunk_pos);
       cudaFree(p->d_doc_start);
       cudaFree(p->d_doc_end);
@@ -421,6 +433,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
 void cp_plan_destroy(cp_plan_t* p) {
   if (!p) return;
   if (p->on_device) {
+    cudaFree(p->d_items_rank);
     cudaFree(p->d_chunk_pos);
     cudaFree(p->d_doc_start);
     cudaFree(p->d_doc_end);
@@ -553,6 +566,29 @@ int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const vo
   a.lse = lse;
   a.items = p->d_items_fused;
   a.n_items = p->n_items_fused;
+  return cpattn::launch_attn_fwd(a, stream);
+}
+
+int cp_attn_fwd_rank(const cp_plan_t* p, int rank, const void* q, const void* k, const void* v, void* o, float* lse,
+                     cudaStream_t stream) {
+  if (!p || !q || !k || !v || !o || !lse) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return CP_ERR_ALIGNMENT;
+  if (rank < 0 || rank >= p->P) return CP_ERR_INVALID_ARG;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = p->desc.d;
+  a.o_fp32 = p->desc.out_fp32;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.items = p->d_items_rank + p->rank_item_off[rank];
+  a.n_items = p->rank_item_off[rank + 1] - p->rank_item_off[rank];
   return cpattn::launch_attn_fwd(a, stream);
 }
 

@@ -8,9 +8,17 @@
 // Parts are folded in index order (ring order).
 //
 // HBM-bound: each (row, head) reads n_parts * (4d + 4) bytes and writes
-// 2d + 4.  d/4 threads own one (row, head), one float4 of every part each;
-// consecutive threads cover consecutive addresses, so all loads and stores
-// are coalesced.
+// 2d + 4 (bf16 O) or 4d + 4 (fp32 O).  One warp owns 32 consecutive rows of
+// one head:
+//   1. lane i takes row i: the LSE partials [p][h][row] are read 128 bytes
+//      at a time, and lane i computes the merged LSE and the weights
+//      e^(lse_p - lse) of its row for every part, parked in shared memory;
+//   2. the warp then walks its rows: a row's d floats of one part are 4d
+//      contiguous bytes (d/4 lanes, one float4 each; two rows at a time for
+//      d = 64), and each lane issues the loads of up to eight parts before
+//      it folds them.
+// Consecutive warps take consecutive heads of the same rows, so together
+// they sweep contiguous (row, head, d) ranges of every part.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,6 +31,10 @@
 namespace cpattn {
 namespace {
 
+constexpr int kRows = 32;     // rows per warp unit
+constexpr int kBatch = 8;     // parts whose loads are in flight together
+constexpr int kMaxSmem = 96 * 1024;
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -30,45 +42,78 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(int n_parts, long long rows, int H, const float* __restrict__ o_parts,
+__global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H, const float* __restrict__ o_parts,
                                                     const float* __restrict__ lse_parts, void* __restrict__ o_out,
-                                                    float* __restrict__ lse_out, long long batch, int out_fp32) {
-  constexpr int TPR = D / 4;  // threads per (row, head)
-  const long long per_batch = rows * H;
-  const long long total = batch * per_batch * TPR;
-  for (long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; tid < total;
-       tid += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c4 = static_cast<int>(tid % TPR);
-    const long long rh = tid / TPR;              // (batch, row, head) flat
-    const long long b = rh / per_batch;
-    const long long w = rh - b * per_batch;      // row * H + head
-    const long long row = w / H;
-    const int h = static_cast<int>(w - row * H);
-    const float* lp = lse_parts + b * n_parts * per_batch + static_cast<long long>(h) * rows + row;
-    float m = -INFINITY;
-    for (int p = 0; p < n_parts; ++p) m = fmaxf(m, __ldg(lp + p * per_batch));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int p = 0; p < n_parts; ++p) sum += __expf(__ldg(lp + p * per_batch) - m);
-      lse = m + __logf(sum);
-      const float* op = o_parts + b * n_parts * per_batch * D + w * D + c4 * 4;
-      for (int p = 0; p < n_parts; ++p) {
-        const float wgt = __expf(__ldg(lp + p * per_batch) - lse);
-        const float4 x = __ldg(reinterpret_cast<const float4*>(op + p * per_batch * D));
-        acc.x = fmaf(wgt, x.x, acc.x);
-        acc.y = fmaf(wgt, x.y, acc.y);
-        acc.z = fmaf(wgt, x.z, acc.z);
-        acc.w = fmaf(wgt, x.w, acc.w);
+                                                    float* __restrict__ lse_out, int batch, int out_fp32) {
+  constexpr int TPR = D / 4;         // lanes per row (one float4 each)
+  constexpr int RPI = 32 / TPR;      // rows per warp iteration
+  extern __shared__ float s_w[];     // [warps][n_parts][kRows] weights
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* w = s_w + static_cast<size_t>(warp) * n_parts * kRows;
+  const long long per_batch = static_cast<long long>(rows) * H;
+  const int row_blocks = (rows + kRows - 1) / kRows;
+  const long long units = static_cast<long long>(batch) * row_blocks * H;
+  const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int sub = lane / TPR, c4 = lane % TPR;
+  for (long long un = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + warp; un < units; un += warps_total) {
+    const int h = static_cast<int>(un % H);
+    const long long x = un / H;
+    const int rb = static_cast<int>(x % row_blocks);
+    const int b = static_cast<int>(x / row_blocks);
+    const int row0 = rb * kRows;
+    const int nrow = min(kRows, rows - row0);
+    // 1. merged LSE and per-part weights of row row0 + lane.
+    {
+      const int row = row0 + lane;
+      const bool valid = lane < nrow;
+      const float* lp =
+          lse_parts + static_cast<long long>(b) * n_parts * per_batch + static_cast<long long>(h) * rows + row;
+      float m = -INFINITY;
+      if (valid)
+        for (int p = 0; p < n_parts; ++p) m = fmaxf(m, __ldg(lp + p * per_batch));
+      float lse = -INFINITY;
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int p = 0; p < n_parts; ++p) sum += __expf(__ldg(lp + p * per_batch) - m);
+        lse = m + __logf(sum);
+      }
+      for (int p = 0; p < n_parts; ++p)
+        w[p * kRows + lane] = (m != -INFINITY) ? __expf(__ldg(lp + p * per_batch) - lse) : 0.f;
+      if (valid) lse_out[static_cast<long long>(b) * per_batch + static_cast<long long>(h) * rows + row] = lse;
+    }
+    __syncwarp();
+    // 2. O rows, RPI at a time.
+    const float* ob = o_parts + static_cast<long long>(b) * n_parts * per_batch * D;
+    for (int j0 = 0; j0 < nrow; j0 += RPI) {
+      const int j = j0 + sub;
+      if (j < nrow) {
+        const long long off = (static_cast<long long>(row0 + j) * H + h) * D + c4 * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p0 = 0; p0 < n_parts; p0 += kBatch) {
+          float4 v[kBatch];
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i)
+            if (p0 + i < n_parts) v[i] = __ldg(reinterpret_cast<const float4*>(ob + (p0 + i) * per_batch * D + off));
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            if (p0 + i < n_parts) {
+              const float wt = w[(p0 + i) * kRows + j];
+              acc.x = fmaf(wt, v[i].x, acc.x);
+              acc.y = fmaf(wt, v[i].y, acc.y);
+              acc.z = fmaf(wt, v[i].z, acc.z);
+              acc.w = fmaf(wt, v[i].w, acc.w);
+            }
+          }
+        }
+        const long long oi = static_cast<long long>(b) * per_batch * D + off;
+        if (out_fp32)
+          *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc;
+        else
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oi) =
+              make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
       }
     }
-    const long long oi = (b * per_batch + w) * D + c4 * 4;
-    if (out_fp32)
-      *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc;
-    else
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oi) = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
-    if (c4 == 0) lse_out[b * per_batch + static_cast<long long>(h) * rows + row] = lse;
+    __syncwarp();  // the next unit rewrites the weights
   }
 }
 
@@ -76,22 +121,37 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, long long rows,
 
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts,
                  void* o_out, float* lse_out, int out_fp32, cudaStream_t stream) {
-  const long long work = static_cast<long long>(batch) * rows * H * (d / 4);
-  if (work == 0) return CP_OK;
+  if (static_cast<long long>(batch) * rows * H == 0) return CP_OK;
+  if (n_parts <= 0) return CP_ERR_INVALID_ARG;
+  // Shared memory: n_parts * 32 weights per warp; fewer warps per CTA when
+  // there are many parts.
+  const long long per_warp = static_cast<long long>(n_parts) * kRows * sizeof(float);
+  int warps = 8;
+  while (warps > 1 && per_warp * warps > kMaxSmem) warps >>= 1;
+  if (per_warp * warps > kMaxSmem) return CP_ERR_UNSUPPORTED;  // more than 768 parts
+  const int smem = static_cast<int>(per_warp * warps);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int threads = 256;
-  long long grid = (work + threads - 1) / threads;
-  const long long cap = static_cast<long long>(sms) * 8;
+  const long long units = static_cast<long long>(batch) * ((rows + kRows - 1) / kRows) * H;
+  long long grid = (units + warps - 1) / warps;
+  const long long cap = static_cast<long long>(sms) * (64 / warps);
   if (grid > cap) grid = cap;
-  if (d == 128)
-    merge_kernel<128><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
-                                                                      lse_out, batch, out_fp32);
-  else if (d == 64)
-    merge_kernel<64><<<static_cast<int>(grid), threads, 0, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
-                                                                     lse_out, batch, out_fp32);
-  else
+  const int threads = warps * 32;
+  if (d == 128) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return CP_ERR_CUDA;
+    merge_kernel<128><<<static_cast<int>(grid), threads, smem, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
+                                                                        lse_out, batch, out_fp32);
+  } else if (d == 64) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return CP_ERR_CUDA;
+    merge_kernel<64><<<static_cast<int>(grid), threads, smem, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
+                                                                       lse_out, batch, out_fp32);
+  } else {
     return CP_ERR_UNSUPPORTED;
+  }
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 

@@ -179,6 +179,17 @@ int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void 
 int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                       void *o, float *lse, cudaStream_t stream);
 
+/* One attention rank's share of cp_attn_fwd_local: the outputs of rank
+ * `rank` (= r*U + u; the ring rank r when U == 1), reading every rank's K/V
+ * chunks from the same buffers, i.e. the work one GPU does when each rank
+ * has its own GPU ([MTX] "Split heads or rotate KV": each chip keeps its
+ * queries and visits every KV chunk).  Same layouts and results as
+ * cp_attn_fwd_local (bit for bit on this rank's rows); other ranks' rows of
+ * o and lse are not touched.  rank outside [0, P) => CP_ERR_INVALID_ARG.
+ * No workspace. */
+int cp_attn_fwd_rank(const cp_plan_t *plan, int rank, const void *q, const void *k, const void *v,
+                     void *o, float *lse, cudaStream_t stream);
+
 /* Causal CP attention backward from the forward's O and LSE (activation
  * recompute, [L3P] "Long context changes more than attention cost"): with
  * P = exp(scale*QK^T - LSE),

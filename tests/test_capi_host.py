@@ -101,6 +101,13 @@ def test_workspace_sizes(cpa):
     assert p.workspace_size(cpa.CP_OP_FWD) == 0
 
 
+def test_fwd_rank_rejects_bad_rank(cpa):
+    p = cpa.Plan(1024, 4, 2, 64, ring_degree=4)
+    fake = 256  # aligned, never dereferenced: the rank check comes first
+    for r in (-1, 4):
+        assert cpa._L().cp_attn_fwd_rank(p.handle, r, fake, fake, fake, fake, fake, None) == cpa.CP_ERR_INVALID_ARG
+
+
 def test_strerror(cpa):
     assert cpa.cp_strerror(0) == "ok"
     assert "align" in cpa.cp_strerror(cpa.CP_ERR_ALIGNMENT)

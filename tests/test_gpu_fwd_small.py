@@ -85,6 +85,30 @@ def test_fwd_balanced_layout_matches_oracle(cpa, case):
     gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name)
 
 
+@pytest.mark.parametrize("layout,m,docs", [(1, 2, [0, 300, 1536]), (2, 4, [0, 100, 1000, 1536]), (0, 1, None)])
+def test_fwd_rank_by_rank_equals_all_ranks(cpa, layout, m, docs):
+    """cp_attn_fwd_rank for every ring rank reproduces cp_attn_fwd_local bit
+    for bit, and a rank's call leaves the other ranks' rows untouched."""
+    import gpu_harness as gh
+    L, Hq, Hkv, d, R = 1536, 4, 2, 128, 3
+    inp = _inputs(L, Hq, Hkv, d, seed=50 + layout)
+    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=R, layout=layout, doc_offsets=docs, chunks_per_rank=m)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64))
+    q, k, v = (gh.to_slots(inp[n], idx).cuda() for n in ("q", "k", "v"))
+    o_all = torch.empty_like(q)
+    lse_all = torch.empty(R, Hq, L // R, device="cuda")
+    cpa.cp_attn_fwd_local(plan, q, k, v, o_all, lse_all)
+    o = torch.full_like(q, 7.0)
+    lse = torch.full_like(lse_all, 7.0)
+    n = L // R
+    for r in range(R):
+        cpa.cp_attn_fwd_rank(plan, r, q, k, v, o, lse)
+        torch.cuda.synchronize()
+        assert torch.equal(o[:(r + 1) * n], o_all[:(r + 1) * n]) and torch.equal(lse[:r + 1], lse_all[:r + 1])
+        assert (o[(r + 1) * n:] == 7.0).all() and (lse[r + 1:] == 7.0).all()
+    assert cpa.cp_get_status() == 0
+
+
 def test_fwd_deterministic(cpa):
     import gpu_harness as gh
     inp = _inputs(1536, 8, 2, 128, seed=7)
