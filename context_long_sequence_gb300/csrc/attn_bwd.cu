@@ -118,8 +118,9 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
 
 // ---------------------------------------------------------------- dQ (query-tile outer)
 
-enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = 3, DQ_V_FULL = 5, DQ_V_EMPTY = 7, DQ_SP_FULL = 9,
-             DQ_SP_EMPTY = 10, DQ_DS_FULL = 11, DQ_DONE = 12, DQ_DRAIN = 13, DQ_NUM_BARS = 16 };
+enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = 3, DQ_V_FULL = 5, DQ_V_EMPTY = 7, DQ_S_FULL = 9,
+             DQ_S_EMPTY = 11, DQ_DP_FULL = 13, DQ_DS_FREE = 14, DQ_DS_FULL = 15, DQ_DONE = 16, DQ_DRAIN = 17,
+             DQ_NUM_BARS = 18 };
 
 template <int D>
 struct DqSmem {
@@ -187,8 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(DQ_V_FULL + i), 1);
       mbar_init(bar(DQ_V_EMPTY + i), 1);
     }
-    mbar_init(bar(DQ_SP_FULL), 1);
-    mbar_init(bar(DQ_SP_EMPTY), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(DQ_S_FULL + i), 1);
+      mbar_init(bar(DQ_S_EMPTY + i), 4);
+    }
+    mbar_init(bar(DQ_DP_FULL), 1);
+    mbar_init(bar(DQ_DS_FREE), 1);
     mbar_init(bar(DQ_DS_FULL), 4);
     mbar_init(bar(DQ_DONE), 1);
     mbar_init(bar(DQ_DRAIN), 1);
@@ -203,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  // TMEM: S double-buffered (columns 0 and 384), dP at 128, dQ at 256.
+  const uint32_t tdP = tmem + 128, tdQ = tmem + 256;
+  auto tS = [&](int b) { return tmem + (b ? 384u : 0u); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -243,29 +250,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024), dDS = smem_desc_sw128(sDS, 16, 1024);
+      constexpr uint64_t kStep = SM::kT >> 4;  // one K/V stage in descriptor units
+      // Issue order for key tile n: S_n (into S buffer n & 1), dP_n, dQ_{n-1}.
+      // S_n only needs the element-wise warps to have read S_{n-2}, so it is
+      // queued while they still work on tile n-1.
       int n = 0;
       if (mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status)) {
         for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int, int) {
           if (*abort_flag) return;
           const int st = n & 1;
           const uint32_t ph = (n >> 1) & 1;
+          const uint64_t step = static_cast<uint64_t>(st) * kStep, pstep = static_cast<uint64_t>(st ^ 1) * kStep;
           if (!mbar_wait(bar(DQ_K_FULL + st), ph, abort_flag, status)) return;
+          if (n >= 2 && !mbar_wait(bar(DQ_S_EMPTY + st), ph ^ 1, abort_flag, status)) return;
+          tc_fence_after();
+          mma_qk<D>(tS(st), dQ0, dK0 + step, idesc_s);
+          mma_commit(bar(DQ_S_FULL + st));
           if (!mbar_wait(bar(DQ_V_FULL + st), ph, abort_flag, status)) return;
-          if (!mbar_wait(bar(DQ_SP_EMPTY), (n & 1) ^ 1, abort_flag, status)) return;
+          // DS_FULL: dS_{n-1} is in shared memory and the dP columns are free.
+          if (n > 0 && !mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
           tc_fence_after();
-          const uint64_t step = static_cast<uint64_t>(st) * (SM::kT >> 4);
-          mma_qk<D>(tS, dQ0, dK0 + step, idesc_s);
           mma_qk<D>(tdP, dDO0, dV0 + step, idesc_s);
-          mma_commit(bar(DQ_SP_FULL));
+          mma_commit(bar(DQ_DP_FULL));
           mma_commit(bar(DQ_V_EMPTY + st));
-          if (!mbar_wait(bar(DQ_DS_FULL), n & 1, abort_flag, status)) return;
-          tc_fence_after();
-          // A = dS [queries x keys] K-major; B = K [keys x d] read as N=d x K=keys (MN-major).
-          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + step, idesc_dq, n > 0 ? 1u : 0u);
-          mma_commit(bar(DQ_K_EMPTY + st));
-          mma_commit(bar(DQ_DONE));
+          if (n > 0) {
+            // A = dS [queries x keys] K-major; B = K [keys x d] read as N=d x K=keys (MN-major).
+            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + pstep, idesc_dq, n > 1 ? 1u : 0u);
+            mma_commit(bar(DQ_DS_FREE));
+            mma_commit(bar(DQ_K_EMPTY + (st ^ 1)));
+          }
           ++n;
         });
+        if (n > 0 && !*abort_flag) {
+          if (mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) {
+            tc_fence_after();
+            const uint64_t pstep = static_cast<uint64_t>((n - 1) & 1) * kStep;
+            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + pstep, idesc_dq, n > 1 ? 1u : 0u);
+            mma_commit(bar(DQ_DS_FREE));
+            mma_commit(bar(DQ_K_EMPTY + ((n - 1) & 1)));
+            mma_commit(bar(DQ_DONE));
+          }
+        }
       }
       mma_commit(bar(DQ_DRAIN));
       mbar_wait(bar(DQ_DRAIN), 0, nullptr, status);
@@ -285,41 +310,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int kpos0, int klen) {
       if (!ok) return;
-      ok = warp_all(mbar_wait(bar(DQ_SP_FULL), n & 1, abort_flag, status));
+      const int sb = n & 1;
+      ok = warp_all(mbar_wait(bar(DQ_S_FULL + sb), (n >> 1) & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
       const bool full = (klen == BN) && (kpos0 + BN - 1 <= qpos0) && (lo_max <= kpos0);
       const int c_lo = my_lo - kpos0;
       const int c_hi = min(my_pos - kpos0, klen - 1);
-#pragma unroll 1
+      // Phase A: P = exp2(S * scale*log2e - LSE*log2e), masked, as packed bf16.
+      uint32_t pp[BN / 2];
+      const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
+#pragma unroll
       for (int c4 = 0; c4 < BN / 32; ++c4) {
-        uint32_t sr[32], pr[32];
-        tmem_ld32(tS + lane_off + c4 * 32, sr);
-        tmem_ld32(tdP + lane_off + c4 * 32, pr);
+        uint32_t sr[32];
+        tmem_ld32(tS(sb) + lane_off + c4 * 32, sr);
         tmem_wait_ld();
         reg_fence(sr);
-        reg_fence(pr);
-        float ds[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
-          float p = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -lse2));
-          if (!full && (col < c_lo || col > c_hi)) p = 0.f;
-          ds[e] = p * (__uint_as_float(pr[e]) - dlt);
+          const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, nlse2);
+          float y0, y1;
+          split_f32x2(y, y0, y1);
+          float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
+          if (!full) {
+            if (col < c_lo || col > c_hi) x0 = 0.f;
+            if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+          }
+          pp[c4 * 16 + e / 2] = pack_bf16x2(x0, x1);
         }
-        store_row32_bf16(sDS, row, c4, ds);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQ_S_EMPTY + sb));
+      // Phase B: dS = P * (dP - D) as packed bf16, parked in the dP columns
+      // already read (32-column chunk c4 lands in columns 16c4..).
+      ok = warp_all(mbar_wait(bar(DQ_DP_FULL), n & 1, abort_flag, status));
+      if (!ok) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < BN / 32; ++c4) {
+        uint32_t pr[32], dsp[16];
+        tmem_ld32(tdP + lane_off + c4 * 32, pr);
+        tmem_wait_ld();
+        reg_fence(pr);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const uint32_t pk = pp[c4 * 16 + e / 2];
+          const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                                     make_f32x2(-dlt, -dlt));
+          float d0, d1;
+          split_f32x2(dd, d0, d1);
+          dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
+        }
+        tmem_st16(tdP + lane_off + c4 * 16, dsp);
+      }
+      tmem_wait_st();
+      // dS into shared memory once dQ of the previous key tile has read it.
+      if (n > 0) {
+        ok = warp_all(mbar_wait(bar(DQ_DS_FREE), (n - 1) & 1, abort_flag, status));
+        if (!ok) return;
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < BN / 32; ++c4) {
+        uint32_t dsp[16];
+        tmem_ld16(tdP + lane_off + c4 * 16, dsp);
+        tmem_wait_ld();
+        reg_fence16(dsp);
+        store_row32_packed(sDS, row, c4, dsp);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(DQ_SP_EMPTY));
-        mbar_arrive(bar(DQ_DS_FULL));
-      }
+      if (lane == 0) mbar_arrive(bar(DQ_DS_FULL));
       ++n;
     });
     if (ok && n > 0) {
-      ok = warp_all(mbar_wait(bar(DQ_DONE), (n - 1) & 1, abort_flag, status));
+      ok = warp_all(mbar_wait(bar(DQ_DONE), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
@@ -352,8 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dK, dV (key-tile outer)
 
-enum DkvBar { KV_FULL = 0, KV_QD_FULL = 1, KV_QD_EMPTY = 3, KV_ST_FULL = 5, KV_ST_EMPTY = 6, KV_PT_FULL = 7,
-              KV_PB_FREE = 8, KV_DS_FULL = 9, KV_ACC_DONE = 10, KV_DRAIN = 11, KV_NUM_BARS = 12 };
+enum DkvBar { KV_FULL = 0, KV_QD_FULL = 1, KV_QD_EMPTY = 3, KV_S_FULL = 5, KV_DP_FULL = 6, KV_ST_EMPTY = 7,
+              KV_P_FULL = 8, KV_PB_FREE = 9, KV_DS_FULL = 10, KV_SPB_FREE = 11, KV_ACC_DONE = 12, KV_DRAIN = 13,
+              KV_NUM_BARS = 14 };
 
 template <int D>
 struct DkvSmem {
@@ -424,11 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(KV_QD_FULL + i), 1);
       mbar_init(bar(KV_QD_EMPTY + i), 1);
     }
-    mbar_init(bar(KV_ST_FULL), 1);
+    mbar_init(bar(KV_S_FULL), 1);
+    mbar_init(bar(KV_DP_FULL), 1);
     mbar_init(bar(KV_ST_EMPTY), 4);
-    mbar_init(bar(KV_PT_FULL), 4);
+    mbar_init(bar(KV_P_FULL), 4);
     mbar_init(bar(KV_PB_FREE), 1);
     mbar_init(bar(KV_DS_FULL), 4);
+    mbar_init(bar(KV_SPB_FREE), 1);
     mbar_init(bar(KV_ACC_DONE), 1);
     mbar_init(bar(KV_DRAIN), 1);
     *abort_flag = 0;
@@ -479,30 +549,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dQmn0 = smem_desc_sw128(sQ, HALF_BYTES, 1024), dDOmn0 = smem_desc_sw128(sDO, HALF_BYTES, 1024);
       const uint64_t dPB = smem_desc_sw128(sPB, 16, 1024);
+      constexpr uint64_t kStep = SM::kT >> 4;  // one Q/dO stage in descriptor units
+      // Issue order for query tile n: S_n, dV_{n-1}, dP_n, dK_{n-1}.  S_n only
+      // waits for the element-wise warps to have read S_{n-1} (phase A), so
+      // it runs while they compute dS_{n-1}; dP_n, dV_{n-1} and dK_{n-1} run
+      // while they compute P_n.
       int n = 0;
       if (mbar_wait(bar(KV_FULL), 0, abort_flag, status)) {
         for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int, int, int, int, int) {
           if (*abort_flag) return;
           const int st = n & 1;
+          const uint64_t step = static_cast<uint64_t>(st) * kStep, pstep = static_cast<uint64_t>(st ^ 1) * kStep;
           if (!mbar_wait(bar(KV_QD_FULL + st), (n >> 1) & 1, abort_flag, status)) return;
-          if (!mbar_wait(bar(KV_ST_EMPTY), (n & 1) ^ 1, abort_flag, status)) return;
+          if (n > 0 && !mbar_wait(bar(KV_ST_EMPTY), (n - 1) & 1, abort_flag, status)) return;
           tc_fence_after();
-          const uint64_t step = static_cast<uint64_t>(st) * (SM::kT >> 4);
           mma_qk<D>(tSt, dK0, dQ0 + step, idesc_s);
+          mma_commit(bar(KV_S_FULL));
+          if (n > 0) {
+            // A = P^T [keys x queries] K-major; B = dO [queries x d] as N=d x K=queries (MN-major).
+            if (!mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) return;
+            tc_fence_after();
+            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
+            mma_commit(bar(KV_PB_FREE));
+          }
+          // DS_FULL: dS^T_{n-1} is in shared memory and the dP^T columns are free.
+          if (n > 0 && !mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+          tc_fence_after();
           mma_qk<D>(tdPt, dV0, dDO0 + step, idesc_s);
-          mma_commit(bar(KV_ST_FULL));
-          if (!mbar_wait(bar(KV_PT_FULL), n & 1, abort_flag, status)) return;
-          tc_fence_after();
-          // A = P^T [keys x queries] K-major; B = dO [queries x d] as N=d x K=queries (MN-major).
-          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + step, idesc_acc, n > 0 ? 1u : 0u);
-          mma_commit(bar(KV_PB_FREE));
-          if (!mbar_wait(bar(KV_DS_FULL), n & 1, abort_flag, status)) return;
-          tc_fence_after();
-          mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + step, idesc_acc, n > 0 ? 1u : 0u);
-          mma_commit(bar(KV_QD_EMPTY + st));
-          mma_commit(bar(KV_ACC_DONE));
+          mma_commit(bar(KV_DP_FULL));
+          if (n > 0) {
+            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
+            mma_commit(bar(KV_SPB_FREE));
+            mma_commit(bar(KV_QD_EMPTY + (st ^ 1)));
+          }
           ++n;
         });
+        // dV and dK of the last query tile.
+        if (n > 0 && !*abort_flag) {
+          const uint64_t pstep = static_cast<uint64_t>((n - 1) & 1) * kStep;
+          if (mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) {
+            tc_fence_after();
+            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
+            mma_commit(bar(KV_PB_FREE));
+            if (mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) {
+              tc_fence_after();
+              mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
+              mma_commit(bar(KV_SPB_FREE));
+              mma_commit(bar(KV_QD_EMPTY + ((n - 1) & 1)));
+              mma_commit(bar(KV_ACC_DONE));
+            }
+          }
+        }
       }
       mma_commit(bar(KV_DRAIN));
       mbar_wait(bar(KV_DRAIN), 0, nullptr, status);
@@ -530,48 +627,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar_sync(1, 128);
       if (!ok) return;
-      ok = warp_all(mbar_wait(bar(KV_ST_FULL), n & 1, abort_flag, status));
+      ok = warp_all(mbar_wait(bar(KV_S_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
       const bool full = (it.len == BN) && (qlen == BM) && (kpos_last <= qpos0) && (qpos0 + BM - 1 <= hi_min);
       const int c_lo = key_valid ? kpos - qpos0 : BM;
       const int c_hi = min(hi_k - qpos0, qlen - 1);
-      // Pass 1: P^T -> shared memory (for dV); dS^T (bf16 pairs) parked in
-      // the dP^T columns of TMEM already consumed, until dV has read P^T.
-#pragma unroll 1
+      // Phase A: P^T row = exp2(S^T * scale*log2e - LSE*log2e), masked,
+      // kept as packed bf16 pairs (the operand dV reads, and the P of dS).
+      uint32_t pp[BM / 2];
+#pragma unroll
       for (int c4 = 0; c4 < BM / 32; ++c4) {
-        uint32_t sr[32], pr[32];
+        uint32_t sr[32];
         tmem_ld32(tSt + lane_off + c4 * 32, sr);
-        tmem_ld32(tdPt + lane_off + c4 * 32, pr);
         tmem_wait_ld();
         reg_fence(sr);
-        reg_fence(pr);
-        float p[32];
-        uint32_t dsp[16];
+        const f32x2 nsl2 = make_f32x2(sl2, sl2);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
-          float x = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -sLse[col]));
-          if (!full && (col < c_lo || col > c_hi)) x = 0.f;
-          p[e] = x;
+          const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
+                                    make_f32x2(-sLse[col], -sLse[col + 1]));
+          float y0, y1;
+          split_f32x2(y, y0, y1);
+          float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
+          if (!full) {
+            if (col < c_lo || col > c_hi) x0 = 0.f;
+            if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+          }
+          pp[c4 * 16 + e / 2] = pack_bf16x2(x0, x1);
         }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KV_ST_EMPTY));
+      // P^T into shared memory once dK of the previous tile has read dS^T there.
+      if (n > 0) {
+        ok = warp_all(mbar_wait(bar(KV_SPB_FREE), (n - 1) & 1, abort_flag, status));
+        if (!ok) return;
+      }
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          dsp[e / 2] = pack_bf16x2(p[e] * (__uint_as_float(pr[e]) - sDel[c4 * 32 + e]),
-                                   p[e + 1] * (__uint_as_float(pr[e + 1]) - sDel[c4 * 32 + e + 1]));
-        store_row32_bf16(sPB, row, c4, p);
+      for (int c4 = 0; c4 < BM / 32; ++c4) store_row32_packed(sPB, row, c4, pp + c4 * 16);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KV_P_FULL));
+      // Phase B: dS^T = P^T * (dP^T - D) as packed bf16, parked in the dP^T
+      // columns already read (32-column chunk c4 lands in columns 16c4..).
+      ok = warp_all(mbar_wait(bar(KV_DP_FULL), n & 1, abort_flag, status));
+      if (!ok) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < BM / 32; ++c4) {
+        uint32_t pr[32], dsp[16];
+        tmem_ld32(tdPt + lane_off + c4 * 32, pr);
+        tmem_wait_ld();
+        reg_fence(pr);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = c4 * 32 + e;
+          const uint32_t pk = pp[c4 * 16 + e / 2];
+          const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                                     make_f32x2(-sDel[col], -sDel[col + 1]));
+          float d0, d1;
+          split_f32x2(dd, d0, d1);
+          dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
+        }
         tmem_st16(tdPt + lane_off + c4 * 16, dsp);
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KV_PT_FULL));
-      // Pass 2: dV has read P^T; overwrite the buffer with dS^T.
+      // dS^T over P^T once dV has read P^T.
       ok = warp_all(mbar_wait(bar(KV_PB_FREE), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
-#pragma unroll 1
+#pragma unroll
       for (int c4 = 0; c4 < BM / 32; ++c4) {
         uint32_t dsp[16];
         tmem_ld16(tdPt + lane_off + c4 * 16, dsp);
@@ -582,12 +710,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KV_ST_EMPTY));
       if (lane == 0) mbar_arrive(bar(KV_DS_FULL));
       ++n;
     });
     if (ok && n > 0) {
-      ok = warp_all(mbar_wait(bar(KV_ACC_DONE), (n - 1) & 1, abort_flag, status));
+      ok = warp_all(mbar_wait(bar(KV_ACC_DONE), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
