@@ -15,10 +15,14 @@
 //            query tile of every ring rank (ring order: the chunk of rank
 //            src visits ranks src, src+1, ...) and every query head of the
 //            group; S^T = K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T
-//            through shared memory, dV and dK accumulated in TMEM
+//            written back over them as packed bf16 and read from TMEM as
+//            the A operands of dV += P^T dO and dK += dS^T Q; dV and dK
+//            accumulated in TMEM; three Q and two dO tiles in flight
 //   dq       one CTA per 128-query tile and head: walks the visible key
-//            tiles in ring order like the forward; S = Q K^T and
-//            dP = dO V^T in TMEM, dS through shared memory, dQ in TMEM
+//            tiles in ring order like the forward; S = Q K^T (two TMEM
+//            buffers) and dP = dO V^T in TMEM, dS written back over dP and
+//            read from TMEM as the A operand of dQ += dS K; three K and two
+//            V tiles in flight
 // Gradients of a KV chunk land on the rank that owns the chunk ([MTX]
 // nougat.kr "MaxText long-context training and KV parallelism", "Split heads
 // or rotate KV": the chunk's partial results travel with it).
@@ -27,8 +31,10 @@
 // a = r*U + u holds ring rank r's slots for head group u; U == 1 is plain
 // sequence sharding); the ring runs over r within each head group.
 //
-// Warp roles as in the forward: warp 0 TMA producer, warp 1 TMEM allocator
-// and MMA issuer, warps 2..5 element-wise (one TMEM lane = one row each).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
+// warps 2..9 element-wise: one TMEM lane = one row, warps 2-5 take the
+// first 64 columns of their rows and warps 6-9 the last 64, so two
+// element-wise warps share each SM sub-partition.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,7 +52,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr uint32_t HALF_BYTES = 128 * 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 element-wise
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
@@ -55,27 +61,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Store 32 fp32 values as bf16 into a 128-row, K-major, 128-byte-swizzled
-// tile (two 64-column halves of HALF_BYTES), row `row`, columns
-// [32*c4, 32*c4+32).
-__device__ __forceinline__ void store_row32_bf16(uint32_t tile, int row, int c4, const float* x) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int ch = c4 * 4 + q;  // 16-byte chunk: 8 columns
-    const uint32_t addr = tile + row * 128 + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (row & 7)) << 4);
-    st_shared_v4(addr, pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
-                 pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
-  }
-}
-
-__device__ __forceinline__ void store_row32_packed(uint32_t tile, int row, int c4, const uint32_t* p) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int ch = c4 * 4 + q;
-    const uint32_t addr = tile + row * 128 + (ch >> 3) * HALF_BYTES + (((ch & 7) ^ (row & 7)) << 4);
-    st_shared_v4(addr, p[4 * q + 0], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-  }
-}
 
 // Q K^T-type product over d: A and B both K-major, 128-byte swizzled.
 template <int D>
@@ -118,17 +103,18 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
 
 // ---------------------------------------------------------------- dQ (query-tile outer)
 
-enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = 3, DQ_V_FULL = 5, DQ_V_EMPTY = 7, DQ_S_FULL = 9,
-             DQ_S_EMPTY = 11, DQ_DP_FULL = 13, DQ_DS_FREE = 14, DQ_DS_FULL = 15, DQ_DONE = 16, DQ_DRAIN = 17,
-             DQ_NUM_BARS = 18 };
+enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = 4, DQ_V_FULL = 7, DQ_V_EMPTY = 9, DQ_S_FULL = 11,
+             DQ_S_EMPTY = 13, DQ_DP_FULL = 15, DQ_DS_FULL = 16, DQ_DONE = 17, DQ_DRAIN = 18, DQ_NUM_BARS = 19 };
+
+constexpr int kKStages = 3;  // K tiles in flight (K is last read by dQ, issued a tile later)
+constexpr int kVStages = 2;  // V tiles in flight (V is read by dP only)
 
 template <int D>
 struct DqSmem {
   static constexpr uint32_t kT = 128 * D * 2;
-  static constexpr uint32_t kP = 128 * 128 * 2;
-  static constexpr uint32_t offQ = 0, offDO = kT, offK = 2 * kT, offV = 4 * kT, offDS = 6 * kT;
-  static constexpr uint32_t offBar = offDS + kP;
-  static constexpr uint32_t offMisc = offBar + DQ_NUM_BARS * 8;
+  static constexpr uint32_t offQ = 0, offDO = kT, offK = 2 * kT, offV = offK + kKStages * kT;
+  static constexpr uint32_t offBar = offV + kVStages * kT;
+  static constexpr uint32_t offMisc = offBar + 24 * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
 };
@@ -161,8 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + SM::offQ, sDO = s_base + SM::offDO, sK = s_base + SM::offK, sV = s_base + SM::offV,
-                 sDS = s_base + SM::offDS;
+  const uint32_t sQ = s_base + SM::offQ, sDO = s_base + SM::offDO, sK = s_base + SM::offK, sV = s_base + SM::offV;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
@@ -182,19 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(DQ_QD_FULL), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(bar(DQ_K_FULL + i), 1);
       mbar_init(bar(DQ_K_EMPTY + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(bar(DQ_V_FULL + i), 1);
       mbar_init(bar(DQ_V_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(DQ_S_FULL + i), 1);
-      mbar_init(bar(DQ_S_EMPTY + i), 4);
+      mbar_init(bar(DQ_S_EMPTY + i), 8);
     }
     mbar_init(bar(DQ_DP_FULL), 1);
-    mbar_init(bar(DQ_DS_FREE), 1);
-    mbar_init(bar(DQ_DS_FULL), 4);
+    mbar_init(bar(DQ_DS_FULL), 8);
     mbar_init(bar(DQ_DONE), 1);
     mbar_init(bar(DQ_DRAIN), 1);
     *abort_flag = 0;
@@ -208,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM: S double-buffered (columns 0 and 384), dP at 128, dQ at 256.
+  // TMEM: S double-buffered (columns 0 and 384), dP (then dS, packed bf16) at 128, dQ at 256.
   const uint32_t tdP = tmem + 128, tdQ = tmem + 256;
   auto tS = [&](int b) { return tmem + (b ? 384u : 0u); };
 
@@ -223,73 +209,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk = 0, nv = 0;
       for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int kv_row, int, int) {
         if (*abort_flag) return;
-        const int st = nk & 1;
-        const uint32_t ph = ((nk >> 1) & 1) ^ 1;
-        if (!mbar_wait(bar(DQ_K_EMPTY + st), ph, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(DQ_K_FULL + st), SM::kT);
+        const int ks = nk % kKStages, vs = nv % kVStages;
+        if (!mbar_wait(bar(DQ_K_EMPTY + ks), ((nk / kKStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(DQ_K_FULL + ks), SM::kT);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sK + st * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + st), hkv * D + hh * 64, kv_row);
+          tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + ks), hkv * D + hh * 64, kv_row);
         ++nk;
-        if (!mbar_wait(bar(DQ_V_EMPTY + st), ph, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(DQ_V_FULL + st), SM::kT);
+        if (!mbar_wait(bar(DQ_V_EMPTY + vs), ((nv / kVStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(DQ_V_FULL + vs), SM::kT);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sV + st * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_V_FULL + st), hkv * D + hh * 64, kv_row);
+          tma_load_2d(sV + vs * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_V_FULL + vs), hkv * D + hh * 64, kv_row);
         ++nv;
       });
       if (*abort_flag) {
+        // Wait for this CTA's own copies: the last loads of each stage.
         mbar_wait(bar(DQ_QD_FULL), 0, nullptr, status);
-        for (int i = max(0, nk - 2); i < nk; ++i) mbar_wait(bar(DQ_K_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
-        for (int i = max(0, nv - 2); i < nv; ++i) mbar_wait(bar(DQ_V_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
+        for (int i = max(0, nk - kKStages); i < nk; ++i)
+          mbar_wait(bar(DQ_K_FULL + i % kKStages), (i / kKStages) & 1, nullptr, status);
+        for (int i = max(0, nv - kVStages); i < nv; ++i)
+          mbar_wait(bar(DQ_V_FULL + i % kVStages), (i / kVStages) & 1, nullptr, status);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, D, 1);
-      // Descriptors built once; stage st adds st * tile bytes (>> 4).
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
-      const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024), dDS = smem_desc_sw128(sDS, 16, 1024);
-      constexpr uint64_t kStep = SM::kT >> 4;  // one K/V stage in descriptor units
-      // Issue order for key tile n: S_n (into S buffer n & 1), dP_n, dQ_{n-1}.
-      // S_n only needs the element-wise warps to have read S_{n-2}, so it is
-      // queued while they still work on tile n-1.
+      const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024);
+      constexpr uint64_t kStep = SM::kT >> 4;  // one stage in descriptor units
+      // Issue order for key tile n: S_n (into S buffer n & 1), dQ_{n-1},
+      // dP_n.  dS stays in TMEM over the dP columns it came from and is the
+      // A operand of dQ; dP_n overwrites those columns only after dQ_{n-1},
+      // issued before it by this thread, has read them.
+      auto issue_dq = [&](int m) {  // dQ += dS_m K_m
+        mma_bf16_ts_k128_halves(tdQ, tdP, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
+                                m > 0 ? 1u : 0u);
+        mma_commit(bar(DQ_K_EMPTY + m % kKStages));
+      };
       int n = 0;
       if (mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status)) {
         for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int, int) {
           if (*abort_flag) return;
-          const int st = n & 1;
-          const uint32_t ph = (n >> 1) & 1;
-          const uint64_t step = static_cast<uint64_t>(st) * kStep, pstep = static_cast<uint64_t>(st ^ 1) * kStep;
-          if (!mbar_wait(bar(DQ_K_FULL + st), ph, abort_flag, status)) return;
-          if (n >= 2 && !mbar_wait(bar(DQ_S_EMPTY + st), ph ^ 1, abort_flag, status)) return;
+          const int ks = n % kKStages, vs = n % kVStages, sb = n & 1;
+          if (!mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status)) return;
+          // S buffer sb: the element-wise warps have read S_{n-2} from it.
+          if (n >= 2 && !mbar_wait(bar(DQ_S_EMPTY + sb), ((n >> 1) & 1) ^ 1, abort_flag, status)) return;
           tc_fence_after();
-          mma_qk<D>(tS(st), dQ0, dK0 + step, idesc_s);
-          mma_commit(bar(DQ_S_FULL + st));
-          if (!mbar_wait(bar(DQ_V_FULL + st), ph, abort_flag, status)) return;
-          // DS_FULL: dS_{n-1} is in shared memory and the dP columns are free.
-          if (n > 0 && !mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
-          tc_fence_after();
-          mma_qk<D>(tdP, dDO0, dV0 + step, idesc_s);
-          mma_commit(bar(DQ_DP_FULL));
-          mma_commit(bar(DQ_V_EMPTY + st));
+          mma_qk<D>(tS(sb), dQ0, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
+          mma_commit(bar(DQ_S_FULL + sb));
           if (n > 0) {
-            // A = dS [queries x keys] K-major; B = K [keys x d] read as N=d x K=keys (MN-major).
-            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + pstep, idesc_dq, n > 1 ? 1u : 0u);
-            mma_commit(bar(DQ_DS_FREE));
-            mma_commit(bar(DQ_K_EMPTY + (st ^ 1)));
+            if (!mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+            tc_fence_after();
+            issue_dq(n - 1);
           }
+          if (!mbar_wait(bar(DQ_V_FULL + vs), (n / kVStages) & 1, abort_flag, status)) return;
+          tc_fence_after();
+          mma_qk<D>(tdP, dDO0, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s);
+          mma_commit(bar(DQ_DP_FULL));
+          mma_commit(bar(DQ_V_EMPTY + vs));
           ++n;
         });
-        if (n > 0 && !*abort_flag) {
-          if (mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) {
-            tc_fence_after();
-            const uint64_t pstep = static_cast<uint64_t>((n - 1) & 1) * kStep;
-            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdQ, dDS, dKmn0 + pstep, idesc_dq, n > 1 ? 1u : 0u);
-            mma_commit(bar(DQ_DS_FREE));
-            mma_commit(bar(DQ_K_EMPTY + ((n - 1) & 1)));
-            mma_commit(bar(DQ_DONE));
-          }
+        if (n > 0 && !*abort_flag && mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) {
+          tc_fence_after();
+          issue_dq(n - 1);
+          mma_commit(bar(DQ_DONE));
         }
       }
       mma_commit(bar(DQ_DRAIN));
@@ -297,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int wq = warp & 3;
+    const int half = (warp - 2) >> 2;  // warps 2-5: key columns 0-63; warps 6-9: 64-127
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const bool row_valid = row < it.len;
@@ -317,11 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = (klen == BN) && (kpos0 + BN - 1 <= qpos0) && (lo_max <= kpos0);
       const int c_lo = my_lo - kpos0;
       const int c_hi = min(my_pos - kpos0, klen - 1);
-      // Phase A: P = exp2(S * scale*log2e - LSE*log2e), masked, as packed bf16.
-      uint32_t pp[BN / 2];
+      // Phase A: P = exp2(S * scale*log2e - LSE*log2e), masked, as packed bf16
+      // (this warp's half of the row: 32-column chunks c4 = 2*half, 2*half+1).
+      uint32_t pp[BN / 4];
       const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
 #pragma unroll
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c4 = 2 * half + cc;
         uint32_t sr[32];
         tmem_ld32(tS(sb) + lane_off + c4 * 32, sr);
         tmem_wait_ld();
@@ -337,49 +324,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col < c_lo || col > c_hi) x0 = 0.f;
             if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
           }
-          pp[c4 * 16 + e / 2] = pack_bf16x2(x0, x1);
+          pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(DQ_S_EMPTY + sb));
-      // Phase B: dS = P * (dP - D) as packed bf16, parked in the dP columns
-      // already read (32-column chunk c4 lands in columns 16c4..).
+      // Phase B: dS = P * (dP - D), packed to bf16 pairs over the dP columns
+      // this warp has read (32-column chunk cc of this half -> columns
+      // 64*half + 16*cc ..): the A operand of dQ.
       ok = warp_all(mbar_wait(bar(DQ_DP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c4 = 2 * half + cc;
         uint32_t pr[32], dsp[16];
         tmem_ld32(tdP + lane_off + c4 * 32, pr);
         tmem_wait_ld();
         reg_fence(pr);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const uint32_t pk = pp[c4 * 16 + e / 2];
+          const uint32_t pk = pp[cc * 16 + e / 2];
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(-dlt, -dlt));
           float d0, d1;
           split_f32x2(dd, d0, d1);
           dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
         }
-        tmem_st16(tdP + lane_off + c4 * 16, dsp);
+        tmem_st16(tdP + lane_off + 64 * half + 16 * cc, dsp);
       }
       tmem_wait_st();
-      // dS into shared memory once dQ of the previous key tile has read it.
-      if (n > 0) {
-        ok = warp_all(mbar_wait(bar(DQ_DS_FREE), (n - 1) & 1, abort_flag, status));
-        if (!ok) return;
-      }
-#pragma unroll
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
-        uint32_t dsp[16];
-        tmem_ld16(tdP + lane_off + c4 * 16, dsp);
-        tmem_wait_ld();
-        reg_fence16(dsp);
-        store_row32_packed(sDS, row, c4, dsp);
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(DQ_DS_FULL));
@@ -391,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       float* dst = args.dq + (static_cast<size_t>(a * g.T + it.q0 + row) * Hq + h) * D;
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32];
         if (n > 0) {
           tmem_ld32(tdQ + lane_off + c4 * 32, v);
@@ -419,17 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dK, dV (key-tile outer)
 
-enum DkvBar { KV_FULL = 0, KV_QD_FULL = 1, KV_QD_EMPTY = 3, KV_S_FULL = 5, KV_DP_FULL = 6, KV_ST_EMPTY = 7,
-              KV_P_FULL = 8, KV_PB_FREE = 9, KV_DS_FULL = 10, KV_SPB_FREE = 11, KV_ACC_DONE = 12, KV_DRAIN = 13,
-              KV_NUM_BARS = 14 };
+enum DkvBar { KV_FULL = 0, KV_Q_FULL = 1, KV_Q_EMPTY = 4, KV_DO_FULL = 7, KV_DO_EMPTY = 9, KV_S_FULL = 11,
+              KV_DP_FULL = 12, KV_P_FULL = 13, KV_DS_FULL = 14, KV_ACC_DONE = 15, KV_DRAIN = 16, KV_NUM_BARS = 17 };
+
+constexpr int kQStages = 3;   // Q tiles in flight (Q is last read by dK, the last product of a tile)
+constexpr int kDOStages = 2;  // dO tiles in flight (dO is last read by dV)
 
 template <int D>
 struct DkvSmem {
   static constexpr uint32_t kT = 128 * D * 2;
-  static constexpr uint32_t kP = 128 * 128 * 2;
-  static constexpr uint32_t offK = 0, offV = kT, offQ = 2 * kT, offDO = 4 * kT, offPB = 6 * kT;
-  static constexpr uint32_t offBar = offPB + kP;
-  static constexpr uint32_t offLD = offBar + KV_NUM_BARS * 8;   // 128 lse2 + 128 delta floats
+  static constexpr uint32_t offK = 0, offV = kT, offQ = 2 * kT, offDO = offQ + kQStages * kT;
+  static constexpr uint32_t offBar = offDO + kDOStages * kT;
+  static constexpr uint32_t offLD = offBar + 24 * 8;   // 128 -LSE*log2(e) + 128 -D floats
   static constexpr uint32_t offMisc = offLD + 2 * 128 * 4;
   static constexpr uint32_t kUsed = offMisc + 16;
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
@@ -456,6 +432,57 @@ __device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int 
   }
 }
 
+// The same walk as for_each_q_tile, one tile at a time, so a caller can look
+// one tile ahead.
+struct QTile {
+  int rr, qslot0, qpos0, qlen, h;
+};
+
+struct QTileWalk {
+  const AttnGeom& g;
+  int src, kpos0, hi_max, jh;
+  int s = 0, ch = 0, t = 0, t1 = -1, hh = 0, rr = 0, cslot0 = 0, cpos0 = 0;
+  bool in_chunk = false;
+  __device__ QTileWalk(const AttnGeom& g_, int src_, int kpos0_, int hi_max_, int jh_)
+      : g(g_), src(src_), kpos0(kpos0_), hi_max(hi_max_), jh(jh_) {}
+  __device__ bool next(QTile& q) {
+    for (;;) {
+      if (in_chunk) {
+        if (hh < g.G) {
+          q.rr = rr;
+          q.qslot0 = cslot0 + t * BM;
+          q.qpos0 = cpos0 + t * BM;
+          q.qlen = min(BM, g.chunk - t * BM);
+          q.h = jh * g.G + hh;
+          ++hh;
+          return true;
+        }
+        hh = 0;
+        if (++t <= t1) continue;
+        in_chunk = false;
+        ++ch;
+      }
+      if (ch >= g.nchunks) {
+        ch = 0;
+        ++s;
+      }
+      if (s >= g.R) return false;
+      rr = (src + s) % g.R;
+      cslot0 = ch * g.chunk;
+      cpos0 = slot_pos(g, rr, cslot0);
+      const int lo = max(cpos0, kpos0);
+      const int hi = min(cpos0 + g.chunk - 1, hi_max);
+      if (lo > hi) {
+        ++ch;
+        continue;
+      }
+      t = (lo - cpos0) / BM;
+      t1 = (hi - cpos0) / BM;
+      in_chunk = true;
+    }
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -466,11 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV, sQ = s_base + SM::offQ, sDO = s_base + SM::offDO,
-                 sPB = s_base + SM::offPB;
+  const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV, sQ = s_base + SM::offQ, sDO = s_base + SM::offDO;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
-  float* sLse = reinterpret_cast<float*>(smem + SM::offLD);
-  float* sDel = sLse + 128;
+  float* sLse = reinterpret_cast<float*>(smem + SM::offLD);  // -LSE * log2(e) per query column
+  float* sDel = sLse + 128;                                  // -D per query column
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
 
@@ -488,17 +514,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(KV_FULL), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(KV_QD_FULL + i), 1);
-      mbar_init(bar(KV_QD_EMPTY + i), 1);
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(bar(KV_Q_FULL + i), 1);
+      mbar_init(bar(KV_Q_EMPTY + i), 1);
+    }
+    for (int i = 0; i < kDOStages; ++i) {
+      mbar_init(bar(KV_DO_FULL + i), 1);
+      mbar_init(bar(KV_DO_EMPTY + i), 1);
     }
     mbar_init(bar(KV_S_FULL), 1);
     mbar_init(bar(KV_DP_FULL), 1);
-    mbar_init(bar(KV_ST_EMPTY), 4);
-    mbar_init(bar(KV_P_FULL), 4);
-    mbar_init(bar(KV_PB_FREE), 1);
-    mbar_init(bar(KV_DS_FULL), 4);
-    mbar_init(bar(KV_SPB_FREE), 1);
+    mbar_init(bar(KV_P_FULL), 8);
+    mbar_init(bar(KV_DS_FULL), 8);
     mbar_init(bar(KV_ACC_DONE), 1);
     mbar_init(bar(KV_DRAIN), 1);
     *abort_flag = 0;
@@ -512,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // TMEM: S^T (then P^T, packed bf16) at 0, dP^T (then dS^T) at 128, dV at 256, dK at 256 + D.
   const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp == 0) {
@@ -522,23 +550,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
       }
-      int nq = 0;
+      int nq = 0, ndo = 0;  // Q and dO loads issued
       for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int rr, int qslot0, int, int, int h) {
         if (*abort_flag) return;
-        const int st = nq & 1;
-        const uint32_t ph = ((nq >> 1) & 1) ^ 1;
-        if (!mbar_wait(bar(KV_QD_EMPTY + st), ph, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(KV_QD_FULL + st), 2 * SM::kT);
+        const int qs = nq % kQStages, ds = ndo % kDOStages;
         const int qrow = (rr * g.U + u) * g.T + qslot0;
-        for (int hh = 0; hh < NH; ++hh) {
-          tma_load_2d(sQ + st * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_QD_FULL + st), h * D + hh * 64, qrow);
-          tma_load_2d(sDO + st * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_QD_FULL + st), h * D + hh * 64, qrow);
-        }
+        if (!mbar_wait(bar(KV_Q_EMPTY + qs), ((nq / kQStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(KV_Q_FULL + qs), SM::kT);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_Q_FULL + qs), h * D + hh * 64, qrow);
         ++nq;
+        if (!mbar_wait(bar(KV_DO_EMPTY + ds), ((ndo / kDOStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(KV_DO_FULL + ds), SM::kT);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_DO_FULL + ds), h * D + hh * 64, qrow);
+        ++ndo;
       });
       if (*abort_flag) {
+        // Wait for this CTA's own copies before it exits (a stage is reused
+        // only after its previous load landed, so the last loads of each
+        // stage are the only ones that can still be in flight).
         mbar_wait(bar(KV_FULL), 0, nullptr, status);
-        for (int i = max(0, nq - 2); i < nq; ++i) mbar_wait(bar(KV_QD_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
+        for (int i = max(0, nq - kQStages); i < nq; ++i)
+          mbar_wait(bar(KV_Q_FULL + i % kQStages), (i / kQStages) & 1, nullptr, status);
+        for (int i = max(0, ndo - kDOStages); i < ndo; ++i)
+          mbar_wait(bar(KV_DO_FULL + i % kDOStages), (i / kDOStages) & 1, nullptr, status);
       }
     }
   } else if (warp == 1) {
@@ -548,56 +584,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dQmn0 = smem_desc_sw128(sQ, HALF_BYTES, 1024), dDOmn0 = smem_desc_sw128(sDO, HALF_BYTES, 1024);
-      const uint64_t dPB = smem_desc_sw128(sPB, 16, 1024);
-      constexpr uint64_t kStep = SM::kT >> 4;  // one Q/dO stage in descriptor units
-      // Issue order for query tile n: S_n, dV_{n-1}, dP_n, dK_{n-1}.  S_n only
-      // waits for the element-wise warps to have read S_{n-1} (phase A), so
-      // it runs while they compute dS_{n-1}; dP_n, dV_{n-1} and dK_{n-1} run
-      // while they compute P_n.
+      constexpr uint64_t kStep = SM::kT >> 4;  // one stage in descriptor units
+      // Issue order for query tile n: dV_{n-1}, S_n, dK_{n-1}, dP_n.  P^T and
+      // dS^T stay in TMEM, where the element-wise warps wrote them over the
+      // S^T and dP^T they came from, and are the A operands of dV and dK;
+      // S_n (dP_n) overwrites those columns only after dV_{n-1} (dK_{n-1}),
+      // issued before it by this thread, has read them.
+      auto issue_dv = [&](int m) {  // dV += P^T_m dO_m
+        mma_bf16_ts_k128_halves(tdV, tSt, dDOmn0 + static_cast<uint64_t>(m % kDOStages) * kStep, idesc_acc,
+                                m > 0 ? 1u : 0u);
+        mma_commit(bar(KV_DO_EMPTY + m % kDOStages));
+      };
+      auto issue_dk = [&](int m) {  // dK += dS^T_m Q_m
+        mma_bf16_ts_k128_halves(tdK, tdPt, dQmn0 + static_cast<uint64_t>(m % kQStages) * kStep, idesc_acc,
+                                m > 0 ? 1u : 0u);
+        mma_commit(bar(KV_Q_EMPTY + m % kQStages));
+      };
       int n = 0;
       if (mbar_wait(bar(KV_FULL), 0, abort_flag, status)) {
         for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int, int, int, int, int) {
           if (*abort_flag) return;
-          const int st = n & 1;
-          const uint64_t step = static_cast<uint64_t>(st) * kStep, pstep = static_cast<uint64_t>(st ^ 1) * kStep;
-          if (!mbar_wait(bar(KV_QD_FULL + st), (n >> 1) & 1, abort_flag, status)) return;
-          if (n > 0 && !mbar_wait(bar(KV_ST_EMPTY), (n - 1) & 1, abort_flag, status)) return;
-          tc_fence_after();
-          mma_qk<D>(tSt, dK0, dQ0 + step, idesc_s);
-          mma_commit(bar(KV_S_FULL));
           if (n > 0) {
-            // A = P^T [keys x queries] K-major; B = dO [queries x d] as N=d x K=queries (MN-major).
             if (!mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) return;
             tc_fence_after();
-            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
-            mma_commit(bar(KV_PB_FREE));
+            issue_dv(n - 1);
           }
-          // DS_FULL: dS^T_{n-1} is in shared memory and the dP^T columns are free.
-          if (n > 0 && !mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+          const int qs = n % kQStages, ds = n % kDOStages;
+          if (!mbar_wait(bar(KV_Q_FULL + qs), (n / kQStages) & 1, abort_flag, status)) return;
           tc_fence_after();
-          mma_qk<D>(tdPt, dV0, dDO0 + step, idesc_s);
-          mma_commit(bar(KV_DP_FULL));
+          mma_qk<D>(tSt, dK0, dQ0 + static_cast<uint64_t>(qs) * kStep, idesc_s);
+          mma_commit(bar(KV_S_FULL));
           if (n > 0) {
-            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
-            mma_commit(bar(KV_SPB_FREE));
-            mma_commit(bar(KV_QD_EMPTY + (st ^ 1)));
+            if (!mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+            tc_fence_after();
+            issue_dk(n - 1);
           }
+          if (!mbar_wait(bar(KV_DO_FULL + ds), (n / kDOStages) & 1, abort_flag, status)) return;
+          tc_fence_after();
+          mma_qk<D>(tdPt, dV0, dDO0 + static_cast<uint64_t>(ds) * kStep, idesc_s);
+          mma_commit(bar(KV_DP_FULL));
           ++n;
         });
         // dV and dK of the last query tile.
-        if (n > 0 && !*abort_flag) {
-          const uint64_t pstep = static_cast<uint64_t>((n - 1) & 1) * kStep;
-          if (mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) {
+        if (n > 0 && !*abort_flag && mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) {
+          tc_fence_after();
+          issue_dv(n - 1);
+          if (mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) {
             tc_fence_after();
-            mma_bf16_ss_k128_bmn<HALF_BYTES>(tdV, dPB, dDOmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
-            mma_commit(bar(KV_PB_FREE));
-            if (mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) {
-              tc_fence_after();
-              mma_bf16_ss_k128_bmn<HALF_BYTES>(tdK, dPB, dQmn0 + pstep, idesc_acc, n > 1 ? 1u : 0u);
-              mma_commit(bar(KV_SPB_FREE));
-              mma_commit(bar(KV_QD_EMPTY + ((n - 1) & 1)));
-              mma_commit(bar(KV_ACC_DONE));
-            }
+            issue_dk(n - 1);
+            mma_commit(bar(KV_ACC_DONE));
           }
         }
       }
@@ -606,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;  // key row of the tile
-    const int etid = threadIdx.x - 64;  // 0..127 across the element-wise warps
+    const int half = (warp - 2) >> 2;  // warps 2-5: query columns 0-63; warps 6-9: 64-127
+    const int row = wq * 32 + lane;     // key row of the tile
+    const int etid = threadIdx.x - 64;  // 0..255 across the element-wise warps
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const bool key_valid = row < it.len;
     const int kpos = kpos0 + row;
@@ -615,17 +651,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = g.scale * kLog2e;
     int n = 0;
     bool ok = true;
-    for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int rr, int qslot0, int qpos0, int qlen, int h) {
-      // Stage this query tile's LSE (log2 units) and D for all 128 columns.
-      // Every element-wise warp walks the same tiles and reaches both
-      // barriers on every tile, also after an abort, so they stay balanced.
-      named_bar_sync(1, 128);  // everyone finished reading the previous tile's values
-      {
-        const size_t li = (static_cast<size_t>(rr * g.U + u) * Hq + h) * g.T + qslot0 + etid;
-        sLse[etid] = etid < qlen ? args.lse[li] * kLog2e : INFINITY;
-        sDel[etid] = etid < qlen ? args.delta[li] : 0.f;
+    // LSE and D of the next query tile are loaded (into registers) while the
+    // current one is processed, then staged in shared memory for all warps.
+    QTileWalk walk(g, src, kpos0, hi_max, jh);
+    QTile cur, nxt;
+    bool have = walk.next(cur);
+    float pf_lse = 0.f, pf_del = 0.f;
+    int pf_len = 0;
+    auto prefetch = [&](const QTile& q) {
+      pf_len = q.qlen;
+      if (etid < q.qlen) {
+        const size_t li = (static_cast<size_t>(q.rr * g.U + u) * Hq + q.h) * g.T + q.qslot0 + etid;
+        pf_lse = args.lse[li];
+        pf_del = args.delta[li];
       }
-      named_bar_sync(1, 128);
+    };
+    if (have) prefetch(cur);
+    auto process = [&](int qpos0, int qlen) {
       if (!ok) return;
       ok = warp_all(mbar_wait(bar(KV_S_FULL), n & 1, abort_flag, status));
       if (!ok) return;
@@ -633,21 +675,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = (it.len == BN) && (qlen == BM) && (kpos_last <= qpos0) && (qpos0 + BM - 1 <= hi_min);
       const int c_lo = key_valid ? kpos - qpos0 : BM;
       const int c_hi = min(hi_k - qpos0, qlen - 1);
-      // Phase A: P^T row = exp2(S^T * scale*log2e - LSE*log2e), masked,
-      // kept as packed bf16 pairs (the operand dV reads, and the P of dS).
-      uint32_t pp[BM / 2];
+      // Phase A: P^T = exp2(S^T * scale*log2e - LSE*log2e), masked, packed to
+      // bf16 pairs and written back over the S^T columns this warp has read
+      // (32-column chunk cc of this half -> columns 64*half + 16*cc ..).
+      uint32_t pp[BM / 4];
+      const f32x2 nsl2 = make_f32x2(sl2, sl2);
 #pragma unroll
-      for (int c4 = 0; c4 < BM / 32; ++c4) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c4 = 2 * half + cc;
         uint32_t sr[32];
         tmem_ld32(tSt + lane_off + c4 * 32, sr);
         tmem_wait_ld();
         reg_fence(sr);
-        const f32x2 nsl2 = make_f32x2(sl2, sl2);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
+          const float2 nl = *reinterpret_cast<const float2*>(sLse + col);
           const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
-                                    make_f32x2(-sLse[col], -sLse[col + 1]));
+                                    make_f32x2(nl.x, nl.y));
           float y0, y1;
           split_f32x2(y, y0, y1);
           float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
@@ -655,29 +700,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col < c_lo || col > c_hi) x0 = 0.f;
             if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
           }
-          pp[c4 * 16 + e / 2] = pack_bf16x2(x0, x1);
+          pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
         }
+        tmem_st16(tSt + lane_off + 64 * half + 16 * cc, *reinterpret_cast<const uint32_t(*)[16]>(pp + cc * 16));
       }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KV_ST_EMPTY));
-      // P^T into shared memory once dK of the previous tile has read dS^T there.
-      if (n > 0) {
-        ok = warp_all(mbar_wait(bar(KV_SPB_FREE), (n - 1) & 1, abort_flag, status));
-        if (!ok) return;
-      }
-#pragma unroll
-      for (int c4 = 0; c4 < BM / 32; ++c4) store_row32_packed(sPB, row, c4, pp + c4 * 16);
-      fence_proxy_async_smem();
-      __syncwarp();
       if (lane == 0) mbar_arrive(bar(KV_P_FULL));
-      // Phase B: dS^T = P^T * (dP^T - D) as packed bf16, parked in the dP^T
-      // columns already read (32-column chunk c4 lands in columns 16c4..).
+      // Phase B: dS^T = P^T * (dP^T - D), packed to bf16 pairs over the dP^T
+      // columns this warp has read (same column map as P^T).
       ok = warp_all(mbar_wait(bar(KV_DP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < BM / 32; ++c4) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c4 = 2 * half + cc;
         uint32_t pr[32], dsp[16];
         tmem_ld32(tdPt + lane_off + c4 * 32, pr);
         tmem_wait_ld();
@@ -685,41 +723,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
-          const uint32_t pk = pp[c4 * 16 + e / 2];
+          const uint32_t pk = pp[cc * 16 + e / 2];
+          const float2 nd = *reinterpret_cast<const float2*>(sDel + col);
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
-                                     make_f32x2(-sDel[col], -sDel[col + 1]));
+                                     make_f32x2(nd.x, nd.y));
           float d0, d1;
           split_f32x2(dd, d0, d1);
           dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
         }
-        tmem_st16(tdPt + lane_off + c4 * 16, dsp);
+        tmem_st16(tdPt + lane_off + 64 * half + 16 * cc, dsp);
       }
       tmem_wait_st();
-      // dS^T over P^T once dV has read P^T.
-      ok = warp_all(mbar_wait(bar(KV_PB_FREE), n & 1, abort_flag, status));
-      if (!ok) return;
-      tc_fence_after();
-#pragma unroll
-      for (int c4 = 0; c4 < BM / 32; ++c4) {
-        uint32_t dsp[16];
-        tmem_ld16(tdPt + lane_off + c4 * 16, dsp);
-        tmem_wait_ld();
-        reg_fence16(dsp);
-        store_row32_packed(sPB, row, c4, dsp);
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(KV_DS_FULL));
       ++n;
-    });
+    };
+    while (have) {
+      // Every element-wise warp walks the same tiles and reaches both
+      // barriers on every tile, also after an abort, so they stay balanced.
+      named_bar_sync(1, 256);  // everyone finished reading the previous tile's values
+      if (etid < BM) {
+        const bool in = etid < pf_len;
+        sLse[etid] = in ? -pf_lse * kLog2e : -INFINITY;
+        sDel[etid] = in ? -pf_del : 0.f;
+      }
+      named_bar_sync(1, 256);
+      const bool have_next = walk.next(nxt);
+      if (have_next) prefetch(nxt);
+      process(cur.qpos0, cur.qlen);
+      cur = nxt;
+      have = have_next;
+    }
     if (ok && n > 0) {
       ok = warp_all(mbar_wait(bar(KV_ACC_DONE), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
       const size_t orow = (static_cast<size_t>(a * g.T + it.q0 + row) * Hkv + jh) * D;
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32], k[32];
         if (n > 0) {
           tmem_ld32(tdV + lane_off + c4 * 32, v);
