@@ -464,6 +464,31 @@ def ring_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True
     return np.stack(O), np.stack(LSE)
 
 
+def allgather_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True,
+                      scale=None, chunks_per_rank=4):
+    """All-gather CP forward ([MTX] "Why KV comes back together": every chip
+    gathers the K/V of all chips and computes attention for the tokens it
+    holds; [L3P] "Four parallelisms secure different resources": the packed
+    documents' mask is kept).  The gathered K/V is the global sequence, so
+    rank r attends with its own query rows over every key position.
+    Returns per-rank O [R][n][Hq][d] and LSE [R][Hq][n] in slot order.
+    """
+    L = q.shape[0]
+    n = L // R
+    pos = ring_positions(L, R, layout, offsets, chunks_per_rank)
+    k_all = unshard(shard(k, pos), pos)      # all-gather: the shards put back in position order
+    v_all = unshard(shard(v, pos), pos)
+    key_pos = np.arange(L, dtype=np.int64)
+    O, LSE = [], []
+    for r in range(R):
+        rows = pos[r * n:(r + 1) * n]
+        o, lse = attention_rows(q, k_all, v_all, rows=rows, k_pos=key_pos,
+                                offsets=offsets, causal=causal, scale=scale)
+        O.append(o)
+        LSE.append(lse)
+    return np.stack(O), np.stack(LSE)
+
+
 def usp_forward(q, k, v, U, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True,
                 scale=None, chunks_per_rank=4):
     """USP = Ulysses groups x ring ([MTX] "Split heads or rotate KV").

@@ -329,6 +329,20 @@ def pin_ring_balanced_equals_full(orc):
         np.testing.assert_allclose(o.reshape(L, Hq, d), O[pos], rtol=1e-12, atol=1e-12)
 
 
+def pin_allgather_equals_full(orc):
+    """All-gather CP (every layout, with documents) equals full attention,
+    rank by rank in slot order."""
+    L, Hq, Hkv, d = 48, 4, 2, 4
+    q, k, v = _rand((L, Hq, d), 43), _rand((L, Hkv, d), 44), _rand((L, Hkv, d), 45)
+    for offs in (None, [0, 7, 30, 48]):
+        O, LSE = orc.attention(q, k, v, offsets=offs)
+        for R, layout, m in [(4, 0, 1), (3, 1, 2), (2, 2, 3)]:
+            o, lse = orc.allgather_forward(q, k, v, R, layout, offsets=offs, chunks_per_rank=m)
+            pos = orc.ring_positions(L, R, layout, offs, m)
+            np.testing.assert_allclose(o.reshape(L, Hq, d), O[pos], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(np.concatenate(list(lse), axis=1), LSE[:, pos], rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- backward
 
 
