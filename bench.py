@@ -215,6 +215,8 @@ def main():
     ap.add_argument("--layout", choices=["workload", "contiguous", "zigzag", "balanced"], default="workload",
                     help="token layout of the ring shards (default: the workload's own)")
     ap.add_argument("--chunks-per-rank", type=int, default=8, help="chunks per ring rank of the balanced layout")
+    ap.add_argument("--kv-exchange", choices=["ring", "allgather"], default="ring",
+                    help="how ranks obtain the other ranks' K/V (all-gather: ring plans with U == 1 only)")
     ap.add_argument("--backward", action="store_true",
                     help="add the backward to every step (the ring fwd+bwd workload always has it)")
     ap.add_argument("--L", type=int, default=0,
@@ -251,7 +253,8 @@ def main():
     dev = torch.device("cuda", local_rank)
 
     plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
-                    doc_offsets=offsets, emit_partials=w.emit_partials, chunks_per_rank=args.chunks_per_rank)
+                    doc_offsets=offsets, emit_partials=w.emit_partials, chunks_per_rank=args.chunks_per_rank,
+                    kv_exchange=cpa.CP_KV_ALLGATHER if args.kv_exchange == "allgather" else cpa.CP_KV_RING)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
     # each rank draws its own sequence.
     g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale,
@@ -355,6 +358,8 @@ def main():
         lh = torch.empty(R, U, w.Hq // U, plan.L // R, dtype=torch.float32, device=dev)
     else:
         qh, kh, vh, oh, lh = q, k, v, o, lse
+        if args.kv_exchange == "allgather":  # the attention alone reads the gathered K/V (position order)
+            kh, vh = g_inputs["k"], g_inputs["v"]
 
     def timed(fn, reps):
         ts = []
@@ -374,7 +379,7 @@ def main():
     if U == 1 and not w.emit_partials:
         # Each ring rank's share alone (cp_attn_fwd_rank): the forward time of
         # one GPU per rank, communication aside, is the slowest rank's.
-        per_rank = [timed(lambda r=r: cpa.cp_attn_fwd_rank(plan, r, q, k, v, o, lse, stream=stream), reps)
+        per_rank = [timed(lambda r=r: cpa.cp_attn_fwd_rank(plan, r, q, kh, vh, o, lse, stream=stream), reps)
                     for r in range(R)]
         kern["attn_fwd_per_rank"] = {"ms": [round(t, 4) for t in per_rank], "max_ms": max(per_rank),
                                      "max_over_mean": max(per_rank) / statistics.mean(per_rank)}
@@ -440,6 +445,7 @@ def main():
             "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": U, "ring": R,
                        "layout": ["contiguous", "zigzag", f"balanced (m={args.chunks_per_rank})"][w.layout],
                        "rank_work_spread": rank_work_spread(plan.index_map(), w.ring, offsets),
+                       "kv_exchange": args.kv_exchange,
                        "docs": bool(offsets is not None),
                        "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
                        "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",

@@ -31,6 +31,8 @@ CP_NOALLOC_SCRATCH_BYTES = 8 << 20
 CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1
 CP_LAYOUT_BALANCED = 2
+CP_KV_RING = 0
+CP_KV_ALLGATHER = 1
 CP_SEQ_TO_HEAD = 0
 CP_HEAD_TO_SEQ = 1
 CP_TOKEN_MAJOR = 0
@@ -56,6 +58,7 @@ class cp_plan_desc_t(ctypes.Structure):
         ("emit_partials", ctypes.c_int32),
         ("out_fp32", ctypes.c_int32),
         ("chunks_per_rank", ctypes.c_int32),
+        ("kv_exchange", ctypes.c_int32),
     ]
 
 
@@ -135,7 +138,7 @@ class Plan:
 
     def __init__(self, L, Hq, Hkv, d, ulysses_degree=1, ring_degree=1, layout=CP_LAYOUT_CONTIGUOUS,
                  doc_offsets=None, softmax_scale=0.0, emit_partials=False, causal=True, out_fp32=False,
-                 chunks_per_rank=8):
+                 chunks_per_rank=8, kv_exchange=CP_KV_RING):
         self._h = None
         desc = cp_plan_desc_t()
         desc.version = CP_ATTN_PLAN_VERSION
@@ -155,6 +158,7 @@ class Plan:
         desc.emit_partials = 1 if emit_partials else 0
         desc.out_fp32 = 1 if out_fp32 else 0
         desc.chunks_per_rank = int(chunks_per_rank)
+        desc.kv_exchange = int(kv_exchange)
         h = _vp()
         _check(_L().cp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "cp_plan_create")
         self._h = h
@@ -164,6 +168,7 @@ class Plan:
         self.n = self.L // self.P
         self.layout = desc.layout
         self.chunks_per_rank = desc.chunks_per_rank
+        self.kv_exchange = desc.kv_exchange
         self.emit_partials = bool(emit_partials)
         self.out_fp32 = bool(out_fp32)
 

@@ -95,6 +95,12 @@ struct FwdSmem {
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end,
                                                  int lo_min, int qpos_last, F&& f) {
+  if (g.kv_global) {
+    // All-gathered K/V: row = position; one pass in position order.
+    const int t1 = qpos_last / BN;
+    for (int t = lo_min / BN; t <= t1; ++t) f(t * BN, t * BN, min(BN, g.L - t * BN));
+    return;
+  }
   const int nchunks = g.nchunks;
   for (int s = s_begin; s < s_end; ++s) {
     const int src = (r - s + g.R) % g.R;

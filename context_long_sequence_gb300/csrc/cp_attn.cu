@@ -85,6 +85,7 @@ AttnGeom geom(const cp_plan* p, bool on_host = false) {
   g.chunk = p->chunk;
   g.nchunks = p->nchunks;
   g.chunk_pos = p->chunk_pos.empty() ? nullptr : (on_host ? p->chunk_pos.data() : p->d_chunk_pos);
+  g.kv_global = d.kv_exchange == CP_KV_ALLGATHER ? 1 : 0;
   g.scale = p->scale;
   g.doc_start = p->d_doc_start;
   g.doc_end = p->d_doc_end;
@@ -97,6 +98,7 @@ int visited_tiles(const cp_plan* p, const AttnGeom& g, int r, int q0, int len, i
   const int qpos0 = cpattn::slot_pos(g, r, q0);
   const int qpos_last = qpos0 + len - 1;
   const int lo_min = doc_start_host(p, qpos0);
+  if (g.kv_global) return qpos_last / kTile - lo_min / kTile + 1;
   int count = 0;
   for (int s = s_begin; s < s_end; ++s) {
     const int src = (r - s + g.R) % g.R;
@@ -238,7 +240,7 @@ int check_device(const cp_plan* p) {
 }
 
 struct FwdWorkspace {
-  size_t qh, kh, vh, oh, lseh, opart, lsepart, total;
+  size_t qh, kh, vh, oh, lseh, opart, lsepart, kall, vall, total;
 };
 
 FwdWorkspace fwd_workspace(const cp_plan* p) {
@@ -261,6 +263,10 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
   if (d.emit_partials) {
     w.opart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * d.d * 4);
     w.lsepart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * 4);
+  }
+  if (d.kv_exchange == CP_KV_ALLGATHER) {  // the gathered K and V, in position order
+    w.kall = take(L * d.Hkv * d.d * 2);
+    w.vall = take(L * d.Hkv * d.d * 2);
   }
   w.total = off;
   return w;
@@ -325,6 +331,8 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   const int T = d.L / R;
   if (T % U) return CP_ERR_INVALID_ARG;
   if (d.emit_partials && U != 1) return CP_ERR_UNSUPPORTED;
+  if (d.kv_exchange != CP_KV_RING && d.kv_exchange != CP_KV_ALLGATHER) return CP_ERR_INVALID_ARG;
+  if (d.kv_exchange == CP_KV_ALLGATHER && (U != 1 || d.emit_partials)) return CP_ERR_UNSUPPORTED;
   // Index arithmetic in the kernels is 32-bit for positions and slots.
   if (static_cast<long long>(d.L) * U >= (1LL << 31)) return CP_ERR_UNSUPPORTED;
 
@@ -519,6 +527,16 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
       return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse,
                                   d.out_fp32, stream);
     }
+    if (d.kv_exchange == CP_KV_ALLGATHER) {
+      // All-gather: K and V of every rank to their positions, then each
+      // rank's queries attend over the gathered sequence.
+      const long long row_bytes = static_cast<long long>(d.Hkv) * d.d * 2;
+      if ((rc = cpattn::launch_gather_rows(a.g, row_bytes, k, ws + w.kall, stream)) ||
+          (rc = cpattn::launch_gather_rows(a.g, row_bytes, v, ws + w.vall, stream)))
+        return rc;
+      a.k = ws + w.kall;
+      a.v = ws + w.vall;
+    }
     a.items = p->d_items_fused;
     a.n_items = p->n_items_fused;
     return cpattn::launch_attn_fwd(a, stream);
@@ -606,6 +624,7 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cpattn::BwdArgs a{};
   a.g = geom(p);
+  a.g.kv_global = 0;  // the backward walks the ring order over the owners' K/V slots
   a.q = q;
   a.k = k;
   a.v = v;

@@ -25,6 +25,7 @@ struct AttnGeom {
   int nchunks;             // chunks per ring rank: 1 (contiguous), 2 (zigzag), m (balanced)
   const int32_t* chunk_pos;  // balanced: [R][nchunks] first position of each chunk (host or
                              // device copy, matching where slot_pos runs); else null
+  int kv_global;           // 1: K/V rows are in global position order (all-gathered), U == 1
   float scale;             // softmax scale
   const int32_t* doc_start;  // [L] start of the document holding each position, or null
   const int32_t* doc_end;    // [L] one past the end of that document, or null
@@ -77,6 +78,10 @@ struct BwdArgs {
 };
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+
+// All-gather of K or V in the emulation: out[slot_pos(r, t)] = in[r*T + t],
+// rows of row_bytes (a multiple of 16).
+int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream);
 
 // Block-permutation copy behind ulysses_reshard.
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind,

@@ -15,6 +15,10 @@
 // writes are both contiguous and fully coalesced; the source offset is
 // computed once per segment, not per vector.  Each warp keeps four segments
 // in flight.  HBM-bound; the grid is a multiple of the SM count.
+//
+// gather_rows_kernel is the all-gather of K/V in the one-GPU emulation
+// ([MTX] "Why KV comes back together": every chip collects the whole K/V):
+// slot rows of every rank are written to their global positions.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -112,6 +116,20 @@ __global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, 
   }
 }
 
+// All-gather in the emulation: each warp moves one slot row to its position.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                                          AttnGeom g, uint32_t vecs) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t rows = static_cast<uint32_t>(g.R) * g.T;
+  for (uint32_t slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; slot < rows; slot += warps) {
+    const int r = static_cast<int>(slot / g.T), t = static_cast<int>(slot % g.T);
+    const uint64_t src = static_cast<uint64_t>(slot) * vecs;
+    const uint64_t dst = static_cast<uint64_t>(slot_pos(g, r, t)) * vecs;
+    for (uint32_t v = lane; v < vecs; v += 32) out[dst + v] = __ldg(in + src + v);
+  }
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -123,6 +141,20 @@ int sm_count() {
 }
 
 }  // namespace
+
+int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream) {
+  if (g.U != 1 || row_bytes <= 0 || row_bytes % 16 || row_bytes / 16 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(g.R) * g.T;
+  if (rows == 0) return CP_OK;
+  const int threads = 256;
+  long long grid = (rows * 32 + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (grid > cap) grid = cap;
+  gather_rows_kernel<<<static_cast<int>(grid), threads, 0, stream>>>(static_cast<const uint4*>(in),
+                                                                     static_cast<uint4*>(out), g,
+                                                                     static_cast<uint32_t>(row_bytes / 16));
+  return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
 
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind, int elem_bytes,
                    const void* in, void* out, cudaStream_t stream) {

@@ -82,6 +82,12 @@ extern "C" {
                                      rank keeps its chunks in position order.  With m = 2 and one
                                      document this is exactly the zigzag layout. */
 
+/* How a rank obtains the other ranks' K/V ([MTX] "Why KV comes back together",
+ * "Split heads or rotate KV"; [L3P] "Four parallelisms secure different resources"). */
+#define CP_KV_RING      0         /* ring (P2P): KV chunks visit the ranks in ring order */
+#define CP_KV_ALLGATHER 1         /* all-gather: every rank first gathers the whole K/V, then
+                                     attends over it in position order (U == 1, fused merge) */
+
 /* Reshard directions and tensor kinds for ulysses_reshard(). */
 #define CP_SEQ_TO_HEAD 0
 #define CP_HEAD_TO_SEQ 1
@@ -115,6 +121,10 @@ typedef struct {
                                  cp_attn_fwd, cp_attn_fwd_local and cp_attn_fwd_noalloc and to the
                                  o input of cp_attn_bwd; cp_merge_lse always writes bf16. */
   int32_t chunks_per_rank;    /* CP_LAYOUT_BALANCED: m >= 1 chunks per ring rank; ignored otherwise */
+  int32_t kv_exchange;        /* CP_KV_RING (0) or CP_KV_ALLGATHER (1; requires U == 1 and
+                                 emit_partials == 0).  The backward is the same computation either
+                                 way: dK, dV land in the owner's slots (the reduce-scatter that
+                                 mirrors the all-gather). */
 } cp_plan_desc_t;
 
 typedef struct cp_plan cp_plan_t;   /* opaque; immutable after creation; usable from any stream */
@@ -162,7 +172,10 @@ int ulysses_reshard(const cp_plan_t *plan, int direction, int tensor_kind, int H
  * workspace, runs ring attention per head group and reshards O and LSE back
  * ([MTX] "Split heads or rotate KV": the two exchanges around attention).
  * Per ring rank r and step s the visiting chunk comes from rank (r-s) mod R;
- * tiles with no visible pair are skipped, partially visible tiles are masked.
+ * with CP_KV_ALLGATHER the call first gathers K and V of all ranks into
+ * position order in the workspace, and every rank's queries then walk the
+ * gathered keys in position order.  Tiles with no visible pair are skipped,
+ * partially visible tiles are masked.
  * workspace: cp_workspace_size(plan, CP_OP_FWD) bytes (may be NULL when 0). */
 int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                 void *o, float *lse, void *workspace, size_t workspace_bytes,
@@ -175,7 +188,9 @@ int cp_attn_fwd(const cp_plan_t *plan, const void *q, const void *k, const void 
  * the ring runs over r for each head group u).
  *   q  [R][U][T][Hq/U][d] bf16,  k, v [R][U][T][Hkv/U][d] bf16, T = L/R
  *   o  [R][U][T][Hq/U][d] bf16 (fp32 if out_fp32) out,  lse [R][U][Hq/U][T] fp32 out
- * With U == 1 this is cp_attn_fwd with the fused merge.  No workspace. */
+ * With U == 1 this is cp_attn_fwd with the fused merge; for a CP_KV_ALLGATHER
+ * plan k and v are the gathered copies, [L][Hkv][d] in position order.
+ * No workspace. */
 int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                       void *o, float *lse, cudaStream_t stream);
 
@@ -184,8 +199,9 @@ int cp_attn_fwd_local(const cp_plan_t *plan, const void *q, const void *k, const
  * chunks from the same buffers, i.e. the work one GPU does when each rank
  * has its own GPU ([MTX] "Split heads or rotate KV": each chip keeps its
  * queries and visits every KV chunk).  Same layouts and results as
- * cp_attn_fwd_local (bit for bit on this rank's rows); other ranks' rows of
- * o and lse are not touched.  rank outside [0, P) => CP_ERR_INVALID_ARG.
+ * cp_attn_fwd_local (bit for bit on this rank's rows; for a CP_KV_ALLGATHER
+ * plan k and v are the gathered copies in position order); other ranks'
+ * rows of o and lse are not touched.  rank outside [0, P) => CP_ERR_INVALID_ARG.
  * No workspace. */
 int cp_attn_fwd_rank(const cp_plan_t *plan, int rank, const void *q, const void *k, const void *v,
                      void *o, float *lse, cudaStream_t stream);

@@ -473,6 +473,7 @@ def allgather_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal
     rank r attends with its own query rows over every key position.
     Returns per-rank O [R][n][Hq][d] and LSE [R][Hq][n] in slot order.
     """
+    q, k, v = _f64(q), _f64(k), _f64(v)     # exact for bf16 / fp32 inputs
     L = q.shape[0]
     n = L // R
     pos = ring_positions(L, R, layout, offsets, chunks_per_rank)

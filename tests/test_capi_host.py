@@ -77,6 +77,9 @@ def test_balanced_index_map_matches_oracle(cpa, L, R, U, m, docs):
     (dict(L=96, Hq=8, Hkv=4, d=64, ring_degree=2, layout=2, chunks_per_rank=0), -1),   # balanced needs m >= 1
     (dict(L=96, Hq=8, Hkv=4, d=64, ring_degree=2, layout=2, chunks_per_rank=5), -1),   # m*R does not divide L
     (dict(L=96, Hq=8, Hkv=4, d=64, layout=3), -1),                                    # unknown layout
+    (dict(L=96, Hq=8, Hkv=4, d=64, kv_exchange=2), -1),                               # unknown KV exchange
+    (dict(L=96, Hq=8, Hkv=4, d=64, ulysses_degree=2, kv_exchange=1), -2),             # all-gather is U == 1
+    (dict(L=96, Hq=8, Hkv=4, d=64, ring_degree=2, emit_partials=True, kv_exchange=1), -2),
 ])
 def test_plan_validation(cpa, kw, code):
     with pytest.raises(cpa.CPError) as e:
@@ -99,6 +102,8 @@ def test_workspace_sizes(cpa):
     assert p.workspace_size(cpa.CP_OP_FWD) == al(4 * 1024 * 4 * 64 * 4) + al(4 * 1024 * 4 * 4)
     p = cpa.Plan(1024, 4, 4, 64, ring_degree=4)
     assert p.workspace_size(cpa.CP_OP_FWD) == 0
+    p = cpa.Plan(1000, 4, 2, 64, ring_degree=4, layout=1, kv_exchange=cpa.CP_KV_ALLGATHER)
+    assert p.workspace_size(cpa.CP_OP_FWD) == 2 * al(1000 * 2 * 64 * 2)   # gathered K and V
 
 
 def test_fwd_rank_rejects_bad_rank(cpa):

@@ -67,6 +67,19 @@ def test_bwd_balanced_layout(cpa, U, R, m, docs):
     gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], f"balanced U{U} R{R} m{m}")
 
 
+def test_bwd_allgather_plan(cpa):
+    """An all-gather plan's backward (dK, dV land in the owners' slots)."""
+    import gpu_harness as gh
+    L, Hq, Hkv, d = 1024, 4, 2, 128
+    docs = [0, 300, 1024]
+    inp = workloads.make_inputs(L, Hq, Hkv, d, 61, with_do=True)
+    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=4, layout=1, doc_offsets=docs, kv_exchange=cpa.CP_KV_ALLGATHER)
+    got = gh.bwd(plan, inp["q"], inp["k"], inp["v"], inp["do"])
+    _, _, dq, dk, dv = oracle.attention_bwd(inp["q"].double().numpy(), inp["k"].double().numpy(),
+                                            inp["v"].double().numpy(), inp["do"].double().numpy(), offsets=docs)
+    gh.assert_grads_close([g.numpy() for g in got], [dq, dk, dv], "allgather plan")
+
+
 def test_bwd_deterministic(cpa):
     import gpu_harness as gh
     inp = workloads.make_inputs(1024, 4, 2, 128, 5, with_do=True)

@@ -109,6 +109,58 @@ def test_fwd_rank_by_rank_equals_all_ranks(cpa, layout, m, docs):
     assert cpa.cp_get_status() == 0
 
 
+ALLGATHER_CASES = [
+    # name, L, Hq, Hkv, d, R, layout, chunks_per_rank, docs
+    ("allgather_contig_R4_docs", 1024, 4, 2, 128, 4, 0, 1, [0, 100, 700, 1024]),
+    ("allgather_zigzag_R3_d64", 1536, 8, 2, 64, 3, 1, 2, None),
+    ("allgather_balanced_m3_docs", 1536, 4, 1, 128, 2, 2, 3, [0, 5, 900, 1536]),
+    ("allgather_ragged", 1000, 4, 4, 128, 2, 1, 2, [0, 499, 1000]),
+]
+
+
+@pytest.mark.parametrize("case", ALLGATHER_CASES, ids=[c[0] for c in ALLGATHER_CASES])
+def test_fwd_allgather_matches_oracle(cpa, case):
+    """All-gather KV exchange: gather K/V to position order, then every rank's
+    queries walk the gathered keys."""
+    import gpu_harness as gh
+    name, L, Hq, Hkv, d, R, layout, m, docs = case
+    inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(name.encode()) % 1000)
+    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=R, layout=layout, doc_offsets=docs, chunks_per_rank=m,
+                    kv_exchange=cpa.CP_KV_ALLGATHER, out_fp32=True)
+    O, LSE = gh.fwd(plan, inp["q"], inp["k"], inp["v"])
+    o_ref, lse_ref = oracle.allgather_forward(inp["q"], inp["k"], inp["v"], R, layout, offsets=docs,
+                                              chunks_per_rank=m)
+    pos = oracle.ring_positions(L, R, layout, docs, m)
+    O_ref = np.empty((L, Hq, d))
+    O_ref[pos] = o_ref.reshape(L, Hq, d)
+    LSE_ref = np.empty((Hq, L))
+    LSE_ref[:, pos] = np.concatenate(list(lse_ref), axis=1)
+    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name)
+
+
+def test_fwd_allgather_rank_by_rank(cpa):
+    """cp_attn_fwd_rank on an all-gather plan (K/V passed gathered, in
+    position order) reproduces cp_attn_fwd bit for bit."""
+    import gpu_harness as gh
+    L, Hq, Hkv, d, R = 1536, 4, 2, 128, 3
+    inp = _inputs(L, Hq, Hkv, d, seed=77)
+    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=R, layout=1, doc_offsets=[0, 800, 1536],
+                    kv_exchange=cpa.CP_KV_ALLGATHER)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64))
+    q, k, v = (gh.to_slots(inp[n], idx).cuda() for n in ("q", "k", "v"))
+    o_all = torch.empty_like(q)
+    lse_all = torch.empty(R, Hq, L // R, device="cuda")
+    cpa.cp_attn_fwd(plan, q, k, v, o_all, lse_all, cpa.alloc_workspace(plan))
+    kg, vg = inp["k"].cuda(), inp["v"].cuda()
+    o = torch.full_like(q, 3.0)
+    lse = torch.full_like(lse_all, 3.0)
+    for r in range(R):
+        cpa.cp_attn_fwd_rank(plan, r, q, kg, vg, o, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_all) and torch.equal(lse, lse_all)
+    assert cpa.cp_get_status() == 0
+
+
 def test_fwd_deterministic(cpa):
     import gpu_harness as gh
     inp = _inputs(1536, 8, 2, 128, seed=7)

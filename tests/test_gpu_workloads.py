@@ -87,22 +87,25 @@ def test_workload_forward_sampled(cpa, wi, out_fp32):
     gh.assert_close(O, LSE, O_ref, LSE_ref, w.name, bf16_out=not out_fp32)
 
 
-def test_packed_documents_balanced_layout_sampled(cpa):
+@pytest.mark.parametrize("kv_exchange", [0, 1], ids=["ring", "allgather"])
+def test_packed_documents_balanced_layout_sampled(cpa, kv_exchange):
     """The packed-document workload (L = 131072, R = 16, seeded documents)
-    on the work-balanced layout with 8 chunks per rank: sampled rows against
-    the oracle."""
+    on the work-balanced layout with 8 chunks per rank, with the ring or the
+    all-gather KV exchange: sampled rows against the oracle."""
     import gpu_harness as gh
     w = workloads.WORKLOADS[3]
     offsets = workloads.workload_doc_offsets(w)
     plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ring_degree=w.ring, layout=cpa.CP_LAYOUT_BALANCED, doc_offsets=offsets,
-                    chunks_per_rank=8, out_fp32=True)
+                    chunks_per_rank=8, out_fp32=True, kv_exchange=kv_exchange)
     g = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device="cuda", k_scale=w.k_scale)
     idx = torch.from_numpy(plan.index_map().astype(np.int64)).to("cuda")
     q, k, v = (g[n][idx].contiguous() for n in ("q", "k", "v"))
     o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device="cuda")
-    cpa.cp_attn_fwd(plan, q, k, v, o, lse, cpa.alloc_workspace(plan))
+    ws = cpa.alloc_workspace(plan)
+    cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws)
     assert cpa.cp_get_status() == 0
+    del ws
     slot_of = torch.empty_like(idx)
     slot_of[idx] = torch.arange(w.L, device="cuda")
     c = w.L // (8 * w.ring)
