@@ -57,9 +57,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 
 // Q K^T-type product over d: A and B both K-major, 128-byte swizzled.
