@@ -57,6 +57,20 @@ def row_visible(pos: np.ndarray, offsets) -> np.ndarray:
     return pos - start + 1
 
 
+def workload_config(w, offsets, args, world: int, positions) -> dict:
+    """The `config` object of the JSON line (both arms print the same one).
+    positions: the slot -> global position map of the plan."""
+    return {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": w.ulysses, "ring": w.ring,
+            "layout": ["contiguous", "zigzag", f"balanced (m={args.chunks_per_rank})"][w.layout],
+            "rank_work_spread": rank_work_spread(positions, w.ring, offsets),
+            "kv_exchange": args.kv_exchange,
+            "docs": bool(offsets is not None),
+            "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
+            "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",
+            "step": "forward + backward" if w.backward else "forward",
+            "l2": "flushed (256 MiB write) before every timed step"}
+
+
 def rank_work_spread(index_map, R: int, offsets) -> float:
     """max / mean over ring ranks of the visible (query, key) pairs whose
     query the rank holds: a query at position i sees i - doc_start(i) + 1 keys."""
@@ -442,15 +456,7 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": U, "ring": R,
-                       "layout": ["contiguous", "zigzag", f"balanced (m={args.chunks_per_rank})"][w.layout],
-                       "rank_work_spread": rank_work_spread(plan.index_map(), w.ring, offsets),
-                       "kv_exchange": args.kv_exchange,
-                       "docs": bool(offsets is not None),
-                       "num_docs": 0 if offsets is None else len(offsets) - 1, "P": w.P,
-                       "parallelism": f"replicas x{world} (all {w.P} CP ranks emulated per GPU)",
-                       "step": "forward + backward" if w.backward else "forward",
-                       "l2": "flushed (256 MiB write) before every timed step"},
+            "config": workload_config(w, offsets, args, world, plan.index_map()),
             "tokens_per_s": round(world * w.L / (ms_per_step * 1e-3), 1),
             "useful_flops_per_step": flops_step,
             "e2e": {"value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
@@ -490,6 +496,7 @@ def cpu_baseline(w, g_inputs, offsets):
 def run_reference(args, w, offsets, flops_step, warmup, world):
     """The CPU oracle as the reference arm: each step is a bounded sample (a
     fixed number of seeded random query rows over all heads)."""
+    import oracle
     cpu = cpu_inputs(w)
     heads = list(range(w.Hq))
     rows = 16 if w.L >= 65536 else 32
@@ -510,8 +517,8 @@ def run_reference(args, w, offsets, flops_step, warmup, world):
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
         "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": w.ulysses,
-                   "ring": w.ring},
+        "config": workload_config(w, offsets, args, world,
+                                  oracle.ring_positions(w.L, w.ring, w.layout, offsets, args.chunks_per_rank)),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
