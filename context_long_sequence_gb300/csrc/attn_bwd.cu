@@ -303,13 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (this warp's half of the row: 32-column chunks c4 = 2*half, 2*half+1).
       uint32_t pp[BN / 4];
       const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
+      uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
+      tmem_ld32(tS(sb) + lane_off + 64 * half, sr2[0]);
+      tmem_ld32(tS(sb) + lane_off + 64 * half + 32, sr2[1]);
+      tmem_wait_ld();
+      reg_fence(sr2[0]);
+      reg_fence(sr2[1]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c4 = 2 * half + cc;
-        uint32_t sr[32];
-        tmem_ld32(tS(sb) + lane_off + c4 * 32, sr);
-        tmem_wait_ld();
-        reg_fence(sr);
+        const uint32_t* sr = sr2[cc];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
@@ -333,13 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_all(mbar_wait(bar(DQ_DP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
+      uint32_t pr2[2][32];
+      tmem_ld32(tdP + lane_off + 64 * half, pr2[0]);
+      tmem_ld32(tdP + lane_off + 64 * half + 32, pr2[1]);
+      tmem_wait_ld();
+      reg_fence(pr2[0]);
+      reg_fence(pr2[1]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c4 = 2 * half + cc;
-        uint32_t pr[32], dsp[16];
-        tmem_ld32(tdP + lane_off + c4 * 32, pr);
-        tmem_wait_ld();
-        reg_fence(pr);
+        const uint32_t* pr = pr2[cc];
+        uint32_t dsp[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const uint32_t pk = pp[cc * 16 + e / 2];
@@ -677,13 +683,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (32-column chunk cc of this half -> columns 64*half + 16*cc ..).
       uint32_t pp[BM / 4];
       const f32x2 nsl2 = make_f32x2(sl2, sl2);
+      uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
+      tmem_ld32(tSt + lane_off + 64 * half, sr2[0]);
+      tmem_ld32(tSt + lane_off + 64 * half + 32, sr2[1]);
+      tmem_wait_ld();
+      reg_fence(sr2[0]);
+      reg_fence(sr2[1]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c4 = 2 * half + cc;
-        uint32_t sr[32];
-        tmem_ld32(tSt + lane_off + c4 * 32, sr);
-        tmem_wait_ld();
-        reg_fence(sr);
+        const uint32_t* sr = sr2[cc];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
@@ -710,13 +719,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_all(mbar_wait(bar(KV_DP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
+      uint32_t pr2[2][32];
+      tmem_ld32(tdPt + lane_off + 64 * half, pr2[0]);
+      tmem_ld32(tdPt + lane_off + 64 * half + 32, pr2[1]);
+      tmem_wait_ld();
+      reg_fence(pr2[0]);
+      reg_fence(pr2[1]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c4 = 2 * half + cc;
-        uint32_t pr[32], dsp[16];
-        tmem_ld32(tdPt + lane_off + c4 * 32, pr);
-        tmem_wait_ld();
-        reg_fence(pr);
+        const uint32_t* pr = pr2[cc];
+        uint32_t dsp[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
