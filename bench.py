@@ -330,36 +330,83 @@ def main():
         raise RuntimeError("device status set during the timed region")
 
     # ---- end to end through the public API with host buffers
-    q_h, k_h, v_h = (t.cpu().pin_memory() for t in (q, k, v))
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-
-    ins = [(q, q_h), (k, k_h), (v, v_h)]
-    outs = [(o, o_h), (lse, lse_h)]
+    # Every step copies its inputs from pinned host memory and its results
+    # back.  Pipelined: two device buffer sets, host->device copies on one
+    # stream and device->host copies on another, so the copies of
+    # neighbouring steps overlap the computation of this one (the way a
+    # training loop feeds the GPU).  The serial figure (copy in, compute,
+    # copy out, one step after the other on one stream) is reported too.
+    in_names = ["q", "k", "v"] + (["do"] if w.backward else [])
+    out_names = ["o", "lse"] + (["dq", "dk", "dv"] if w.backward else [])
+    set0 = {"q": q, "k": k, "v": v, "o": o, "lse": lse}
     if w.backward:
-        ins.append((do, do.cpu().pin_memory()))
-        outs += [(t, torch.empty(t.shape, dtype=t.dtype).pin_memory()) for t in (dq, dk, dv)]
+        set0.update(do=do, dq=dq, dk=dk, dv=dv)
+    sets = [set0, {n: torch.empty_like(t) for n, t in set0.items()}]
+    host_in = {n: set0[n].cpu().pin_memory() for n in in_names}
+    host_out = [{n: torch.empty(set0[n].shape, dtype=set0[n].dtype).pin_memory() for n in out_names}
+                for _ in range(2)]
 
-    def e2e_step():
-        for dst, src in ins:
-            dst.copy_(src, non_blocking=True)
-        step()
-        for src, dst in outs:
-            dst.copy_(src, non_blocking=True)
+    def step_on(b):
+        S = sets[b]
+        cpa.cp_attn_fwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], ws, stream=stream)
+        if w.backward:
+            cpa.cp_attn_bwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], S["do"], S["dq"], S["dk"], S["dv"],
+                            ws_bwd, stream=stream)
 
-    for _ in range(2):
-        e2e_step()
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def pipelined(nsteps):
+        s_h2d.wait_stream(stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_h2d)
+        for i in range(nsteps):
+            b = i % 2
+            if i >= 2:
+                s_h2d.wait_event(ev_comp[b])     # step i-2 no longer reads these inputs
+            with torch.cuda.stream(s_h2d):
+                for n in in_names:
+                    sets[b][n].copy_(host_in[n], non_blocking=True)
+            ev_in[b].record(s_h2d)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])     # step i-2's results have left these buffers
+            step_on(b)
+            ev_comp[b].record(stream)
+            s_d2h.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_d2h):
+                for n in out_names:
+                    host_out[b][n].copy_(sets[b][n], non_blocking=True)
+            ev_out[b].record(s_d2h)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(s_d2h)                         # after the last copy, which follows everything
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    def serial_step():
+        for n in in_names:
+            set0[n].copy_(host_in[n], non_blocking=True)
+        step_on(0)
+        for n in out_names:
+            host_out[0][n].copy_(set0[n], non_blocking=True)
+
     e2e_steps = max(3, min(args.steps, 10))
+    pipelined(2)
+    barrier()
+    e2e_ms = pipelined(e2e_steps) / e2e_steps
+    for _ in range(2):
+        serial_step()
     barrier()
     ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ee0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        serial_step()
     ee1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
-    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
+    e2e_serial_ms = ee0.elapsed_time(ee1) / e2e_steps
+    h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in in_names)
+    d2h = sum(set0[n].numel() * set0[n].element_size() for n in out_names)
+    del sets[1]
 
     # ---- per-kernel breakdown (the dominant kernel's roofline)
     kern = {}
@@ -431,7 +478,8 @@ def main():
     del o_parts, lse_parts, o_m, lse_m
 
     peaks, peak_src = load_peaks()
-    total_ms, e2e_ms_max, attn_ms_max = max_over_ranks([total_ms, e2e_ms, attn_ms], dist, dev)
+    total_ms, e2e_ms_max, e2e_serial_ms_max, attn_ms_max = max_over_ranks(
+        [total_ms, e2e_ms, e2e_serial_ms, attn_ms], dist, dev)
 
     result = None
     if rank == 0:
@@ -460,7 +508,10 @@ def main():
             "tokens_per_s": round(world * w.L / (ms_per_step * 1e-3), 1),
             "useful_flops_per_step": flops_step,
             "e2e": {"value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4)},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
+                    "overlap": "2 device buffer sets; H2D and D2H of neighbouring steps overlap compute",
+                    "serial_value": round(world * flops_step / (e2e_serial_ms_max * 1e-3) / 1e12, 3),
+                    "serial_ms_per_step": round(e2e_serial_ms_max, 4)},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
