@@ -488,6 +488,7 @@ def main():
         # forward: 3 reshards in, attention, 2 reshards out (U > 1); merge with
         # partials.  backward: delta, dkv, dq, plus 6 reshards in and 3 out (U > 1).
         launches_per_step = ((6 if U > 1 else 1) + (1 if w.emit_partials else 0)
+                             + (2 if args.kv_exchange == "allgather" else 0)
                              + ((3 + (9 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
