@@ -30,8 +30,31 @@
 namespace cpattn {
 namespace {
 
+// Division by a runtime divisor d >= 1 for x < 2^31, by multiply and shift
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994: with 2^(l-1) < d <= 2^l and m = floor(2^(31+l)/d) + 1,
+// floor(x/d) = floor(m*x / 2^(31+l)) for every 31-bit x; m < 2^32).
+struct FastDiv {
+  uint32_t d, m, sh;
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t x) const {
+    return static_cast<uint32_t>((static_cast<uint64_t>(x) * m) >> sh);
+  }
+  __host__ __device__ __forceinline__ uint32_t mod(uint32_t x) const { return x - div(x) * d; }
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.d = d;
+  f.m = static_cast<uint32_t>((1ull << (31 + l)) / d + 1);
+  f.sh = 31 + l;
+  return f;
+}
+
 struct ReshardGeom {
   uint32_t U, n, H, Hl;  // Hl = H / U
+  FastDiv fU, fn, fH, fHl;
   uint32_t blk;          // block size in vectors
   uint32_t nblocks;      // output blocks
   uint32_t seg, nseg;    // segment size in vectors, segments per block
@@ -45,39 +68,39 @@ __device__ __forceinline__ uint32_t in_block(const ReshardGeom& g, uint32_t ob) 
   if (g.kind == CP_TOKEN_MAJOR) {
     if (g.dir == CP_SEQ_TO_HEAD) {
       // out [r][u][s*n+t] (block = Hl heads)  <-  in [r][s][t][u*Hl ..]
-      const uint32_t t = ob % n;
-      uint32_t x = ob / n;
-      const uint32_t s = x % U;
-      x /= U;
-      const uint32_t u = x % U;
-      const uint32_t r = x / U;
+      uint32_t x = g.fn.div(ob);
+      const uint32_t t = ob - x * n;
+      uint32_t y = g.fU.div(x);
+      const uint32_t s = x - y * U;
+      const uint32_t r = g.fU.div(y);
+      const uint32_t u = y - r * U;
       return ((r * U + s) * n + t) * U + u;  // an input row holds U blocks
     }
     // out [r][s][t][u*Hl ..] (block (r,s,t,u))  <-  in [r][u][s*n+t]
-    const uint32_t u = ob % U;
-    uint32_t x = ob / U;
-    const uint32_t t = x % n;
-    x /= n;
-    const uint32_t s = x % U;
-    const uint32_t r = x / U;
+    uint32_t x = g.fU.div(ob);
+    const uint32_t u = ob - x * U;
+    uint32_t y = g.fn.div(x);
+    const uint32_t t = x - y * n;
+    const uint32_t r = g.fU.div(y);
+    const uint32_t s = y - r * U;
     return (r * U + u) * U * n + s * n + t;
   }
   if (g.dir == CP_SEQ_TO_HEAD) {
     // out [r][u][h'][s*n .. +n]  (block (r,u,h',s))  <-  in [r][s][u*Hl+h'][0..n)
-    const uint32_t s = ob % U;
-    uint32_t x = ob / U;
-    const uint32_t hl = x % Hl;
-    x /= Hl;
-    const uint32_t u = x % U;
-    const uint32_t r = x / U;
+    uint32_t x = g.fU.div(ob);
+    const uint32_t s = ob - x * U;
+    uint32_t y = g.fHl.div(x);
+    const uint32_t hl = x - y * Hl;
+    const uint32_t r = g.fU.div(y);
+    const uint32_t u = y - r * U;
     return (r * U + s) * H + u * Hl + hl;
   }
   // out [r][s][h = u*Hl+h'][0..n)  (block (r,s,h))  <-  in [r][u][h'][s*n ..]
-  const uint32_t h = ob % H;
-  uint32_t x = ob / H;
-  const uint32_t s = x % U;
-  const uint32_t r = x / U;
-  const uint32_t u = h / Hl, hl = h % Hl;
+  uint32_t x = g.fH.div(ob);
+  const uint32_t h = ob - x * H;
+  const uint32_t r = g.fU.div(x);
+  const uint32_t s = x - r * U;
+  const uint32_t u = g.fHl.div(h), hl = h - u * Hl;
   return ((r * U + u) * Hl + hl) * U + s;
 }
 
@@ -165,19 +188,25 @@ int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int
   g.Hl = H / U;
   g.dir = direction;
   g.kind = kind;
+  g.fU = make_fastdiv(g.U);
+  g.fn = make_fastdiv(g.n);
+  g.fH = make_fastdiv(g.H);
+  g.fHl = make_fastdiv(g.Hl);
   const long long block_bytes = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(g.Hl) * row_elems * elem_bytes
                                                          : static_cast<long long>(n) * elem_bytes;
   const long long nblocks = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(R) * U * n * U
                                                      : static_cast<long long>(R) * U * H;
   if (nblocks == 0 || block_bytes == 0) return CP_OK;
-  if (nblocks >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  if (nblocks >= (1LL << 31)) return CP_ERR_UNSUPPORTED;  // the block index math is 31-bit
   g.nblocks = static_cast<uint32_t>(nblocks);
   const int threads = 256, warps_per_cta = threads / 32;
   const long long vec_bytes = (block_bytes % 16 == 0) ? 16 : 4;
   const long long blk = block_bytes / vec_bytes;
   if (block_bytes % 4 != 0) return CP_ERR_UNSUPPORTED;
   if (blk >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
-  const long long seg = std::min<long long>(blk, 4096 / vec_bytes);
+  // Segments: 4 KB of a token-major block; 512 bytes of a head-major (LSE)
+  // block, whose blocks are few and long.
+  const long long seg = std::min<long long>(blk, (kind == CP_HEAD_MAJOR ? 512 : 4096) / vec_bytes);
   const long long nseg = (blk + seg - 1) / seg;
   const long long nunits = nblocks * nseg;
   if (nunits >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
