@@ -500,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   float* sLse = reinterpret_cast<float*>(smem + SM::offLD);  // -LSE * log2(e) per query column
   float* sDel = sLse + 128;                                  // -D per query column
+  const uint32_t aLse = smem_u32(sLse), aDel = smem_u32(sDel);  // the same, as shared-window addresses
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
 
@@ -696,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
-          const float2 nl = *reinterpret_cast<const float2*>(sLse + col);
+          const float2 nl = ld_shared_f32x2(aLse + 4 * col);
           const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
                                     make_f32x2(nl.x, nl.y));
           float y0, y1;
@@ -734,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
           const uint32_t pk = pp[cc * 16 + e / 2];
-          const float2 nd = *reinterpret_cast<const float2*>(sDel + col);
+          const float2 nd = ld_shared_f32x2(aDel + 4 * col);
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(nd.x, nd.y));
           float d0, d1;
