@@ -351,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pk = pp[cc * 16 + e / 2];
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(-dlt, -dlt));
-          float d0, d1;
-          split_f32x2(dd, d0, d1);
-          dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
+          float s0, s1;
+          split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)), dd), s0, s1);
+          dsp[e / 2] = pack_bf16x2(s0, s1);
         }
         tmem_st16(tdP + lane_off + 64 * half + 16 * cc, dsp);
       }
@@ -738,9 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 nd = ld_shared_f32x2(aDel + 4 * col);
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(nd.x, nd.y));
-          float d0, d1;
-          split_f32x2(dd, d0, d1);
-          dsp[e / 2] = pack_bf16x2(__uint_as_float(pk << 16) * d0, __uint_as_float(pk & 0xffff0000u) * d1);
+          float s0, s1;
+          split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)), dd), s0, s1);
+          dsp[e / 2] = pack_bf16x2(s0, s1);
         }
         tmem_st16(tdPt + lane_off + 64 * half + 16 * cc, dsp);
       }
