@@ -89,6 +89,7 @@ def _L():
     lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
     lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.cp_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), _vp]
     lib.cp_strerror.argtypes = [_i]
     lib.cp_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -97,7 +98,7 @@ def _L():
 
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
-            "cp_merge_lse", "cp_get_status", "cp_strerror"]
+            "cp_merge_lse", "cp_get_status", "cp_strerror", "cp_selftest_wait_timeout"]
 
 
 class CPError(RuntimeError):
@@ -243,6 +244,13 @@ def cp_attn_bwd(plan: Plan, q, k, v, o, lse, dO, dq, dk, dv, workspace=None, wor
 def cp_merge_lse(n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream=None):
     _check(_L().cp_merge_lse(int(n_parts), int(rows), int(H), int(d), _ptr(o_parts), _ptr(lse_parts),
                              _ptr(o_out), _ptr(lse_out), _stream(stream)), "cp_merge_lse")
+
+
+def cp_selftest_wait_timeout(limit_us, stream=None):
+    """Run the bounded-wait self-test; returns (timed_out, left_on_abort, wait_us)."""
+    out = (ctypes.c_int32 * 3)()
+    _check(_L().cp_selftest_wait_timeout(int(limit_us), out, _stream(stream)), "cp_selftest_wait_timeout")
+    return int(out[0]), int(out[1]), int(out[2])
 
 
 def cp_get_status(stream=None) -> int:

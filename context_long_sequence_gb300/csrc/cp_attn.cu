@@ -13,6 +13,7 @@
 
 #include "cp_attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 using cpattn::AttnGeom;
 using cpattn::WorkItem;
@@ -708,6 +709,61 @@ const char* cp_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits (cp_selftest_wait_timeout).
+//
+// Two roles of one CTA, as in the attention kernels: warp 0 waits on an
+// mbarrier that nothing will ever complete; after `limit_ns` its wait gives
+// up, records CP_ERR_DEVICE_TIMEOUT and raises the CTA's abort flag.  Warp 1
+// waits (with the production 2 s limit) on a barrier that only warp 0 would
+// have completed, and must leave because of the abort flag, long before its
+// own limit.  out[0] = 1 if warp 0 timed out, out[1] = 1 if warp 1 left on
+// the abort, out[2] = warp 1's wait in microseconds.  No fault, no trap: the
+// kernel returns normally and the context stays usable.
+namespace {
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* status, int32_t* out) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    cpattn::mbar_init(cpattn::smem_u32(&bars[0]), 1);
+    cpattn::mbar_init(cpattn::smem_u32(&bars[1]), 1);
+    abort_flag = 0;
+    cpattn::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort = &abort_flag;
+  if (warp == 0 && lane == 0) {
+    const bool ok = cpattn::mbar_wait_limit(cpattn::smem_u32(&bars[0]), 0, abort, status, limit_ns);
+    out[0] = ok ? 0 : 1;
+  } else if (warp == 1 && lane == 0) {
+    const uint64_t t0 = cpattn::globaltimer_ns();
+    const bool ok = cpattn::mbar_wait(cpattn::smem_u32(&bars[1]), 0, abort, status);
+    out[1] = (!ok && *abort) ? 1 : 0;
+    out[2] = static_cast<int32_t>((cpattn::globaltimer_ns() - t0) / 1000);
+  }
+}
+}  // namespace
+
+extern "C" int cp_selftest_wait_timeout(int32_t limit_us, int32_t* out3, cudaStream_t stream) {
+  if (limit_us <= 0 || limit_us > 1000000 || !out3) return CP_ERR_INVALID_ARG;
+  int32_t* st = status_ptr();
+  if (!st) return CP_ERR_CUDA;
+  int32_t* d_out = nullptr;
+  if (cudaMalloc(&d_out, 3 * sizeof(int32_t)) != cudaSuccess) return CP_ERR_CUDA;
+  int rc = CP_OK;
+  if (cudaMemsetAsync(d_out, 0, 3 * sizeof(int32_t), stream) != cudaSuccess) rc = CP_ERR_CUDA;
+  if (rc == CP_OK) {
+    selftest_wait_kernel<<<1, 64, 0, stream>>>(static_cast<uint64_t>(limit_us) * 1000, st, d_out);
+    if (cudaGetLastError() != cudaSuccess) rc = CP_ERR_CUDA;
+  }
+  if (rc == CP_OK && (cudaMemcpyAsync(out3, d_out, 3 * sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+                      cudaStreamSynchronize(stream) != cudaSuccess))
+    rc = CP_ERR_CUDA;
+  cudaFree(d_out);
+  return rc;
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free emit-partials forward (cp_attn_fwd_noalloc).

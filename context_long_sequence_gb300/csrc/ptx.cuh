@@ -73,21 +73,26 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // recording the timeout and raising *abort) if the limit passed, or at once
 // if another role of the CTA already aborted.  abort == nullptr: a drain
 // wait that ignores other roles' aborts but still has the time limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int32_t* status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                int32_t* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort) *abort = 1;
         record_status(status, CP_ERR_DEVICE_TIMEOUT);
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          int32_t* status) {
+  return mbar_wait_limit(bar, parity, abort, status, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -236,6 +236,19 @@ int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void 
 int cp_merge_lse(int n_parts, int rows, int H, int d, const float *o_parts,
                  const float *lse_parts, void *o_out, float *lse_out, cudaStream_t stream);
 
+/* Self-test of the device-side failure detection (no counterpart in the
+ * pages: it checks this library's own bounded waits).  Launches one small
+ * kernel in which one role waits on a barrier that nothing completes: after
+ * limit_us microseconds (1 .. 1000000) it gives up, records
+ * CP_ERR_DEVICE_TIMEOUT in the status word read by cp_get_status and raises
+ * the CTA's abort flag; a second role, waiting on a barrier only the first
+ * would have completed, must leave on that flag.  out3 (host, 3 ints):
+ * [0] = 1 if the first wait timed out, [1] = 1 if the second left on the
+ * abort, [2] = the second wait's duration in microseconds.  Synchronises
+ * `stream`; the status word is left set for cp_get_status to read.  No
+ * fault or trap: the context stays usable. */
+int cp_selftest_wait_timeout(int32_t limit_us, int32_t *out3, cudaStream_t stream);
+
 /* Allocation-free variant of the emit-partials forward (no counterpart in
  * the paper: it exists for callers, not for the method).
  *
