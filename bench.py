@@ -152,7 +152,7 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "ptx.cuh", "kernels.h"):
+    for f in ("attn_fwd.cu", "ptx.cuh", "kernels.h", "debug.cuh", "tmap.h"):
         h.update(open(os.path.join(ROOT, "context_long_sequence_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -14,7 +14,10 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libcpattn.so")
+# CPATTN_DEBUG=1 in the environment selects the bounds-checked debug build
+# (libcpattn_debug.so, compiled with -DCP_DEBUG) for this process.
+DEBUG = os.environ.get("CPATTN_DEBUG", "") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libcpattn_debug.so" if DEBUG else "libcpattn.so")
 
 # Constants (mirrors include/cp_attn.h).
 CP_ATTN_PLAN_VERSION = 1
@@ -73,7 +76,7 @@ def _L():
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"libcpattn.so is not built ({LIB_PATH}); run "
+        raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
                            "`python -m context_long_sequence_gb300.build` first")
     lib = ctypes.CDLL(LIB_PATH)
     lib.cp_plan_create.argtypes = [ctypes.POINTER(cp_plan_desc_t), ctypes.POINTER(_vp)]
@@ -90,6 +93,11 @@ def _L():
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
     lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
     lib.cp_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.cp_selftest_bounds.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.cp_get_status_detail.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.cp_tile_classes.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64,
+                                    ctypes.POINTER(ctypes.c_int64), _vp]
+    lib.cp_debug_build.argtypes = []
     lib.cp_strerror.argtypes = [_i]
     lib.cp_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -98,7 +106,8 @@ def _L():
 
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
-            "cp_merge_lse", "cp_get_status", "cp_strerror", "cp_selftest_wait_timeout"]
+            "cp_merge_lse", "cp_get_status", "cp_get_status_detail", "cp_debug_build", "cp_strerror",
+            "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes"]
 
 
 class CPError(RuntimeError):
@@ -251,6 +260,37 @@ def cp_selftest_wait_timeout(limit_us, stream=None):
     out = (ctypes.c_int32 * 3)()
     _check(_L().cp_selftest_wait_timeout(int(limit_us), out, _stream(stream)), "cp_selftest_wait_timeout")
     return int(out[0]), int(out[1]), int(out[2])
+
+
+def cp_tile_classes(plan, stream=None) -> np.ndarray:
+    """The forward's tile-class table of `plan`: int32 [n][8] rows
+    {a, q0, len, step, kpos0, klen, class0, class1} (see include/cp_attn.h)."""
+    n = ctypes.c_int64()
+    _check(_L().cp_tile_classes(plan.handle, None, 0, ctypes.byref(n), _stream(stream)), "cp_tile_classes")
+    out = np.zeros((max(n.value, 1), 8), dtype=np.int32)
+    _check(_L().cp_tile_classes(plan.handle, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n.value,
+                                ctypes.byref(n), _stream(stream)), "cp_tile_classes")
+    return out[:n.value]
+
+
+def cp_selftest_bounds(block, stream=None) -> int:
+    """Run the bounds-record self-test in block `block`; returns the source
+    line the kernel recorded (read the record with cp_get_status_detail)."""
+    line = ctypes.c_int32()
+    _check(_L().cp_selftest_bounds(int(block), ctypes.byref(line), _stream(stream)), "cp_selftest_bounds")
+    return line.value
+
+
+def cp_get_status_detail(stream=None):
+    """Read and clear the device status record: (code, block, line, file id)."""
+    out = (ctypes.c_int32 * 4)()
+    _check(_L().cp_get_status_detail(_stream(stream), out), "cp_get_status_detail")
+    return tuple(int(x) for x in out)
+
+
+def cp_debug_build() -> bool:
+    """True when the loaded library is the -DCP_DEBUG build."""
+    return bool(_L().cp_debug_build())
 
 
 def cp_get_status(stream=None) -> int:

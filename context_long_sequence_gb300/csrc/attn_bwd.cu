@@ -42,6 +42,8 @@
 #include <climits>
 #include <cmath>
 
+#define CP_TU_ID ::cpattn::kTuAttnBwd
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -76,7 +78,8 @@ __device__ __forceinline__ float to_f32(float x) { return x; }
 template <int D, typename OT>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dO,
-                                                        float* __restrict__ delta, long long rows, int H, int T) {
+                                                        float* __restrict__ delta, long long rows, int H, int T,
+                                                        int32_t* status) {
   constexpr int E = D / 32;  // elements per lane
   const int lane = threadIdx.x & 31;
   const long long total = rows * H;
@@ -93,7 +96,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       const long long r = row / T, t = row - r * T;
-      delta[(r * H + h) * T + t] = acc;
+      const long long di = (r * H + h) * T + t;
+      if (CP_IN_BOUNDS(di >= 0 && di < total, status)) delta[di] = acc;
     }
   }
 }
@@ -153,11 +157,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnGeom& g = args.g;
   int32_t* status = args.status;
   const int Hq = g.Hq_loc;
+  if (!CP_IN_BOUNDS(static_cast<int>(blockIdx.x / Hq) < args.n_items_q, status)) return;
   const WorkItem it = args.items_q[blockIdx.x / Hq];
+  // A query tile lies inside its attention rank's slots.
+  if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
+                        it.q0 + it.len <= g.T, status))
+    return;
+  [[maybe_unused]] const int rows = g.R * g.U * g.T;  // rows of Q, dO, K, V, dQ
   const int h = blockIdx.x % Hq;
   const int a = it.a, r = a / g.U, u = a % g.U;  // rank a = ring rank r, Ulysses member u
   const int qpos0 = slot_pos(g, r, it.q0);
   const int qpos_last = qpos0 + it.len - 1;
+  if (!CP_IN_BOUNDS(qpos0 >= 0 && qpos_last < g.L, status)) return;
   const int lo_min = g.doc_start ? g.doc_start[qpos0] : 0;
   const int lo_max = g.doc_start ? g.doc_start[qpos_last] : 0;
   const int hkv = h / g.G;
@@ -199,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(DQ_QD_FULL), 2 * SM::kT);
       const int qrow = a * g.T + it.q0;
+      (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows, status);
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
         tma_load_2d(sDO + hh * HALF_BYTES, &tm_do, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
@@ -209,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ks = nk % kKStages, vs = nv % kVStages;
         if (!mbar_wait(bar(DQ_K_EMPTY + ks), ((nk / kKStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(DQ_K_FULL + ks), SM::kT);
+        (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < rows && hkv < g.Hkv_loc, status);
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + ks), hkv * D + hh * 64, kv_row);
         ++nk;
@@ -285,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_pos = row_valid ? qpos0 + row : -1;
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
     const size_t lrow = (static_cast<size_t>(a) * Hq + h) * g.T + it.q0 + row;
-    const float lse2 = row_valid ? args.lse[lrow] * kLog2e : INFINITY;
-    const float dlt = row_valid ? args.delta[lrow] : 0.f;
+    const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rows) * Hq, status);
+    const float lse2 = (row_valid && ld_ok) ? args.lse[lrow] * kLog2e : INFINITY;
+    const float dlt = (row_valid && ld_ok) ? args.delta[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
     int n = 0;
     bool ok = true;
@@ -369,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       float* dst = args.dq + (static_cast<size_t>(a * g.T + it.q0 + row) * Hq + h) * D;
+      const bool store_ok = !row_valid || CP_IN_BOUNDS(a * g.T + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32];
         if (n > 0) {
@@ -376,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence(v);
         }
-        if (!row_valid) continue;
+        if (!row_valid || !store_ok) continue;
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(dst + c4 * 32 + e) =
@@ -508,11 +523,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnGeom& g = args.g;
   int32_t* status = args.status;
   const int Hkv = g.Hkv_loc, Hq = g.Hq_loc;
+  if (!CP_IN_BOUNDS(static_cast<int>(blockIdx.x / Hkv) < args.n_items_kv, status)) return;
   const WorkItem it = args.items_kv[blockIdx.x / Hkv];
+  // A key tile lies inside its attention rank's slots.
+  if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
+                        it.q0 + it.len <= g.T, status))
+    return;
+  [[maybe_unused]] const int rows = g.R * g.U * g.T;  // rows of Q, dO, K, V, dK, dV
   const int jh = blockIdx.x % Hkv;
   const int a = it.a, src = a / g.U, u = a % g.U;  // key tile of rank a = ring rank src, member u
   const int kpos0 = slot_pos(g, src, it.q0);
   const int kpos_last = kpos0 + it.len - 1;
+  if (!CP_IN_BOUNDS(kpos0 >= 0 && kpos_last < g.L, status)) return;
   const int hi_max = g.doc_end ? g.doc_end[kpos_last] - 1 : g.L - 1;
   const int hi_min = g.doc_end ? g.doc_end[kpos0] - 1 : g.L - 1;
 
@@ -550,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(KV_FULL), 2 * SM::kT);
       const int krow = a * g.T + it.q0;
+      (void)CP_IN_BOUNDS(krow >= 0 && krow < rows, status);
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
@@ -561,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = (rr * g.U + u) * g.T + qslot0;
         if (!mbar_wait(bar(KV_Q_EMPTY + qs), ((nq / kQStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(KV_Q_FULL + qs), SM::kT);
+        (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows && h < Hq, status);
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_Q_FULL + qs), h * D + hh * 64, qrow);
         ++nq;
@@ -666,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pf_len = q.qlen;
       if (etid < q.qlen) {
         const size_t li = (static_cast<size_t>(q.rr * g.U + u) * Hq + q.h) * g.T + q.qslot0 + etid;
+        if (!CP_IN_BOUNDS(li < static_cast<size_t>(rows) * Hq, status)) return;
         pf_lse = args.lse[li];
         pf_del = args.delta[li];
       }
@@ -772,6 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       const size_t orow = (static_cast<size_t>(a * g.T + it.q0 + row) * Hkv + jh) * D;
+      const bool store_ok = !key_valid || CP_IN_BOUNDS(a * g.T + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32], k[32];
         if (n > 0) {
@@ -781,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence(v);
           reg_fence(k);
         }
-        if (!key_valid) continue;
+        if (!key_valid || !store_ok) continue;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           float4 fv = make_float4(0.f, 0.f, 0.f, 0.f), fk = fv;
@@ -834,11 +860,11 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     if (grid > 0 && a.o_fp32)
       bwd_delta_kernel<D, float><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
           static_cast<const float*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
-          static_cast<long long>(rows), g.Hq_loc, g.T);
+          static_cast<long long>(rows), g.Hq_loc, g.T, a.status);
     else if (grid > 0)
       bwd_delta_kernel<D, __nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
-          static_cast<long long>(rows), g.Hq_loc, g.T);
+          static_cast<long long>(rows), g.Hq_loc, g.T, a.status);
   }
   const long long grid_kv = static_cast<long long>(a.n_items_kv) * g.Hkv_loc;
   const long long grid_q = static_cast<long long>(a.n_items_q) * g.Hq_loc;

@@ -48,6 +48,8 @@
 
 #include <cmath>
 
+#define CP_TU_ID ::cpattn::kTuAttnFwd
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -130,6 +132,25 @@ struct QWin {
   }
 };
 
+// Window of query tile t (0 or 1) of work item `it` of ring rank r; the
+// block's positions are contiguous.
+__device__ __forceinline__ QWin make_qwin(const AttnGeom& g, const WorkItem& it, int r, int t, int32_t* status) {
+  QWin w;
+  w.len = max(0, min(BM, it.len - t * BM));
+  w.qp0 = slot_pos(g, r, it.q0) + t * BM;
+  w.qp_last = w.qp0 + w.len - 1;
+  if (w.len > 0 && !CP_IN_BOUNDS(w.qp0 >= 0 && w.qp_last < g.L, status)) w.len = 0;
+  w.lo_min = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp0] : 0;
+  w.lo_max = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp_last] : 0;
+  return w;
+}
+
+// Class of a key tile for one query tile: 0 = not seen (no MMA, no softmax
+// pass), 1 = seen through the mask, 2 = wholly visible (the mask is skipped).
+__device__ __forceinline__ int tile_class(const QWin& w, int kpos0, int klen) {
+  return w.sees(kpos0, klen) ? (w.full(kpos0, klen) ? 2 : 1) : 0;
+}
+
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
 
 template <int D>
@@ -154,23 +175,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* status = args.status;
   const int item_idx = blockIdx.x / g.Hq_loc;
   const int h = blockIdx.x % g.Hq_loc;
+  if (!CP_IN_BOUNDS(item_idx < args.n_items, status)) return;
   const WorkItem it = args.items[item_idx];
+  // A work item lies inside its attention rank's slots.
+  if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= 2 * BM &&
+                        it.q0 + it.len <= g.T && it.step < g.R, status))
+    return;
+  [[maybe_unused]] const int q_rows = g.R * g.U * g.T;              // rows of Q (and of ring-mode K/V)
+  [[maybe_unused]] const int kv_rows = g.kv_global ? g.L : q_rows;  // rows of K/V
   const int a = it.a, r = a / g.U, u = a % g.U;
   const int s_begin = it.step < 0 ? 0 : it.step;
   const int s_end = it.step < 0 ? g.R : it.step + 1;
   const int hkv = h / g.G;
 
-  // The two query tiles' windows (positions are contiguous within the block).
-  auto make_win = [&](int t) {
-    QWin w;
-    w.len = max(0, min(BM, it.len - t * BM));
-    w.qp0 = slot_pos(g, r, it.q0) + t * BM;
-    w.qp_last = w.qp0 + w.len - 1;
-    w.lo_min = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp0] : 0;
-    w.lo_max = (w.len > 0 && g.doc_start) ? g.doc_start[w.qp_last] : 0;
-    return w;
-  };
-  const QWin win0 = make_win(0), win1 = make_win(1);
+  // The two query tiles' windows; the block walks the keys in [lo_min of
+  // tile 0, last position of the block].
+  const QWin win0 = make_qwin(g, it, r, 0, status), win1 = make_qwin(g, it, r, 1, status);
   const int blk_lo_min = win0.lo_min;
   const int blk_qp_last = win0.qp0 + it.len - 1;
 
@@ -210,14 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(BAR_Q), 2 * SM::kQ);
       const int qrow = a * g.T + it.q0;
-      for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < 2; ++t) {
+        (void)CP_IN_BOUNDS(t * BM >= it.len || (qrow + t * BM >= 0 && qrow + t * BM < q_rows), status);
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
+      }
       int n = 0;  // loads issued
       auto load = [&](const CUtensorMap* map, int kv_row) -> bool {
         const int sl = slot_of(n);
         if (!mbar_wait(bar(BAR_KV_EMPTY + sl), parity_of(n) ^ 1, abort_flag, status)) return false;
         mbar_arrive_expect_tx(bar(BAR_KV_FULL + sl), SM::kKV);
+        (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < kv_rows && hkv < g.Hkv_loc, status);
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sKV + sl * SM::kKV + hh * HALF_BYTES, map, bar(BAR_KV_FULL + sl), hkv * D + hh * 64, kv_row);
         ++n;
@@ -428,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence(ov);
         }
         if (!row_valid) continue;
+        if (!CP_IN_BOUNDS(q_slot < g.T && (!partial || r * g.R + s_begin < g.R * g.R), status)) continue;
         float o[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = (k > 0) ? __uint_as_float(ov[e]) * inv_l : 0.f;
@@ -450,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
         }
       }
-      if (row_valid) {
+      if (row_valid && CP_IN_BOUNDS(q_slot < g.T, status)) {
         if (partial)
           args.lse_part[(static_cast<size_t>(r * g.R + s_begin) * g.Hq_loc + h) * g.T + q_slot] = lse;
         else
@@ -490,7 +514,46 @@ int launch_d(const FwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
+// Debug table of the tile classes (cp_tile_classes): one thread per work
+// item walks the item's key tiles exactly as attn_fwd_kernel does and writes,
+// per walked tile, {a, q0, len, step, kpos0, klen, class of query tile 0,
+// class of query tile 1} (tile_class above).  At most `stride` rows per
+// item; counts[i] = the number of tiles item i walks.
+__global__ void tile_class_kernel(const FwdArgs args, int32_t* rows, int32_t* counts, int stride) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= args.n_items) return;
+  const AttnGeom& g = args.g;
+  const WorkItem it = args.items[i];
+  const int r = it.a / g.U, u = it.a % g.U;
+  const int s_begin = it.step < 0 ? 0 : it.step;
+  const int s_end = it.step < 0 ? g.R : it.step + 1;
+  const QWin win0 = make_qwin(g, it, r, 0, args.status), win1 = make_qwin(g, it, r, 1, args.status);
+  int32_t* out = rows + static_cast<size_t>(i) * stride * 8;
+  int n = 0;
+  for_each_kv_tile(g, r, u, s_begin, s_end, win0.lo_min, win0.qp0 + it.len - 1, [&](int, int kpos0, int klen) {
+    if (n < stride) {
+      int32_t* o = out + static_cast<size_t>(n) * 8;
+      o[0] = it.a;
+      o[1] = it.q0;
+      o[2] = it.len;
+      o[3] = it.step;
+      o[4] = kpos0;
+      o[5] = klen;
+      o[6] = tile_class(win0, kpos0, klen);
+      o[7] = tile_class(win1, kpos0, klen);
+    }
+    ++n;
+  });
+  counts[i] = n;
+}
+
 }  // namespace
+
+int launch_tile_classes(const FwdArgs& a, int32_t* rows, int32_t* counts, int stride, cudaStream_t stream) {
+  if (a.n_items <= 0) return CP_OK;
+  tile_class_kernel<<<(a.n_items + 127) / 128, 128, 0, stream>>>(a, rows, counts, stride);
+  return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (a.d == 128) return launch_d<128>(a, stream);

@@ -3,6 +3,7 @@
 // each entry point.  Host code only; the kernels live in attn_fwd.cu,
 // attn_bwd.cu, reshard.cu and merge.cu.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -11,15 +12,31 @@
 #include <new>
 #include <vector>
 
+#define CP_TU_ID ::cpattn::kTuCpAttn
 #include "cp_attn.h"
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
 using cpattn::AttnGeom;
 using cpattn::WorkItem;
 
-// Device status word: first device-side error since the last cp_get_status().
-__device__ int32_t g_cp_status;
+// Device status words: [0] the first device-side error code since the last
+// cp_get_status(); for a bounds record of a debug build [1] the block, [2]
+// the source line and [3] the file id of the failed check.
+__device__ int32_t g_cp_status[4];
+
+namespace {
+// NVTX range around one phase of an entry point, for timeline tools and for
+// `ncu --nvtx` filters.  Host-side: it brackets the asynchronous launches of
+// the phase, not their execution.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
 
 struct cp_plan {
   cp_plan_desc_t desc;
@@ -490,8 +507,9 @@ int ulysses_reshard(const cp_plan_t* p, int direction, int tensor_kind, int H, i
   const char* b = static_cast<const char*>(out);
   const size_t bytes = static_cast<size_t>(p->desc.L) * H * row_elems * elem_bytes;
   if (a < b + bytes && b < a + bytes) return CP_ERR_INVALID_ARG;
+  NvtxRange range("ulysses_reshard");
   return cpattn::launch_reshard(p->desc.ring_degree, U, p->n, H, row_elems, direction, tensor_kind, elem_bytes, in,
-                                out, stream);
+                                out, stream, status_ptr());
 }
 
 int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -506,6 +524,7 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   if (w.total > 0 && (!workspace || workspace_bytes < w.total)) return CP_ERR_WORKSPACE;
   const cp_plan_desc_t& d = p->desc;
   char* ws = static_cast<char*>(workspace);
+  NvtxRange call("cp_attn_fwd");
   cpattn::FwdArgs a{};
   a.g = geom(p);
   a.d = d.d;
@@ -523,23 +542,28 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
       a.lse_part = reinterpret_cast<float*>(ws + w.lsepart);
       a.items = p->d_items_steps;
       a.n_items = p->n_items_steps;
-      rc = cpattn::launch_attn_fwd(a, stream);
-      if (rc != CP_OK) return rc;
+      {
+        NvtxRange phase("attention_partials");
+        if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
+      }
+      NvtxRange phase("merge");
       return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse,
-                                  d.out_fp32, stream);
+                                  d.out_fp32, stream, a.status);
     }
     if (d.kv_exchange == CP_KV_ALLGATHER) {
       // All-gather: K and V of every rank to their positions, then each
       // rank's queries attend over the gathered sequence.
       const long long row_bytes = static_cast<long long>(d.Hkv) * d.d * 2;
-      if ((rc = cpattn::launch_gather_rows(a.g, row_bytes, k, ws + w.kall, stream)) ||
-          (rc = cpattn::launch_gather_rows(a.g, row_bytes, v, ws + w.vall, stream)))
+      NvtxRange phase("gather_kv");
+      if ((rc = cpattn::launch_gather_rows(a.g, row_bytes, k, ws + w.kall, stream, a.status)) ||
+          (rc = cpattn::launch_gather_rows(a.g, row_bytes, v, ws + w.vall, stream, a.status)))
         return rc;
       a.k = ws + w.kall;
       a.v = ws + w.vall;
     }
     a.items = p->d_items_fused;
     a.n_items = p->n_items_fused;
+    NvtxRange phase("attention");
     return cpattn::launch_attn_fwd(a, stream);
   }
   // Ulysses / USP: reshard in, ring attention per head group, reshard out.
@@ -549,9 +573,17 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   void* vh = ws + w.vh;
   void* oh = ws + w.oh;
   float* lseh = reinterpret_cast<float*>(ws + w.lseh);
-  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh, stream))) return rc;
-  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh, stream))) return rc;
-  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh, stream))) return rc;
+  // One Ulysses exchange of every ring group: H heads of row_elems elements.
+  auto reshard = [&](int H, int row_elems, int dir, int kind, int elem_bytes, const void* in, void* out) {
+    return cpattn::launch_reshard(R, U, p->n, H, row_elems, dir, kind, elem_bytes, in, out, stream, a.status);
+  };
+  {
+    NvtxRange phase("reshard_in");
+    if ((rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh)) ||
+        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh)) ||
+        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh)))
+      return rc;
+  }
   a.q = qh;
   a.k = kh;
   a.v = vh;
@@ -559,11 +591,13 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.lse = lseh;
   a.items = p->d_items_fused;
   a.n_items = p->n_items_fused;
-  if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
-  if ((rc = cpattn::launch_reshard(R, U, p->n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o,
-                                   stream)))
-    return rc;
-  return cpattn::launch_reshard(R, U, p->n, d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse, stream);
+  {
+    NvtxRange phase("attention");
+    if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
+  }
+  NvtxRange phase("reshard_out");
+  if ((rc = reshard(d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o))) return rc;
+  return reshard(d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse);
 }
 
 int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -585,6 +619,7 @@ int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const vo
   a.lse = lse;
   a.items = p->d_items_fused;
   a.n_items = p->n_items_fused;
+  NvtxRange call("cp_attn_fwd_local");
   return cpattn::launch_attn_fwd(a, stream);
 }
 
@@ -608,6 +643,7 @@ int cp_attn_fwd_rank(const cp_plan_t* p, int rank, const void* q, const void* k,
   a.lse = lse;
   a.items = p->d_items_rank + p->rank_item_off[rank];
   a.n_items = p->rank_item_off[rank + 1] - p->rank_item_off[rank];
+  NvtxRange call("cp_attn_fwd_rank");
   return cpattn::launch_attn_fwd(a, stream);
 }
 
@@ -645,19 +681,29 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;
   const cp_plan_desc_t& d = p->desc;
-  if (d.ulysses_degree == 1) return cpattn::launch_attn_bwd(a, stream);
+  NvtxRange call("cp_attn_bwd");
+  if (d.ulysses_degree == 1) {
+    NvtxRange phase("attention_bwd");
+    return cpattn::launch_attn_bwd(a, stream);
+  }
   // Ulysses / USP: the forward's exchanges run in reverse for the gradients.
   // Inputs (q, k, v, o, dO, LSE) go to the head-sharded layout, the ring
   // backward runs per head group, and dQ, dK, dV come back token-sharded.
   const int R = d.ring_degree, U = d.ulysses_degree, n = p->n;
   const int ob = d.out_fp32 ? 4 : 2;
-  if ((rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh, stream)))
-    return rc;
+  auto reshard = [&](int H, int row_elems, int dir, int kind, int elem_bytes, const void* in, void* out) {
+    return cpattn::launch_reshard(R, U, n, H, row_elems, dir, kind, elem_bytes, in, out, stream, a.status);
+  };
+  {
+    NvtxRange phase("reshard_in");
+    if ((rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh)) ||
+        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh)) ||
+        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh)) ||
+        (rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh)) ||
+        (rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh)) ||
+        (rc = reshard(d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh)))
+      return rc;
+  }
   a.q = ws + w.qh;
   a.k = ws + w.kh;
   a.v = ws + w.vh;
@@ -667,11 +713,73 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.dq = reinterpret_cast<float*>(ws + w.dqh);
   a.dk = reinterpret_cast<float*>(ws + w.dkh);
   a.dv = reinterpret_cast<float*>(ws + w.dvh);
-  if ((rc = cpattn::launch_attn_bwd(a, stream))) return rc;
-  if ((rc = cpattn::launch_reshard(R, U, n, d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq, stream)) ||
-      (rc = cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk, stream)))
+  {
+    NvtxRange phase("attention_bwd");
+    if ((rc = cpattn::launch_attn_bwd(a, stream))) return rc;
+  }
+  NvtxRange phase("reshard_out");
+  if ((rc = reshard(d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq)) ||
+      (rc = reshard(d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk)))
     return rc;
-  return cpattn::launch_reshard(R, U, n, d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv, stream);
+  return reshard(d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv);
+}
+
+int cp_tile_classes(const cp_plan_t* p, int32_t* host_rows, int64_t capacity, int64_t* n_rows, cudaStream_t stream) {
+  if (!p || !n_rows || capacity < 0 || (capacity > 0 && !host_rows)) return CP_ERR_INVALID_ARG;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const cp_plan_desc_t& d = p->desc;
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = d.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  const bool steps = d.emit_partials && d.ulysses_degree == 1;
+  a.items = steps ? p->d_items_steps : p->d_items_fused;
+  a.n_items = steps ? p->n_items_steps : p->n_items_fused;
+  // Upper bound on the tiles one item walks: every chunk of every ring step
+  // it covers, plus one for a chunk-unaligned start (position order when the
+  // K/V are all-gathered).
+  const long long per_chunk = (p->chunk + kTile - 1) / kTile + 1;
+  const long long stride = a.g.kv_global ? (d.L + kTile - 1) / kTile + 1
+                                         : static_cast<long long>(steps ? 1 : d.ring_degree) * p->nchunks * per_chunk;
+  const long long cells = static_cast<long long>(a.n_items) * stride * 8;
+  if (stride > 0x7fffffffLL || cells * 4 > (1LL << 30)) return CP_ERR_UNSUPPORTED;  // a debug call: 1 GiB at most
+  *n_rows = 0;
+  if (a.n_items == 0) return CP_OK;
+  int32_t* d_rows = nullptr;
+  int32_t* d_counts = nullptr;
+  if (cudaMalloc(&d_rows, cells * 4) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMalloc(&d_counts, static_cast<size_t>(a.n_items) * 4) != cudaSuccess) {
+    cudaFree(d_rows);
+    return CP_ERR_CUDA;
+  }
+  std::vector<int32_t> counts(a.n_items), rows;
+  rc = cpattn::launch_tile_classes(a, d_rows, d_counts, static_cast<int>(stride), stream);
+  if (rc == CP_OK &&
+      (cudaMemcpyAsync(counts.data(), d_counts, counts.size() * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+       cudaStreamSynchronize(stream) != cudaSuccess))
+    rc = CP_ERR_CUDA;
+  long long total = 0;
+  for (int i = 0; rc == CP_OK && i < a.n_items; ++i) {
+    if (counts[i] > stride) rc = CP_ERR_UNSUPPORTED;  // the bound above is wrong: report, never truncate
+    total += counts[i];
+  }
+  if (rc == CP_OK && host_rows && capacity >= total) {
+    rows.resize(static_cast<size_t>(cells));
+    if (cudaMemcpy(rows.data(), d_rows, cells * 4, cudaMemcpyDeviceToHost) != cudaSuccess) rc = CP_ERR_CUDA;
+    long long o = 0;
+    for (int i = 0; rc == CP_OK && i < a.n_items; ++i) {
+      std::memcpy(host_rows + o * 8, rows.data() + static_cast<size_t>(i) * stride * 8,
+                  static_cast<size_t>(counts[i]) * 8 * 4);
+      o += counts[i];
+    }
+  }
+  cudaFree(d_rows);
+  cudaFree(d_counts);
+  if (rc != CP_OK) return rc;
+  *n_rows = total;
+  return (host_rows && capacity < total) ? CP_ERR_WORKSPACE : CP_OK;
 }
 
 int cp_merge_lse(int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts, void* o_out,
@@ -680,17 +788,36 @@ int cp_merge_lse(int n_parts, int rows, int H, int d, const float* o_parts, cons
   if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
   if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o_out) || !aligned16(lse_out))
     return CP_ERR_ALIGNMENT;
-  return cpattn::launch_merge(1, n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, 0, stream);
+  NvtxRange call("cp_merge_lse");
+  return cpattn::launch_merge(1, n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, 0, stream, status_ptr());
+}
+
+int cp_get_status_detail(cudaStream_t stream, int32_t* out4) {
+  if (!out4) return CP_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
+  int32_t rec[4] = {0, 0, 0, 0};
+  const int32_t zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(rec, g_cp_status, sizeof(rec)) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_cp_status, zero, sizeof(zero)) != cudaSuccess) return CP_ERR_CUDA;
+  std::memcpy(out4, rec, sizeof(rec));
+  return CP_OK;
 }
 
 int cp_get_status(cudaStream_t stream, int32_t* dev_code) {
   if (!dev_code) return CP_ERR_INVALID_ARG;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
-  int32_t code = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&code, g_cp_status, sizeof(code)) != cudaSuccess) return CP_ERR_CUDA;
-  if (cudaMemcpyToSymbol(g_cp_status, &zero, sizeof(zero)) != cudaSuccess) return CP_ERR_CUDA;
-  *dev_code = code;
+  int32_t rec[4];
+  const int rc = cp_get_status_detail(stream, rec);
+  if (rc != CP_OK) return rc;
+  *dev_code = rec[0];
   return CP_OK;
+}
+
+int cp_debug_build(void) {
+#ifdef CP_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 const char* cp_strerror(int code) {
@@ -766,6 +893,42 @@ extern "C" int cp_selftest_wait_timeout(int32_t limit_us, int32_t* out3, cudaStr
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounds record (cp_selftest_bounds).
+//
+// Block `block` of a small grid checks the index one past the end of a
+// 32-element buffer with the same record routine the CP_DEBUG checks use;
+// the check fails, the record is written and the store is skipped.  Nothing
+// outside the buffer is touched.  The kernel also stores the source line it
+// recorded in buf[0], so the host can compare it with the record.
+namespace {
+__global__ void selftest_bounds_kernel(int32_t* status, int32_t* buf, int block) {
+  if (static_cast<int>(blockIdx.x) != block || threadIdx.x != 0) return;
+  const int n = 32, idx = n;  // one past the end
+  const bool in = idx < n;
+  const int line = __LINE__;
+  if (!in) cpattn::debug_bounds_fail(status, line, cpattn::kTuCpAttn);
+  if (in) buf[idx] = 1;
+  buf[0] = line;
+}
+}  // namespace
+
+extern "C" int cp_selftest_bounds(int32_t block, int32_t* line, cudaStream_t stream) {
+  if (block < 0 || block >= 64 || !line) return CP_ERR_INVALID_ARG;
+  int32_t* st = status_ptr();
+  if (!st) return CP_ERR_CUDA;
+  int32_t* d_buf = nullptr;
+  if (cudaMalloc(&d_buf, 32 * sizeof(int32_t)) != cudaSuccess) return CP_ERR_CUDA;
+  int rc = CP_OK;
+  selftest_bounds_kernel<<<64, 32, 0, stream>>>(st, d_buf, block);
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemcpyAsync(line, d_buf, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    rc = CP_ERR_CUDA;
+  cudaFree(d_buf);
+  return rc;
+}
+
+// ---------------------------------------------------------------------------
 // Allocation-free emit-partials forward (cp_attn_fwd_noalloc).
 //
 // For callers that cannot allocate device memory (see the header): the
@@ -829,5 +992,5 @@ extern "C" int cp_attn_fwd_noalloc(const cp_plan_t* p, const void* q, const void
   rc = cpattn::launch_attn_fwd(a, stream);
   if (rc != CP_OK) return rc;
   return cpattn::launch_merge(d.ring_degree, d.ring_degree, p->T, d.Hq, d.d, a.o_part, a.lse_part, o, lse,
-                              d.out_fp32, stream);
+                              d.out_fp32, stream, a.status);
 }

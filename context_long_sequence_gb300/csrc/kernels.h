@@ -58,6 +58,11 @@ struct FwdArgs {
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// Debug table of the forward's tile classes for the work items of `a`:
+// rows [n_items][stride][8] {a, q0, len, step, kpos0, klen, class0, class1},
+// counts [n_items] (tiles walked per item; rows beyond `stride` are dropped).
+int launch_tile_classes(const FwdArgs& a, int32_t* rows, int32_t* counts, int stride, cudaStream_t stream);
+
 // Backward on the head-sharded layout of cp_attn_fwd_local (rank a = r*U+u;
 // with U == 1 that is the sequence-sharded layout).  items_q: 128-row query
 // tiles (all ring steps); items_kv: key tiles {a = owner rank, q0 = first
@@ -81,14 +86,17 @@ int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // All-gather of K or V in the emulation: out[slot_pos(r, t)] = in[r*T + t],
 // rows of row_bytes (a multiple of 16).
-int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream);
+int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream,
+                       int32_t* status);
 
-// Block-permutation copy behind ulysses_reshard.
+// Block-permutation copy behind ulysses_reshard.  `status` (the device
+// status words) receives the bounds records of debug builds.
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind,
-                   int elem_bytes, const void* in, void* out, cudaStream_t stream);
+                   int elem_bytes, const void* in, void* out, cudaStream_t stream, int32_t* status);
 
 // Merge of `n_parts` partials, `batch` independent groups laid out back to back.
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts,
-                 const float* lse_parts, void* o_out, float* lse_out, int out_fp32, cudaStream_t stream);
+                 const float* lse_parts, void* o_out, float* lse_out, int out_fp32, cudaStream_t stream,
+                 int32_t* status);
 
 }  // namespace cpattn

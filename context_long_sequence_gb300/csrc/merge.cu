@@ -25,7 +25,9 @@
 #include <cmath>
 #include <cstdint>
 
+#define CP_TU_ID ::cpattn::kTuMerge
 #include "cp_attn.h"
+#include "debug.cuh"
 #include "kernels.h"
 
 namespace cpattn {
@@ -44,7 +46,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H, const float* __restrict__ o_parts,
                                                     const float* __restrict__ lse_parts, void* __restrict__ o_out,
-                                                    float* __restrict__ lse_out, int batch, int out_fp32) {
+                                                    float* __restrict__ lse_out, int batch, int out_fp32,
+                                                    int32_t* status) {
   constexpr int TPR = D / 4;         // lanes per row (one float4 each)
   constexpr int RPI = 32 / TPR;      // rows per warp iteration
   extern __shared__ float s_w[];     // [warps][n_parts][kRows] weights
@@ -62,6 +65,7 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H
     const int b = static_cast<int>(x / row_blocks);
     const int row0 = rb * kRows;
     const int nrow = min(kRows, rows - row0);
+    if (!CP_IN_BOUNDS(b < batch && h < H && row0 < rows, status)) continue;
     // 1. merged LSE and per-part weights of row row0 + lane.
     {
       const int row = row0 + lane;
@@ -106,6 +110,7 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H
           }
         }
         const long long oi = static_cast<long long>(b) * per_batch * D + off;
+        if (!CP_IN_BOUNDS(oi + 4 <= static_cast<long long>(batch) * per_batch * D, status)) continue;
         if (out_fp32)
           *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc;
         else
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H
 }  // namespace
 
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts, const float* lse_parts,
-                 void* o_out, float* lse_out, int out_fp32, cudaStream_t stream) {
+                 void* o_out, float* lse_out, int out_fp32, cudaStream_t stream, int32_t* status) {
   if (static_cast<long long>(batch) * rows * H == 0) return CP_OK;
   if (n_parts <= 0) return CP_ERR_INVALID_ARG;
   // Shared memory: n_parts * 32 weights per warp; fewer warps per CTA when
@@ -142,13 +147,13 @@ int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_
         cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return CP_ERR_CUDA;
     merge_kernel<128><<<static_cast<int>(grid), threads, smem, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
-                                                                        lse_out, batch, out_fp32);
+                                                                        lse_out, batch, out_fp32, status);
   } else if (d == 64) {
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return CP_ERR_CUDA;
     merge_kernel<64><<<static_cast<int>(grid), threads, smem, stream>>>(n_parts, rows, H, o_parts, lse_parts, o_out,
-                                                                       lse_out, batch, out_fp32);
+                                                                       lse_out, batch, out_fp32, status);
   } else {
     return CP_ERR_UNSUPPORTED;
   }

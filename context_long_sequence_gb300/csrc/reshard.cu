@@ -24,7 +24,9 @@
 #include <algorithm>
 #include <cstdint>
 
+#define CP_TU_ID ::cpattn::kTuReshard
 #include "cp_attn.h"
+#include "debug.cuh"
 #include "kernels.h"
 
 namespace cpattn {
@@ -60,6 +62,7 @@ struct ReshardGeom {
   uint32_t seg, nseg;    // segment size in vectors, segments per block
   uint32_t nunits;       // nblocks * nseg
   int dir, kind;
+  int32_t* status;       // device status words (bounds records of debug builds)
 };
 
 // Source block index of output block `ob`.
@@ -122,8 +125,10 @@ __global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, 
       if (un < g.nunits) {
         const uint32_t ob = un / g.nseg;
         const uint32_t v0 = (un - ob * g.nseg) * g.seg;
+        const uint32_t ib = in_block(g, ob);
+        if (!CP_IN_BOUNDS(ib < g.nblocks && ob < g.nblocks && v0 < g.blk, g.status)) continue;
         len[i] = min(g.seg, g.blk - v0);
-        src[i] = static_cast<uint64_t>(in_block(g, ob)) * g.blk + v0;
+        src[i] = static_cast<uint64_t>(ib) * g.blk + v0;
         dst[i] = static_cast<uint64_t>(ob) * g.blk + v0;
       }
     }
@@ -141,14 +146,16 @@ __global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, 
 
 // All-gather in the emulation: each warp moves one slot row to its position.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                                          AttnGeom g, uint32_t vecs) {
+                                                          AttnGeom g, uint32_t vecs, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   const uint32_t rows = static_cast<uint32_t>(g.R) * g.T;
   for (uint32_t slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; slot < rows; slot += warps) {
     const int r = static_cast<int>(slot / g.T), t = static_cast<int>(slot % g.T);
+    const int pos = slot_pos(g, r, t);
+    if (!CP_IN_BOUNDS(pos >= 0 && pos < g.L, status)) continue;
     const uint64_t src = static_cast<uint64_t>(slot) * vecs;
-    const uint64_t dst = static_cast<uint64_t>(slot_pos(g, r, t)) * vecs;
+    const uint64_t dst = static_cast<uint64_t>(pos) * vecs;
     for (uint32_t v = lane; v < vecs; v += 32) out[dst + v] = __ldg(in + src + v);
   }
 }
@@ -165,7 +172,8 @@ int sm_count() {
 
 }  // namespace
 
-int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream) {
+int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, void* out, cudaStream_t stream,
+                       int32_t* status) {
   if (g.U != 1 || row_bytes <= 0 || row_bytes % 16 || row_bytes / 16 >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(g.R) * g.T;
   if (rows == 0) return CP_OK;
@@ -175,13 +183,14 @@ int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, v
   if (grid > cap) grid = cap;
   gather_rows_kernel<<<static_cast<int>(grid), threads, 0, stream>>>(static_cast<const uint4*>(in),
                                                                      static_cast<uint4*>(out), g,
-                                                                     static_cast<uint32_t>(row_bytes / 16));
+                                                                     static_cast<uint32_t>(row_bytes / 16), status);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind, int elem_bytes,
-                   const void* in, void* out, cudaStream_t stream) {
+                   const void* in, void* out, cudaStream_t stream, int32_t* status) {
   ReshardGeom g;
+  g.status = status;
   g.U = U;
   g.n = n;
   g.H = H;

@@ -36,8 +36,9 @@
  *    caller's buffer.  Calls are asynchronous on `stream` and return 0 on
  *    success or a negative CP_ERR_* code; on an error return nothing was
  *    enqueued.  Errors found on the device while a kernel runs (a bounded
- *    wait that ran out, an index out of range) are recorded in a device
- *    status word read by cp_get_status().
+ *    wait that ran out; in debug builds, an index out of range) are recorded
+ *    in device status words read by cp_get_status() and
+ *    cp_get_status_detail().
  *  - bf16 = bfloat16 (round-to-nearest-even on every conversion).
  *  - Token-major tensors are [tokens][heads][d] row-major.  "Sequence-sharded"
  *    tensors hold the P = U*R ranks' shards back to back, rank-major, rank
@@ -236,6 +237,27 @@ int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void 
 int cp_merge_lse(int n_parts, int rows, int H, int d, const float *o_parts,
                  const float *lse_parts, void *o_out, float *lse_out, cudaStream_t stream);
 
+/* Debug table of the forward's tile classes (no counterpart in the pages: it
+ * exposes which work the kernel skips).  For every work item of the plan's
+ * forward -- a block of up to 256 query slots of one attention rank inside
+ * one contiguous-position chunk, split into query tiles 0 and 1 of up to 128
+ * rows -- the K/V tiles the kernel walks, in its order (ring steps s = 0..R-1,
+ * source rank (r - s) mod R, that rank's chunks in slot order, 128-slot tiles
+ * from each chunk's start; with the all-gather exchange, 128-position tiles
+ * in position order; with emit_partials, one item per ring step), as rows of
+ * 8 int32 {a, q0, len, step, kpos0, klen, class0, class1}: attention rank a,
+ * first query slot q0, length len and ring step (-1: all steps) of the item,
+ * first key position and length of the tile, and per query tile: 0 = not
+ * seen (no MMA, no softmax pass), 1 = seen and masked, 2 = wholly visible
+ * (mask skipped).  Items appear in the plan's launch order.  host_rows (host,
+ * capacity rows of 8) may be null with
+ * capacity 0 to ask for the count.  *n_rows = rows in the table.  Returns
+ * CP_ERR_WORKSPACE if capacity is too small, CP_ERR_UNSUPPORTED if the table
+ * would need more than 1 GiB of device scratch.  Synchronous: allocates and
+ * frees device scratch, synchronises `stream`. */
+int cp_tile_classes(const cp_plan_t *plan, int32_t *host_rows, int64_t capacity, int64_t *n_rows,
+                    cudaStream_t stream);
+
 /* Self-test of the device-side failure detection (no counterpart in the
  * pages: it checks this library's own bounded waits).  Launches one small
  * kernel in which one role waits on a barrier that nothing completes: after
@@ -248,6 +270,17 @@ int cp_merge_lse(int n_parts, int rows, int H, int d, const float *o_parts,
  * `stream`; the status word is left set for cp_get_status to read.  No
  * fault or trap: the context stays usable. */
 int cp_selftest_wait_timeout(int32_t limit_us, int32_t *out3, cudaStream_t stream);
+
+/* Self-test of the bounds record (no counterpart in the pages).  Launches
+ * a 64-block kernel in which block `block` (0 .. 63) checks an index one
+ * past the end of a small device buffer with the record routine of the
+ * CP_DEBUG checks: the check fails, {CP_ERR_DEVICE_BOUNDS, block, line,
+ * file id 1} is recorded in the status words (unless an earlier error is
+ * already held there) and the store is skipped, so nothing outside the
+ * buffer is touched.  *line (host) receives the source line the kernel
+ * recorded.  Works in release and debug builds alike; synchronises
+ * `stream`; the record is left for cp_get_status_detail to read. */
+int cp_selftest_bounds(int32_t block, int32_t *line, cudaStream_t stream);
 
 /* Allocation-free variant of the emit-partials forward (no counterpart in
  * the paper: it exists for callers, not for the method).
@@ -282,6 +315,22 @@ int cp_attn_fwd_noalloc(const cp_plan_t *plan, const void *q, const void *k, con
  * *dev_code = 0 or the first CP_ERR_DEVICE_* code any kernel recorded since
  * the last call.  Returns CP_OK or CP_ERR_CUDA. */
 int cp_get_status(cudaStream_t stream, int32_t *dev_code);
+
+/* As cp_get_status, with the whole record: out4 (host, 4 ints) = {code,
+ * block, source line, file id}.  The last three are set only for
+ * CP_ERR_DEVICE_BOUNDS, which only debug builds record (file ids: 1 the C-ABI
+ * layer, 2 the forward kernel, 3 the backward kernels, 4 reshard and
+ * gather, 5 merge); otherwise 0.  Reads and clears all four words.
+ *
+ * Debug builds (compiled with -DCP_DEBUG, the library libcpattn_debug.so)
+ * check every work item, global index and TMA coordinate of the kernels;
+ * a failed check records CP_ERR_DEVICE_BOUNDS here and skips the access
+ * (a TMA load is still issued: the hardware fills out-of-range rows with
+ * zeros).  Release builds contain no checks. */
+int cp_get_status_detail(cudaStream_t stream, int32_t *out4);
+
+/* 1 if this library was built with -DCP_DEBUG, else 0. */
+int cp_debug_build(void);
 
 /* Static string for a return code. */
 const char *cp_strerror(int code);

@@ -40,6 +40,32 @@ def test_header_symbols_exported(cpa):
         getattr(cpa._L(), n)
 
 
+def test_debug_library_exports_and_flag(cpa):
+    """The -DCP_DEBUG variant exports the same symbols and says it is the
+    debug build; the release library says it is not (host-only calls)."""
+    import ctypes
+    dbg = os.path.join(ROOT, "context_long_sequence_gb300", "libcpattn_debug.so")
+    if not os.path.exists(dbg):
+        from context_long_sequence_gb300 import build as b
+        b.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", dbg], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    assert ctypes.CDLL(dbg).cp_debug_build() == 1
+    assert cpa._L().cp_debug_build() == (1 if cpa.DEBUG else 0)
+
+
+def test_tile_classes_argument_checks(cpa):
+    import ctypes
+    p = cpa.Plan(512, 4, 2, 64, ring_degree=2, layout=1)
+    n = ctypes.c_int64()
+    assert cpa._L().cp_tile_classes(p.handle, None, 0, None, None) == cpa.CP_ERR_INVALID_ARG
+    assert cpa._L().cp_tile_classes(p.handle, None, -1, ctypes.byref(n), None) == cpa.CP_ERR_INVALID_ARG
+    assert cpa._L().cp_tile_classes(p.handle, None, 5, ctypes.byref(n), None) == cpa.CP_ERR_INVALID_ARG
+    assert cpa._L().cp_tile_classes(None, None, 0, ctypes.byref(n), None) == cpa.CP_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("L,R,U,layout", [(64, 4, 1, 0), (64, 4, 1, 1), (96, 3, 2, 1), (128, 2, 4, 1),
                                           (1024, 8, 1, 1), (48, 1, 1, 1), (2048, 8, 4, 1)])
 def test_index_map_matches_oracle(cpa, L, R, U, layout):
