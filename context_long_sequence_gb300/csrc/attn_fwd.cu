@@ -63,17 +63,17 @@ constexpr uint32_t HALF_BYTES = 128 * 128;   // one 64-column (128-byte) swizzle
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kThreads = 320;
 
-constexpr int kSlots = 5;                    // K/V ring slots
+constexpr int kSlots = 5;                    // K/V ring slots (K of key tile j is load 2j, V load 2j+1)
+constexpr int kTileBars = 3;                 // key tiles in flight at most: 5 slots, 2 per tile
 
 enum Bar {
   BAR_Q = 0,
-  BAR_KV_FULL = 1,               // +slot
-  BAR_KV_EMPTY = 1 + kSlots,     // +slot
-  BAR_S_FULL = 1 + 2 * kSlots,   // +query tile
-  BAR_P_FULL = 3 + 2 * kSlots,   // +query tile
-  BAR_O_DONE = 5 + 2 * kSlots,   // +query tile
-  BAR_DRAIN = 7 + 2 * kSlots,
-  NUM_BARS = 8 + 2 * kSlots
+  BAR_T_FULL = 1,                          // +key tile % kTileBars: its K and V landed
+  BAR_KV_EMPTY = 1 + kTileBars,            // +slot
+  BAR_S_FULL = 1 + kTileBars + kSlots,     // +query tile
+  BAR_P_FULL = 3 + kTileBars + kSlots,     // +query tile
+  BAR_DRAIN = 5 + kTileBars + kSlots,      // every MMA of the CTA completed
+  NUM_BARS = 6 + kTileBars + kSlots
 };
 
 template <int D>
@@ -196,14 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(bar(BAR_KV_FULL + i), 1);
-      mbar_init(bar(BAR_KV_EMPTY + i), 1);
-    }
+    for (int i = 0; i < kTileBars; ++i) mbar_init(bar(BAR_T_FULL + i), 1);
+    for (int i = 0; i < kSlots; ++i) mbar_init(bar(BAR_KV_EMPTY + i), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_S_FULL + i), 1);
       mbar_init(bar(BAR_P_FULL + i), 4);
-      mbar_init(bar(BAR_O_DONE + i), 1);
     }
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
@@ -235,25 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
       }
-      int n = 0;  // loads issued
-      auto load = [&](const CUtensorMap* map, int kv_row) -> bool {
-        const int sl = slot_of(n);
-        if (!mbar_wait(bar(BAR_KV_EMPTY + sl), parity_of(n) ^ 1, abort_flag, status)) return false;
-        mbar_arrive_expect_tx(bar(BAR_KV_FULL + sl), SM::kKV);
-        (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < kv_rows && hkv < g.Hkv_loc, status);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sKV + sl * SM::kKV + hh * HALF_BYTES, map, bar(BAR_KV_FULL + sl), hkv * D + hh * 64, kv_row);
-        ++n;
-        return true;
-      };
+      // Key tile nt: K into slot of load 2nt, V into slot of load 2nt+1, both
+      // completing one tile barrier, so the issuer waits once per tile.  The
+      // two slots were last used by V of tile nt-3 and K of tile nt-2, so the
+      // tile barrier nt % 3 was last used by tile nt-3, whose wait is done.
+      int n = 0;   // loads issued
+      int nt = 0;  // key tiles issued
       for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row, int, int) {
         if (*abort_flag) return;
-        if (load(&tm_k, kv_row)) load(&tm_v, kv_row);
+        const int slk = slot_of(n), slv = slot_of(n + 1);
+        if (!mbar_wait(bar(BAR_KV_EMPTY + slk), parity_of(n) ^ 1, abort_flag, status)) return;
+        if (!mbar_wait(bar(BAR_KV_EMPTY + slv), parity_of(n + 1) ^ 1, abort_flag, status)) return;
+        const uint32_t tb = bar(BAR_T_FULL + nt % kTileBars);
+        mbar_arrive_expect_tx(tb, 2 * SM::kKV);
+        (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < kv_rows && hkv < g.Hkv_loc, status);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sKV + slk * SM::kKV + hh * HALF_BYTES, &tm_k, tb, hkv * D + hh * 64, kv_row);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sKV + slv * SM::kKV + hh * HALF_BYTES, &tm_v, tb, hkv * D + hh * 64, kv_row);
+        n += 2;
+        ++nt;
       });
       if (*abort_flag) {
         // Let every copy still in flight land before the CTA exits.
         mbar_wait(bar(BAR_Q), 0, nullptr, status);
-        for (int i = max(0, n - kSlots); i < n; ++i) mbar_wait(bar(BAR_KV_FULL + slot_of(i)), parity_of(i), nullptr, status);
+        for (int i = max(0, nt - kTileBars); i < nt; ++i)
+          mbar_wait(bar(BAR_T_FULL + i % kTileBars), (i / kTileBars) & 1, nullptr, status);
       }
     }
   } else if (warp == 1) {
@@ -263,8 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
       int npv[2] = {0, 0};      // PVs issued per query tile
       int pend_sl = -1;         // V slot of a PV1 still to issue
-      uint32_t pend_ph = 0;
-      bool pend_ready = false;  // that V load was already waited for
       // Descriptors are built once; each MMA only adds a compile-time offset
       // to the start-address field (addresses stay below 256 KB, so the
       // 14-bit field never carries).  This thread shares its scheduler with
@@ -286,51 +288,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_t += P_t V: A = P_t in TMEM (8 columns per 16 keys), B = V [keys x d]
       // read as N=d x K=keys, MN-major (16 keys = 16 rows of 128 bytes; the two
-      // 64-column halves of d are HALF_BYTES apart).
-      // V slot of the load a PV reads; `v_ready` skips the wait when the other
-      // tile's PV of the same key tile already saw that load land.
-      auto issue_pv = [&](int t, int sl, uint32_t ph, bool v_ready, bool release_v) -> bool {
+      // 64-column halves of d are HALF_BYTES apart), from V slot `sl`.  No
+      // per-PV completion signal: the softmax learns that O_t is stable from
+      // the next S_t commit (issued after this PV) or, at the end, from the
+      // drain commit.
+      auto issue_pv = [&](int t, int sl, bool release_v) -> bool {
         if (!mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status)) return false;
-        if (!v_ready && !mbar_wait(bar(BAR_KV_FULL + sl), ph, abort_flag, status)) return false;
         tc_fence_after();
         const uint64_t b0 = dv0 + static_cast<uint64_t>(sl) * kSlotStep;
         mma_bf16_ts_k128(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
-        mma_commit(bar(BAR_O_DONE + t));
         if (release_v) mma_commit(bar(BAR_KV_EMPTY + sl));
         ++npv[t];
         return true;
       };
-      int j = 0;
+      int j = 0;                // key tiles walked
       int ring_slot = 0;        // slot of the next K load
-      uint32_t ring_ph = 0;     // its phase parity
       bool ok = mbar_wait(bar(BAR_Q), 0, abort_flag, status);
       if (ok) {
+        // No abort-flag read per tile: every wait below leaves on the flag.
         for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int, int kpos0, int klen) {
-          if (!ok || *abort_flag) return;
+          if (!ok) return;
           const bool v0 = win0.sees(kpos0, klen), v1 = win1.sees(kpos0, klen);
-          // K of tile j is load 2j, V is load 2j+1 (slots advance by one per load).
           const int kslot = ring_slot, vslot = ring_slot + 1 == kSlots ? 0 : ring_slot + 1;
-          const uint32_t kph = ring_ph, vph = ring_slot + 1 == kSlots ? ring_ph ^ 1u : ring_ph;
           ring_slot = vslot + 1 == kSlots ? 0 : vslot + 1;
-          ring_ph = vslot + 1 == kSlots ? vph ^ 1u : vph;
-          if (!(ok = mbar_wait(bar(BAR_KV_FULL + kslot), kph, abort_flag, status))) return;
+          // One wait per key tile: its K and V complete the same barrier.
+          if (!(ok = mbar_wait(bar(BAR_T_FULL + j % kTileBars), (j / kTileBars) & 1, abort_flag, status))) return;
           tc_fence_after();
           if (v0) issue_qk(0, kslot);
           if (pend_sl >= 0) {
-            if (!(ok = issue_pv(1, pend_sl, pend_ph, pend_ready, true))) return;
+            if (!(ok = issue_pv(1, pend_sl, true))) return;
             pend_sl = -1;
           }
           if (v1) issue_qk(1, kslot);
           mma_commit(bar(BAR_KV_EMPTY + kslot));
-          if (v0 && !(ok = issue_pv(0, vslot, vph, false, !v1))) return;
-          if (v1) {
-            pend_sl = vslot;
-            pend_ph = vph;
-            pend_ready = v0;
-          }
+          if (v0 && !(ok = issue_pv(0, vslot, !v1))) return;
+          if (v1) pend_sl = vslot;
           ++j;
         });
-        if (ok && pend_sl >= 0 && !*abort_flag) issue_pv(1, pend_sl, pend_ph, pend_ready, true);
+        if (ok && pend_sl >= 0 && !*abort_flag) issue_pv(1, pend_sl, true);
       }
       // Every MMA issued so far completes before TMEM and shared memory are released.
       mma_commit(bar(BAR_DRAIN));
@@ -434,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
     });
     if (ok && k > 0) {
-      ok = warp_all(mbar_wait(bar(BAR_O_DONE + t), (k - 1) & 1, abort_flag, status));
+      // All MMAs of the CTA, the last PV_t among them, have completed.
+      ok = warp_all(mbar_wait(bar(BAR_DRAIN), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
