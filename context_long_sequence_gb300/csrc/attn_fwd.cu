@@ -262,16 +262,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one
+    // elected lane executes each tcgen05 instruction.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
       int npv[2] = {0, 0};      // PVs issued per query tile
       int pend_sl = -1;         // V slot of a PV1 still to issue
       // Descriptors are built once; each MMA only adds a compile-time offset
       // to the start-address field (addresses stay below 256 KB, so the
-      // 14-bit field never carries).  This thread shares its scheduler with
-      // softmax warps, so every instruction it saves shortens the critical
-      // path of the tensor core.
+      // 14-bit field never carries).  The issuing warp shares its scheduler
+      // with softmax warps, so every instruction it saves shortens the
+      // critical path of the tensor core.
       const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(sQ + SM::kQ, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sKV, 16, 1024);          // slot 0 read as K (K-major)
@@ -281,10 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t a0 = t ? dq1 : dq0;
         const uint64_t b0 = dk0 + static_cast<uint64_t>(slot) * kSlotStep;
         if constexpr (D == 128)
-          mma_bf16_ss_k128<HALF_BYTES>(tmem + 128 * t, a0, b0, idesc_qk, 0u);
+          mma_bf16_ss_k128_warp<HALF_BYTES>(tmem + 128 * t, a0, b0, idesc_qk, 0u);
         else
-          mma_bf16_ss_k64(tmem + 128 * t, a0, b0, idesc_qk, 0u);
-        mma_commit(bar(BAR_S_FULL + t));
+          mma_bf16_ss_k64_warp(tmem + 128 * t, a0, b0, idesc_qk, 0u);
+        mma_commit_warp(bar(BAR_S_FULL + t));
       };
       // O_t += P_t V: A = P_t in TMEM (8 columns per 16 keys), B = V [keys x d]
       // read as N=d x K=keys, MN-major (16 keys = 16 rows of 128 bytes; the two
@@ -293,17 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next S_t commit (issued after this PV) or, at the end, from the
       // drain commit.
       auto issue_pv = [&](int t, int sl, bool release_v) -> bool {
-        if (!mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status)) return false;
+        if (!warp_all(mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status))) return false;
         tc_fence_after();
         const uint64_t b0 = dv0 + static_cast<uint64_t>(sl) * kSlotStep;
-        mma_bf16_ts_k128(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
-        if (release_v) mma_commit(bar(BAR_KV_EMPTY + sl));
+        mma_bf16_ts_k128_warp(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
+        if (release_v) mma_commit_warp(bar(BAR_KV_EMPTY + sl));
         ++npv[t];
         return true;
       };
       int j = 0;                // key tiles walked
       int ring_slot = 0;        // slot of the next K load
-      bool ok = mbar_wait(bar(BAR_Q), 0, abort_flag, status);
+      bool ok = warp_all(mbar_wait(bar(BAR_Q), 0, abort_flag, status));
       if (ok) {
         // No abort-flag read per tile: every wait below leaves on the flag.
         for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int, int kpos0, int klen) {
@@ -312,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kslot = ring_slot, vslot = ring_slot + 1 == kSlots ? 0 : ring_slot + 1;
           ring_slot = vslot + 1 == kSlots ? 0 : vslot + 1;
           // One wait per key tile: its K and V complete the same barrier.
-          if (!(ok = mbar_wait(bar(BAR_T_FULL + j % kTileBars), (j / kTileBars) & 1, abort_flag, status))) return;
+          if (!(ok = warp_all(mbar_wait(bar(BAR_T_FULL + j % kTileBars), (j / kTileBars) & 1, abort_flag, status))))
+            return;
           tc_fence_after();
           if (v0) issue_qk(0, kslot);
           if (pend_sl >= 0) {
@@ -320,15 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend_sl = -1;
           }
           if (v1) issue_qk(1, kslot);
-          mma_commit(bar(BAR_KV_EMPTY + kslot));
+          mma_commit_warp(bar(BAR_KV_EMPTY + kslot));
           if (v0 && !(ok = issue_pv(0, vslot, !v1))) return;
           if (v1) pend_sl = vslot;
           ++j;
         });
-        if (ok && pend_sl >= 0 && !*abort_flag) issue_pv(1, pend_sl, true);
+        if (ok && pend_sl >= 0 && !warp_all(*abort_flag != 0)) issue_pv(1, pend_sl, true);
       }
       // Every MMA issued so far completes before TMEM and shared memory are released.
-      mma_commit(bar(BAR_DRAIN));
+      mma_commit_warp(bar(BAR_DRAIN));
       mbar_wait(bar(BAR_DRAIN), 0, nullptr, status);
     }
   } else {
