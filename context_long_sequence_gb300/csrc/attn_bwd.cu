@@ -62,12 +62,13 @@ __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu
 
 
 // Q K^T-type product over d: A and B both K-major, 128-byte swizzled.
+// Issued warp-wide (see mma_bf16_ss_k128_warp).
 template <int D>
 __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
   if constexpr (D == 128)
-    mma_bf16_ss_k128<HALF_BYTES>(d_tmem, a, b, idesc, 0u);
+    mma_bf16_ss_k128_warp<HALF_BYTES>(d_tmem, a, b, idesc, 0u);
   else
-    mma_bf16_ss_k64(d_tmem, a, b, idesc, 0u);
+    mma_bf16_ss_k64_warp(d_tmem, a, b, idesc, 0u);
 }
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
@@ -241,7 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one
+    // elected lane executes each tcgen05 instruction.
+    {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, D, 1);
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
@@ -253,40 +256,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A operand of dQ; dP_n overwrites those columns only after dQ_{n-1},
       // issued before it by this thread, has read them.
       auto issue_dq = [&](int m) {  // dQ += dS_m K_m
-        mma_bf16_ts_k128_halves(tdQ, tdP, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
+        mma_bf16_ts_k128_halves_warp(tdQ, tdP, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
                                 m > 0 ? 1u : 0u);
-        mma_commit(bar(DQ_K_EMPTY + m % kKStages));
+        mma_commit_warp(bar(DQ_K_EMPTY + m % kKStages));
       };
       int n = 0;
-      if (mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status)) {
+      if (warp_all(mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status))) {
         for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int, int) {
-          if (*abort_flag) return;
+          if (warp_all(*abort_flag != 0)) return;
           const int ks = n % kKStages, vs = n % kVStages, sb = n & 1;
-          if (!mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status)) return;
+          if (!warp_all(mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status))) return;
           // S buffer sb: the element-wise warps have read S_{n-2} from it.
-          if (n >= 2 && !mbar_wait(bar(DQ_S_EMPTY + sb), ((n >> 1) & 1) ^ 1, abort_flag, status)) return;
+          if (n >= 2 && !warp_all(mbar_wait(bar(DQ_S_EMPTY + sb), ((n >> 1) & 1) ^ 1, abort_flag, status))) return;
           tc_fence_after();
           mma_qk<D>(tS(sb), dQ0, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
-          mma_commit(bar(DQ_S_FULL + sb));
+          mma_commit_warp(bar(DQ_S_FULL + sb));
           if (n > 0) {
-            if (!mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+            if (!warp_all(mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status))) return;
             tc_fence_after();
             issue_dq(n - 1);
           }
-          if (!mbar_wait(bar(DQ_V_FULL + vs), (n / kVStages) & 1, abort_flag, status)) return;
+          if (!warp_all(mbar_wait(bar(DQ_V_FULL + vs), (n / kVStages) & 1, abort_flag, status))) return;
           tc_fence_after();
           mma_qk<D>(tdP, dDO0, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s);
-          mma_commit(bar(DQ_DP_FULL));
-          mma_commit(bar(DQ_V_EMPTY + vs));
+          mma_commit_warp(bar(DQ_DP_FULL));
+          mma_commit_warp(bar(DQ_V_EMPTY + vs));
           ++n;
         });
-        if (n > 0 && !*abort_flag && mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status)) {
+        if (n > 0 && !warp_all(*abort_flag != 0) && warp_all(mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status))) {
           tc_fence_after();
           issue_dq(n - 1);
-          mma_commit(bar(DQ_DONE));
+          mma_commit_warp(bar(DQ_DONE));
         }
       }
-      mma_commit(bar(DQ_DRAIN));
+      mma_commit_warp(bar(DQ_DRAIN));
       mbar_wait(bar(DQ_DRAIN), 0, nullptr, status);
     }
   } else {
@@ -606,7 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one
+    // elected lane executes each tcgen05 instruction.
+    {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(BM, D, 1);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
@@ -619,52 +624,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_n (dP_n) overwrites those columns only after dV_{n-1} (dK_{n-1}),
       // issued before it by this thread, has read them.
       auto issue_dv = [&](int m) {  // dV += P^T_m dO_m
-        mma_bf16_ts_k128_halves(tdV, tSt, dDOmn0 + static_cast<uint64_t>(m % kDOStages) * kStep, idesc_acc,
+        mma_bf16_ts_k128_halves_warp(tdV, tSt, dDOmn0 + static_cast<uint64_t>(m % kDOStages) * kStep, idesc_acc,
                                 m > 0 ? 1u : 0u);
-        mma_commit(bar(KV_DO_EMPTY + m % kDOStages));
+        mma_commit_warp(bar(KV_DO_EMPTY + m % kDOStages));
       };
       auto issue_dk = [&](int m) {  // dK += dS^T_m Q_m
-        mma_bf16_ts_k128_halves(tdK, tdPt, dQmn0 + static_cast<uint64_t>(m % kQStages) * kStep, idesc_acc,
+        mma_bf16_ts_k128_halves_warp(tdK, tdPt, dQmn0 + static_cast<uint64_t>(m % kQStages) * kStep, idesc_acc,
                                 m > 0 ? 1u : 0u);
-        mma_commit(bar(KV_Q_EMPTY + m % kQStages));
+        mma_commit_warp(bar(KV_Q_EMPTY + m % kQStages));
       };
       int n = 0;
-      if (mbar_wait(bar(KV_FULL), 0, abort_flag, status)) {
+      if (warp_all(mbar_wait(bar(KV_FULL), 0, abort_flag, status))) {
         for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int, int, int, int, int) {
-          if (*abort_flag) return;
+          if (warp_all(*abort_flag != 0)) return;
           if (n > 0) {
-            if (!mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) return;
+            if (!warp_all(mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status))) return;
             tc_fence_after();
             issue_dv(n - 1);
           }
           const int qs = n % kQStages, ds = n % kDOStages;
-          if (!mbar_wait(bar(KV_Q_FULL + qs), (n / kQStages) & 1, abort_flag, status)) return;
+          if (!warp_all(mbar_wait(bar(KV_Q_FULL + qs), (n / kQStages) & 1, abort_flag, status))) return;
           tc_fence_after();
           mma_qk<D>(tSt, dK0, dQ0 + static_cast<uint64_t>(qs) * kStep, idesc_s);
-          mma_commit(bar(KV_S_FULL));
+          mma_commit_warp(bar(KV_S_FULL));
           if (n > 0) {
-            if (!mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) return;
+            if (!warp_all(mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status))) return;
             tc_fence_after();
             issue_dk(n - 1);
           }
-          if (!mbar_wait(bar(KV_DO_FULL + ds), (n / kDOStages) & 1, abort_flag, status)) return;
+          if (!warp_all(mbar_wait(bar(KV_DO_FULL + ds), (n / kDOStages) & 1, abort_flag, status))) return;
           tc_fence_after();
           mma_qk<D>(tdPt, dV0, dDO0 + static_cast<uint64_t>(ds) * kStep, idesc_s);
-          mma_commit(bar(KV_DP_FULL));
+          mma_commit_warp(bar(KV_DP_FULL));
           ++n;
         });
         // dV and dK of the last query tile.
-        if (n > 0 && !*abort_flag && mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status)) {
+        if (n > 0 && !warp_all(*abort_flag != 0) && warp_all(mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status))) {
           tc_fence_after();
           issue_dv(n - 1);
-          if (mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status)) {
+          if (warp_all(mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status))) {
             tc_fence_after();
             issue_dk(n - 1);
-            mma_commit(bar(KV_ACC_DONE));
+            mma_commit_warp(bar(KV_ACC_DONE));
           }
         }
       }
-      mma_commit(bar(KV_DRAIN));
+      mma_commit_warp(bar(KV_DRAIN));
       mbar_wait(bar(KV_DRAIN), 0, nullptr, status);
     }
   } else {

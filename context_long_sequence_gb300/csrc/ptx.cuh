@@ -141,149 +141,22 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, "
-      "%3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.  A (M=128 rows x K) sits in
-// TMEM with row i in lane i and two consecutive bf16 K-elements per 32-bit
-// column (the lower half holding the even element).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, "
-      "%3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Eight back-to-back MMAs D (+)= A * B^T over K = 128 (eight K=16 steps) in
-// one asm block: one predicate set-up, descriptor offsets as immediates.
-// A and B are K-major, 128-byte-swizzled, two 64-column halves HALF bytes
-// apart; step kk adds ((kk/4)*HALF + (kk%4)*32) >> 4 to both start
-// addresses.  The first step accumulates only if `accumulate` != 0.
-template <uint32_t HALF>
-__device__ __forceinline__ void mma_bf16_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  constexpr uint64_t h = HALF >> 4;
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 a, b;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %5;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %7;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %8;\n\tadd.s64 b, %2, %8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(h), "n"(h + 2), "n"(h + 4), "n"(h + 6)
-      : "memory");
-}
-
-// Same, K = 64 (four K=16 steps within one 64-column half).
-__device__ __forceinline__ void mma_bf16_ss_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 a, b;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Eight MMAs D (+)= A * B over K = 128 with A K-major (128-byte swizzle,
-// two 64-column halves HALF bytes apart: steps as in mma_bf16_ss_k128) and
-// B MN-major (16 rows of 128 bytes per K=16 step: +2048 bytes per step).
-template <uint32_t HALF>
-__device__ __forceinline__ void mma_bf16_ss_k128_bmn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                     uint32_t idesc, uint32_t accumulate) {
-  constexpr uint64_t h = HALF >> 4;
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 a, b;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %6;\n\tadd.s64 b, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %7;\n\tadd.s64 b, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "add.s64 a, %1, %8;\n\tadd.s64 b, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-      "}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(h), "n"(h + 2), "n"(h + 4), "n"(h + 6)
-      : "memory");
-}
-
-// Eight MMAs D (+)= A[tmem] * B^T over 128 keys: A advances 8 TMEM columns
-// per K=16 step; B (MN-major, 16 rows of 128 bytes per step) advances 2048
-// bytes (128 in descriptor units).
-__device__ __forceinline__ void mma_bf16_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// As mma_bf16_ts_k128, with the 128 K-elements of A held in TMEM as two
-// blocks of 32 packed columns, 64 columns apart: K-steps 0-3 read columns
-// a..a+31, steps 4-7 columns a+64..a+95.
-__device__ __forceinline__ void mma_bf16_ts_k128_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 64;\n\tadd.s64 b, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 72;\n\tadd.s64 b, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 80;\n\tadd.s64 b, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 88;\n\tadd.s64 b, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive (once) on an mbarrier when all prior tcgen05 ops of this thread finish.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// ---------------------------------------------------------------- warp-wide issue
+// ---------------------------------------------------------------- MMA issue (warp-wide)
 //
-// The *_warp forms are executed by all 32 lanes of the issuing warp, with the
-// same operands in every lane; elect.sync picks one lane to execute the
-// tcgen05 instruction.  Keeping the whole issuing loop warp-uniform lets the
-// compiler hold descriptors and TMEM addresses in uniform registers, which
-// tcgen05.mma reads directly; a loop run by one lane alone must first move
-// every operand of every MMA into them and issues measurably slower.  All 32
-// lanes must be converged at each call.
+// Every MMA helper below is executed by all 32 lanes of the issuing warp,
+// with the same operands in every lane; elect.sync picks one lane to execute
+// the tcgen05 instructions.  Keeping the whole issuing loop warp-uniform lets
+// the compiler hold descriptors and TMEM addresses in uniform registers,
+// which tcgen05.mma reads directly; a loop run by one lane alone must first
+// move every operand of every MMA into them and issues measurably slower.
+// All 32 lanes must be converged at each call.  Each helper issues eight
+// back-to-back kind::f16 MMAs (bf16 inputs, fp32 accumulate in TMEM) over
+// K = 128 in one asm block (K = 64: four); only the first accumulates
+// conditionally (`accumulate` != 0), the rest always accumulate.
 
+// D (+)= A * B^T, A and B in shared memory, both K-major, 128-byte swizzled,
+// two 64-column halves HALF bytes apart: K-step kk adds
+// ((kk/4)*HALF + (kk%4)*32) >> 4 to both start addresses.
 template <uint32_t HALF>
 __device__ __forceinline__ void mma_bf16_ss_k128_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                       uint32_t idesc, uint32_t accumulate) {
@@ -304,6 +177,7 @@ __device__ __forceinline__ void mma_bf16_ss_k128_warp(uint32_t d_tmem, uint64_t 
       : "memory");
 }
 
+// Same, K = 64 (four K=16 steps within one 64-column half).
 __device__ __forceinline__ void mma_bf16_ss_k64_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                      uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -318,6 +192,11 @@ __device__ __forceinline__ void mma_bf16_ss_k64_warp(uint32_t d_tmem, uint64_t a
       : "memory");
 }
 
+// D (+)= A[tmem] * B^T over 128 keys.  A (M=128 rows x K) sits in TMEM with
+// row i in lane i and two consecutive bf16 K-elements per 32-bit column (the
+// lower half holding the even element); it advances 8 columns per K=16 step.
+// B is MN-major (16 rows of 128 bytes per step) and advances 2048 bytes (128
+// in descriptor units).
 __device__ __forceinline__ void mma_bf16_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                       uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -336,7 +215,29 @@ __device__ __forceinline__ void mma_bf16_ts_k128_warp(uint32_t d_tmem, uint32_t 
       : "memory");
 }
 
-// mma_commit issued by one elected lane of a converged warp.
+// As mma_bf16_ts_k128_warp, with the 128 K-elements of A held in TMEM as two
+// blocks of 32 packed columns, 64 columns apart: K-steps 0-3 read columns
+// a..a+31, steps 4-7 columns a+64..a+95.
+__device__ __forceinline__ void mma_bf16_ts_k128_halves_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 64;\n\tadd.s64 b, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 72;\n\tadd.s64 b, %2, 640;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 80;\n\tadd.s64 b, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 88;\n\tadd.s64 b, %2, 896;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on an mbarrier when all prior tcgen05 ops of the issuing
+// thread finish; executed by one elected lane of a converged warp.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
