@@ -73,7 +73,8 @@ enum Bar {
   BAR_S_FULL = 1 + kTileBars + kSlots,     // +query tile
   BAR_P_FULL = 3 + kTileBars + kSlots,     // +query tile
   BAR_DRAIN = 5 + kTileBars + kSlots,      // every MMA of the CTA completed
-  NUM_BARS = 6 + kTileBars + kSlots
+  BAR_P_HALF = 6 + kTileBars + kSlots,     // +query tile: P of keys 0-63 written
+  NUM_BARS = 8 + kTileBars + kSlots
 };
 
 template <int D>
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_S_FULL + i), 1);
       mbar_init(bar(BAR_P_FULL + i), 4);
+      mbar_init(bar(BAR_P_HALF + i), 4);
     }
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
@@ -290,15 +292,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_t += P_t V: A = P_t in TMEM (8 columns per 16 keys), B = V [keys x d]
       // read as N=d x K=keys, MN-major (16 keys = 16 rows of 128 bytes; the two
-      // 64-column halves of d are HALF_BYTES apart), from V slot `sl`.  No
-      // per-PV completion signal: the softmax learns that O_t is stable from
-      // the next S_t commit (issued after this PV) or, at the end, from the
-      // drain commit.
+      // 64-column halves of d are HALF_BYTES apart), from V slot `sl`.  The
+      // softmax signals P of keys 0-63 before it computes keys 64-127, so the
+      // first four MMAs start while it finishes.  No per-PV completion
+      // signal: the softmax learns that O_t is stable from the next S_t
+      // commit (issued after this PV) or, at the end, from the drain commit.
       auto issue_pv = [&](int t, int sl, bool release_v) -> bool {
-        if (!warp_all(mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status))) return false;
+        if (!warp_all(mbar_wait(bar(BAR_P_HALF + t), npv[t] & 1, abort_flag, status))) return false;
         tc_fence_after();
         const uint64_t b0 = dv0 + static_cast<uint64_t>(sl) * kSlotStep;
-        mma_bf16_ts_k128_warp(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
+        mma_bf16_ts_k64_warp(tmem + 256 + D * t, tmem + 128 * t, b0, idesc_pv, npv[t] > 0 ? 1u : 0u);
+        if (!warp_all(mbar_wait(bar(BAR_P_FULL + t), npv[t] & 1, abort_flag, status))) return false;
+        tc_fence_after();
+        mma_bf16_ts_k64_warp(tmem + 256 + D * t, tmem + 128 * t + 32, b0 + 512, idesc_pv, 1u);
         if (release_v) mma_commit_warp(bar(BAR_KV_EMPTY + sl));
         ++npv[t];
         return true;
@@ -393,8 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // slots of scalar code); exp2 stays per element on the MUFU pipe.
       const f32x2 sl2x2 = make_f32x2(sl2, sl2), nmbx2 = make_f32x2(-mb, -mb);
       f32x2 rs2[4] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      auto exp_chunk = [&](int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -406,13 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tSt + c * 16, pk);
-      }
-      tmem_wait_st();
-      float rs_lo[4], rs_hi[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) split_f32x2(rs2[i], rs_lo[i], rs_hi[i]);
-      l = l * alpha + (((rs_lo[0] + rs_hi[0]) + (rs_lo[1] + rs_hi[1])) + ((rs_lo[2] + rs_hi[2]) + (rs_lo[3] + rs_hi[3])));
-      // O is stable here: this tile's S_FULL commit came after the previous PV_t.
+      };
+      exp_chunk(0);
+      exp_chunk(1);
+      // O is stable here: this tile's S_FULL commit came after the previous
+      // PV_t; its rescale lands before the first half of this tile's PV.
       if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -424,11 +427,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
           tmem_st32(tOt + c * 32, ov);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_P_HALF + t));
+      exp_chunk(2);
+      exp_chunk(3);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
+      float rs_lo[4], rs_hi[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) split_f32x2(rs2[i], rs_lo[i], rs_hi[i]);
+      l = l * alpha + (((rs_lo[0] + rs_hi[0]) + (rs_lo[1] + rs_hi[1])) + ((rs_lo[2] + rs_hi[2]) + (rs_lo[3] + rs_hi[3])));
       ++k;
     });
     if (ok && k > 0) {

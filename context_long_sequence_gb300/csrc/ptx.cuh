@@ -192,13 +192,14 @@ __device__ __forceinline__ void mma_bf16_ss_k64_warp(uint32_t d_tmem, uint64_t a
       : "memory");
 }
 
-// D (+)= A[tmem] * B^T over 128 keys.  A (M=128 rows x K) sits in TMEM with
-// row i in lane i and two consecutive bf16 K-elements per 32-bit column (the
-// lower half holding the even element); it advances 8 columns per K=16 step.
-// B is MN-major (16 rows of 128 bytes per step) and advances 2048 bytes (128
-// in descriptor units).
-__device__ __forceinline__ void mma_bf16_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                      uint32_t idesc, uint32_t accumulate) {
+// Four MMAs D (+)= A[tmem] * B^T over 64 keys.  A (M=128 rows x K) sits in
+// TMEM with row i in lane i and two consecutive bf16 K-elements per 32-bit
+// column (the lower half holding the even element); it advances 8 columns
+// per K=16 step.  B is MN-major (16 rows of 128 bytes per step) and advances
+// 2048 bytes (128 in descriptor units) per step.  Keys 64-127 of a 128-key
+// tile follow at A + 32 columns and B + 512 descriptor units.
+__device__ __forceinline__ void mma_bf16_ts_k64_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -206,18 +207,15 @@ __device__ __forceinline__ void mma_bf16_ts_k128_warp(uint32_t d_tmem, uint32_t 
       "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
       "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
       "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
       "}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// As mma_bf16_ts_k128_warp, with the 128 K-elements of A held in TMEM as two
+// Eight MMAs over 128 keys with the 128 K-elements of A held in TMEM as two
 // blocks of 32 packed columns, 64 columns apart: K-steps 0-3 read columns
-// a..a+31, steps 4-7 columns a+64..a+95.
+// a..a+31, steps 4-7 columns a+64..a+95 (layout of A and B otherwise as in
+// mma_bf16_ts_k64_warp).
 __device__ __forceinline__ void mma_bf16_ts_k128_halves_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
