@@ -37,6 +37,7 @@ DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
 METRIC = "CP causal attn fwd TFLOPS & tokens/s, L=1K-1M, % of GB300 bf16 dense peak"
 BWD_FLOP_RATIO = 2.5   # backward useful FLOPs per forward FLOP (dV, dP, dQ, dK products + recompute of S excluded)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SUSTAINED_MS = 1000.0  # attention launches this long are compared with the sustained tensor peak
 
 
 def useful_flops(w: workloads.Workload, offsets) -> int:
@@ -491,7 +492,10 @@ def main():
                              + (2 if args.kv_exchange == "allgather" else 0)
                              + ((3 + (9 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # A launch of a second or more runs under the power cap: its peak is
+        # the sustained one; shorter launches are compared with the burst peak.
+        sustained = attn_ms >= SUSTAINED_MS
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         result = {
             "metric": METRIC,
             "value": round(value, 3),
@@ -516,7 +520,7 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"bf16 dense burst, {peak_src}",
+                         "peak_source": f"bf16 dense {'sustained' if sustained else 'burst'}, {peak_src}",
                          "traffic": None if args.L else profiled_traffic(w.name)},
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
