@@ -41,7 +41,6 @@ struct FastDiv {
   __host__ __device__ __forceinline__ uint32_t div(uint32_t x) const {
     return static_cast<uint32_t>((static_cast<uint64_t>(x) * m) >> sh);
   }
-  __host__ __device__ __forceinline__ uint32_t mod(uint32_t x) const { return x - div(x) * d; }
 };
 
 FastDiv make_fastdiv(uint32_t d) {
