@@ -449,16 +449,20 @@ def main():
         bwd_ms = timed(bwd, reps)
         kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,
                             "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"
-                                       + (" and 9 Ulysses reshards" if U > 1 else "")}
+                                       + (" and 2 batched Ulysses reshards (6 tensors in, 3 out)" if U > 1 else "")}
     if U > 1:
+        # The two exchanges as cp_attn_fwd issues them: one launch for Q, K, V
+        # and one for O and LSE.
         def rin():
-            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh, stream=stream)
-            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh, stream=stream)
-            cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, v, vh, stream=stream)
+            cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh),
+                                             (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh),
+                                             (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, v, vh)],
+                                      stream=stream)
 
         def rout():
-            cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, oh, o, stream=stream)
-            cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, w.Hq, 1, 4, lh, lse, stream=stream)
+            cpa.ulysses_reshard_batch(plan, [(cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, oh, o),
+                                             (cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, w.Hq, 1, 4, lh, lse)],
+                                      stream=stream)
         bytes_in = 2 * 2 * w.L * w.d * (w.Hq + 2 * w.Hkv)
         bytes_out = 2 * (2 * w.L * w.d * w.Hq + 4 * w.L * w.Hq)
         t_in = timed(rin, reps)
@@ -486,11 +490,13 @@ def main():
     if rank == 0:
         ms_per_step = total_ms / args.steps
         value = aggregate_value(flops_step, world, ms_per_step)
-        # forward: 3 reshards in, attention, 2 reshards out (U > 1); merge with
-        # partials.  backward: delta, dkv, dq, plus 6 reshards in and 3 out (U > 1).
-        launches_per_step = ((6 if U > 1 else 1) + (1 if w.emit_partials else 0)
+        # forward: attention, plus one batched reshard in (Q, K, V) and one out
+        # (O, LSE) when U > 1; merge with partials; two gathers with the
+        # all-gather exchange.  backward: delta, dkv, dq, plus one batched
+        # reshard in and one out when U > 1.
+        launches_per_step = ((3 if U > 1 else 1) + (1 if w.emit_partials else 0)
                              + (2 if args.kv_exchange == "allgather" else 0)
-                             + ((3 + (9 if U > 1 else 0)) if w.backward else 0))
+                             + ((3 + (2 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
         # A launch of a second or more runs under the power cap: its peak is
         # the sustained one; shorter launches are compared with the burst peak.

@@ -44,6 +44,21 @@ CP_OP_FWD = 0
 CP_OP_BWD = 1
 
 
+CP_RESHARD_MAX_JOBS = 8
+
+
+class cp_reshard_job_t(ctypes.Structure):
+    _fields_ = [
+        ("direction", ctypes.c_int32),
+        ("tensor_kind", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("row_elems", ctypes.c_int32),
+        ("elem_bytes", ctypes.c_int32),
+        ("inp", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+    ]
+
+
 class cp_plan_desc_t(ctypes.Structure):
     _fields_ = [
         ("version", ctypes.c_int32),
@@ -85,6 +100,7 @@ def _L():
     lib.cp_index_map.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
     lib.cp_workspace_size.argtypes = [_vp, _i, ctypes.POINTER(ctypes.c_size_t)]
     lib.ulysses_reshard.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+    lib.ulysses_reshard_batch.argtypes = [_vp, _i, ctypes.POINTER(cp_reshard_job_t), _vp]
     lib.cp_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.cp_attn_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_fwd_rank.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]
@@ -105,6 +121,7 @@ def _L():
 
 
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
+            "ulysses_reshard_batch",
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
             "cp_merge_lse", "cp_get_status", "cp_get_status_detail", "cp_debug_build", "cp_strerror",
             "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes"]
@@ -216,6 +233,15 @@ class Plan:
 def ulysses_reshard(plan: Plan, direction, tensor_kind, H, row_elems, elem_bytes, inp, out, stream=None):
     _check(_L().ulysses_reshard(plan.handle, int(direction), int(tensor_kind), int(H), int(row_elems),
                                 int(elem_bytes), _ptr(inp), _ptr(out), _stream(stream)), "ulysses_reshard")
+
+
+def ulysses_reshard_batch(plan: Plan, jobs, stream=None):
+    """jobs: sequence of (direction, tensor_kind, H, row_elems, elem_bytes, inp, out)."""
+    arr = (cp_reshard_job_t * max(1, len(jobs)))()
+    for i, (direction, kind, H, row_elems, elem_bytes, inp, out) in enumerate(jobs):
+        arr[i] = cp_reshard_job_t(int(direction), int(kind), int(H), int(row_elems), int(elem_bytes),
+                                  _ptr(inp), _ptr(out))
+    _check(_L().ulysses_reshard_batch(plan.handle, len(jobs), arr, _stream(stream)), "ulysses_reshard_batch")
 
 
 def cp_attn_fwd(plan: Plan, q, k, v, o, lse, workspace=None, workspace_bytes=None, stream=None):

@@ -492,24 +492,56 @@ int cp_workspace_size(const cp_plan_t* p, int op, size_t* bytes) {
   return CP_OK;
 }
 
+namespace {
+// Argument checks of one reshard; *bytes = size of its input (= output).
+int check_reshard_job(const cp_plan_t* p, const cp_reshard_job_t& j, size_t* bytes) {
+  if (!j.in || !j.out) return CP_ERR_INVALID_ARG;
+  if (j.direction != CP_SEQ_TO_HEAD && j.direction != CP_HEAD_TO_SEQ) return CP_ERR_INVALID_ARG;
+  if (j.tensor_kind != CP_TOKEN_MAJOR && j.tensor_kind != CP_HEAD_MAJOR) return CP_ERR_INVALID_ARG;
+  const int U = p->desc.ulysses_degree;
+  if (j.H <= 0 || j.row_elems <= 0 || j.elem_bytes <= 0 || j.H % U) return CP_ERR_INVALID_ARG;
+  if (j.tensor_kind == CP_HEAD_MAJOR && j.row_elems != 1) return CP_ERR_INVALID_ARG;
+  if (!aligned16(j.in) || !aligned16(j.out)) return CP_ERR_ALIGNMENT;
+  *bytes = static_cast<size_t>(p->desc.L) * j.H * j.row_elems * j.elem_bytes;
+  return CP_OK;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return x < y + nb && y < x + na;
+}
+}  // namespace
+
 int ulysses_reshard(const cp_plan_t* p, int direction, int tensor_kind, int H, int row_elems, int elem_bytes,
                     const void* in, void* out, cudaStream_t stream) {
-  if (!p || !in || !out) return CP_ERR_INVALID_ARG;
-  if (direction != CP_SEQ_TO_HEAD && direction != CP_HEAD_TO_SEQ) return CP_ERR_INVALID_ARG;
-  if (tensor_kind != CP_TOKEN_MAJOR && tensor_kind != CP_HEAD_MAJOR) return CP_ERR_INVALID_ARG;
-  const int U = p->desc.ulysses_degree;
-  if (H <= 0 || row_elems <= 0 || elem_bytes <= 0 || H % U) return CP_ERR_INVALID_ARG;
-  if (tensor_kind == CP_HEAD_MAJOR && row_elems != 1) return CP_ERR_INVALID_ARG;
-  if (!aligned16(in) || !aligned16(out)) return CP_ERR_ALIGNMENT;
+  if (!p) return CP_ERR_INVALID_ARG;
+  const cp_reshard_job_t job{direction, tensor_kind, H, row_elems, elem_bytes, in, out};
+  return ulysses_reshard_batch(p, 1, &job, stream);
+}
+
+int ulysses_reshard_batch(const cp_plan_t* p, int n_jobs, const cp_reshard_job_t* jobs, cudaStream_t stream) {
+  if (!p || !jobs || n_jobs < 1 || n_jobs > CP_RESHARD_MAX_JOBS) return CP_ERR_INVALID_ARG;
+  size_t bytes[CP_RESHARD_MAX_JOBS];
+  for (int i = 0; i < n_jobs; ++i) {
+    const int rc = check_reshard_job(p, jobs[i], &bytes[i]);
+    if (rc != CP_OK) return rc;
+  }
+  // The jobs run concurrently: no output may overlap any input or another output.
+  for (int i = 0; i < n_jobs; ++i)
+    for (int k = 0; k < n_jobs; ++k) {
+      if (overlap(jobs[i].out, bytes[i], jobs[k].in, bytes[k])) return CP_ERR_INVALID_ARG;
+      if (k != i && overlap(jobs[i].out, bytes[i], jobs[k].out, bytes[k])) return CP_ERR_INVALID_ARG;
+    }
   int rc = check_device(p);
   if (rc != CP_OK) return rc;
-  const char* a = static_cast<const char*>(in);
-  const char* b = static_cast<const char*>(out);
-  const size_t bytes = static_cast<size_t>(p->desc.L) * H * row_elems * elem_bytes;
-  if (a < b + bytes && b < a + bytes) return CP_ERR_INVALID_ARG;
+  cpattn::ReshardSpec spec[CP_RESHARD_MAX_JOBS];
+  for (int i = 0; i < n_jobs; ++i)
+    spec[i] = cpattn::ReshardSpec{jobs[i].H, jobs[i].row_elems, jobs[i].direction, jobs[i].tensor_kind,
+                                  jobs[i].elem_bytes, jobs[i].in, jobs[i].out};
   NvtxRange range("ulysses_reshard");
-  return cpattn::launch_reshard(p->desc.ring_degree, U, p->n, H, row_elems, direction, tensor_kind, elem_bytes, in,
-                                out, stream, status_ptr());
+  return cpattn::launch_reshard_batch(p->desc.ring_degree, p->desc.ulysses_degree, p->n, spec, n_jobs, stream,
+                                      status_ptr());
 }
 
 int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -573,16 +605,14 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   void* vh = ws + w.vh;
   void* oh = ws + w.oh;
   float* lseh = reinterpret_cast<float*>(ws + w.lseh);
-  // One Ulysses exchange of every ring group: H heads of row_elems elements.
-  auto reshard = [&](int H, int row_elems, int dir, int kind, int elem_bytes, const void* in, void* out) {
-    return cpattn::launch_reshard(R, U, p->n, H, row_elems, dir, kind, elem_bytes, in, out, stream, a.status);
-  };
+  // The Ulysses exchanges of every ring group, all tensors of one exchange
+  // in one launch: Q, K, V before attention, O and LSE after it.
   {
     NvtxRange phase("reshard_in");
-    if ((rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh)) ||
-        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh)) ||
-        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh)))
-      return rc;
+    const cpattn::ReshardSpec in[3] = {{d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh},
+                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh},
+                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh}};
+    if ((rc = cpattn::launch_reshard_batch(R, U, p->n, in, 3, stream, a.status))) return rc;
   }
   a.q = qh;
   a.k = kh;
@@ -596,8 +626,9 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
     if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
   }
   NvtxRange phase("reshard_out");
-  if ((rc = reshard(d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o))) return rc;
-  return reshard(d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse);
+  const cpattn::ReshardSpec out[2] = {{d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o},
+                                      {d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse}};
+  return cpattn::launch_reshard_batch(R, U, p->n, out, 2, stream, a.status);
 }
 
 int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -691,18 +722,15 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   // backward runs per head group, and dQ, dK, dV come back token-sharded.
   const int R = d.ring_degree, U = d.ulysses_degree, n = p->n;
   const int ob = d.out_fp32 ? 4 : 2;
-  auto reshard = [&](int H, int row_elems, int dir, int kind, int elem_bytes, const void* in, void* out) {
-    return cpattn::launch_reshard(R, U, n, H, row_elems, dir, kind, elem_bytes, in, out, stream, a.status);
-  };
   {
     NvtxRange phase("reshard_in");
-    if ((rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh)) ||
-        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh)) ||
-        (rc = reshard(d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh)) ||
-        (rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh)) ||
-        (rc = reshard(d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh)) ||
-        (rc = reshard(d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh)))
-      return rc;
+    const cpattn::ReshardSpec in[6] = {{d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh},
+                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh},
+                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh},
+                                       {d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh},
+                                       {d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh},
+                                       {d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh}};
+    if ((rc = cpattn::launch_reshard_batch(R, U, n, in, 6, stream, a.status))) return rc;
   }
   a.q = ws + w.qh;
   a.k = ws + w.kh;
@@ -718,10 +746,10 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
     if ((rc = cpattn::launch_attn_bwd(a, stream))) return rc;
   }
   NvtxRange phase("reshard_out");
-  if ((rc = reshard(d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq)) ||
-      (rc = reshard(d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk)))
-    return rc;
-  return reshard(d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv);
+  const cpattn::ReshardSpec out[3] = {{d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq},
+                                      {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk},
+                                      {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv}};
+  return cpattn::launch_reshard_batch(R, U, n, out, 3, stream, a.status);
 }
 
 int cp_tile_classes(const cp_plan_t* p, int32_t* host_rows, int64_t capacity, int64_t* n_rows, cudaStream_t stream) {

@@ -94,6 +94,18 @@ int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, v
 int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind,
                    int elem_bytes, const void* in, void* out, cudaStream_t stream, int32_t* status);
 
+// One reshard of a batch (the arguments of launch_reshard).
+struct ReshardSpec {
+  int H, row_elems, direction, kind, elem_bytes;
+  const void* in;
+  void* out;
+};
+
+// Up to 8 reshards of one plan geometry in one launch (two when some need
+// 4-byte vectors and others 16-byte ones).
+int launch_reshard_batch(int R, int U, int n, const ReshardSpec* jobs, int count, cudaStream_t stream,
+                         int32_t* status);
+
 // Merge of `n_parts` partials, `batch` independent groups laid out back to back.
 int launch_merge(int batch, int n_parts, int rows, int H, int d, const float* o_parts,
                  const float* lse_parts, void* o_out, float* lse_out, int out_fp32, cudaStream_t stream,

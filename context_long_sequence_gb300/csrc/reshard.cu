@@ -107,38 +107,60 @@ __device__ __forceinline__ uint32_t in_block(const ReshardGeom& g, uint32_t ob) 
 }
 
 constexpr int kBlocksInFlight = 4;
+constexpr int kMaxJobs = 8;
+
+// Several reshards in one launch: job j owns the global units
+// [unit0[j], unit0[j+1]); all jobs use the same vector type.
+struct ReshardBatch {
+  ReshardGeom g[kMaxJobs];
+  const void* in[kMaxJobs];
+  void* out[kMaxJobs];
+  uint32_t unit0[kMaxJobs + 1];
+  int n;
+};
 
 template <typename V>
-__global__ void __launch_bounds__(256) reshard_kernel(const V* __restrict__ in, V* __restrict__ out, ReshardGeom g) {
+__global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ ReshardBatch b) {
   const int lane = threadIdx.x & 31;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   const uint32_t w0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  for (uint32_t base = w0 * kBlocksInFlight; base < g.nunits; base += warps * kBlocksInFlight) {
-    uint64_t src[kBlocksInFlight], dst[kBlocksInFlight];
+  const uint32_t total = b.unit0[b.n];
+  for (uint32_t base = w0 * kBlocksInFlight; base < total; base += warps * kBlocksInFlight) {
+    const V* src[kBlocksInFlight];
+    V* dst[kBlocksInFlight];
     uint32_t len[kBlocksInFlight];
 #pragma unroll
     for (int i = 0; i < kBlocksInFlight; ++i) {
-      const uint32_t un = base + i;
+      const uint32_t gu = base + i;
       len[i] = 0;
-      src[i] = dst[i] = 0;
-      if (un < g.nunits) {
+      src[i] = nullptr;
+      dst[i] = nullptr;
+      if (gu < total) {
+        int j = 0;
+        while (j + 1 < b.n && gu >= b.unit0[j + 1]) ++j;
+        const ReshardGeom& g = b.g[j];
+        const uint32_t un = gu - b.unit0[j];
         const uint32_t ob = un / g.nseg;
         const uint32_t v0 = (un - ob * g.nseg) * g.seg;
         const uint32_t ib = in_block(g, ob);
         if (!CP_IN_BOUNDS(ib < g.nblocks && ob < g.nblocks && v0 < g.blk, g.status)) continue;
         len[i] = min(g.seg, g.blk - v0);
-        src[i] = static_cast<uint64_t>(ib) * g.blk + v0;
-        dst[i] = static_cast<uint64_t>(ob) * g.blk + v0;
+        src[i] = static_cast<const V*>(b.in[j]) + (static_cast<uint64_t>(ib) * g.blk + v0);
+        dst[i] = static_cast<V*>(b.out[j]) + (static_cast<uint64_t>(ob) * g.blk + v0);
       }
     }
-    for (uint32_t v = lane; v < g.seg; v += 32) {
+    // A warp's segments are at most 4 KB, so lane strides cover them in a few steps.
+    uint32_t seg_max = 0;
+#pragma unroll
+    for (int i = 0; i < kBlocksInFlight; ++i) seg_max = max(seg_max, len[i]);
+    for (uint32_t v = lane; v < seg_max; v += 32) {
       V val[kBlocksInFlight];
 #pragma unroll
       for (int i = 0; i < kBlocksInFlight; ++i)
-        if (v < len[i]) val[i] = __ldg(in + src[i] + v);
+        if (v < len[i]) val[i] = __ldg(src[i] + v);
 #pragma unroll
       for (int i = 0; i < kBlocksInFlight; ++i)
-        if (v < len[i]) out[dst[i] + v] = val[i];
+        if (v < len[i]) dst[i][v] = val[i];
     }
   }
 }
@@ -186,51 +208,99 @@ int launch_gather_rows(const AttnGeom& g, long long row_bytes, const void* in, v
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
-int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind, int elem_bytes,
-                   const void* in, void* out, cudaStream_t stream, int32_t* status) {
+namespace {
+
+// Geometry of one reshard; vec_bytes = 16 or 4 (the vector type it needs).
+// Returns CP_OK with g.nunits == 0 for an empty job.
+int reshard_geom(int R, int U, int n, const ReshardSpec& j, int32_t* status, ReshardGeom* out_g, int* vec_bytes) {
   ReshardGeom g;
   g.status = status;
   g.U = U;
   g.n = n;
-  g.H = H;
-  g.Hl = H / U;
-  g.dir = direction;
-  g.kind = kind;
+  g.H = j.H;
+  g.Hl = j.H / U;
+  g.dir = j.direction;
+  g.kind = j.kind;
   g.fU = make_fastdiv(g.U);
   g.fn = make_fastdiv(g.n);
   g.fH = make_fastdiv(g.H);
   g.fHl = make_fastdiv(g.Hl);
-  const long long block_bytes = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(g.Hl) * row_elems * elem_bytes
-                                                         : static_cast<long long>(n) * elem_bytes;
-  const long long nblocks = (kind == CP_TOKEN_MAJOR) ? static_cast<long long>(R) * U * n * U
-                                                     : static_cast<long long>(R) * U * H;
+  g.nunits = 0;
+  const long long block_bytes = (j.kind == CP_TOKEN_MAJOR)
+                                    ? static_cast<long long>(g.Hl) * j.row_elems * j.elem_bytes
+                                    : static_cast<long long>(n) * j.elem_bytes;
+  const long long nblocks = (j.kind == CP_TOKEN_MAJOR) ? static_cast<long long>(R) * U * n * U
+                                                       : static_cast<long long>(R) * U * j.H;
+  *vec_bytes = (block_bytes % 16 == 0) ? 16 : 4;
+  *out_g = g;
   if (nblocks == 0 || block_bytes == 0) return CP_OK;
   if (nblocks >= (1LL << 31)) return CP_ERR_UNSUPPORTED;  // the block index math is 31-bit
-  g.nblocks = static_cast<uint32_t>(nblocks);
-  const int threads = 256, warps_per_cta = threads / 32;
-  const long long vec_bytes = (block_bytes % 16 == 0) ? 16 : 4;
-  const long long blk = block_bytes / vec_bytes;
   if (block_bytes % 4 != 0) return CP_ERR_UNSUPPORTED;
+  const long long blk = block_bytes / *vec_bytes;
   if (blk >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
   // Segments: 4 KB of a token-major block; 512 bytes of a head-major (LSE)
   // block, whose blocks are few and long.
-  const long long seg = std::min<long long>(blk, (kind == CP_HEAD_MAJOR ? 512 : 4096) / vec_bytes);
+  const long long seg = std::min<long long>(blk, (j.kind == CP_HEAD_MAJOR ? 512 : 4096) / *vec_bytes);
   const long long nseg = (blk + seg - 1) / seg;
   const long long nunits = nblocks * nseg;
   if (nunits >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+  g.nblocks = static_cast<uint32_t>(nblocks);
   g.blk = static_cast<uint32_t>(blk);
   g.seg = static_cast<uint32_t>(seg);
   g.nseg = static_cast<uint32_t>(nseg);
   g.nunits = static_cast<uint32_t>(nunits);
-  const long long need = (nunits + warps_per_cta * kBlocksInFlight - 1) / (warps_per_cta * kBlocksInFlight);
+  *out_g = g;
+  return CP_OK;
+}
+
+template <typename V>
+int launch_batch(const ReshardBatch& b, cudaStream_t stream) {
+  const uint32_t total = b.unit0[b.n];
+  if (total == 0) return CP_OK;
+  const int threads = 256, warps_per_cta = threads / 32;
+  const long long need = (static_cast<long long>(total) + warps_per_cta * kBlocksInFlight - 1) /
+                         (warps_per_cta * kBlocksInFlight);
   const long long cap = static_cast<long long>(sm_count()) * 8;
   const int grid = static_cast<int>(need < cap ? need : cap);
-  if (vec_bytes == 16)
-    reshard_kernel<uint4><<<grid, threads, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
-  else
-    reshard_kernel<uint32_t><<<grid, threads, 0, stream>>>(static_cast<const uint32_t*>(in),
-                                                           static_cast<uint32_t*>(out), g);
+  reshard_kernel<V><<<grid, threads, 0, stream>>>(b);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_reshard_batch(int R, int U, int n, const ReshardSpec* jobs, int count, cudaStream_t stream,
+                         int32_t* status) {
+  if (count < 0 || count > kMaxJobs) return CP_ERR_INVALID_ARG;
+  // Jobs that need 16-byte vectors go in one launch, the others in a second.
+  ReshardBatch b16{}, b4{};
+  long long u16 = 0, u4 = 0;
+  for (int i = 0; i < count; ++i) {
+    ReshardGeom g;
+    int vb = 16;
+    const int rc = reshard_geom(R, U, n, jobs[i], status, &g, &vb);
+    if (rc != CP_OK) return rc;
+    if (g.nunits == 0) continue;
+    ReshardBatch& b = vb == 16 ? b16 : b4;
+    long long& u = vb == 16 ? u16 : u4;
+    b.g[b.n] = g;
+    b.in[b.n] = jobs[i].in;
+    b.out[b.n] = jobs[i].out;
+    b.unit0[b.n] = static_cast<uint32_t>(u);
+    u += g.nunits;
+    if (u >= (1LL << 32)) return CP_ERR_UNSUPPORTED;
+    ++b.n;
+    b.unit0[b.n] = static_cast<uint32_t>(u);
+  }
+  int rc = CP_OK;
+  if (b16.n > 0) rc = launch_batch<uint4>(b16, stream);
+  if (rc == CP_OK && b4.n > 0) rc = launch_batch<uint32_t>(b4, stream);
+  return rc;
+}
+
+int launch_reshard(int R, int U, int n, int H, int row_elems, int direction, int kind, int elem_bytes,
+                   const void* in, void* out, cudaStream_t stream, int32_t* status) {
+  const ReshardSpec j{H, row_elems, direction, kind, elem_bytes, in, out};
+  return launch_reshard_batch(R, U, n, &j, 1, stream, status);
 }
 
 }  // namespace cpattn

@@ -164,6 +164,27 @@ int ulysses_reshard(const cp_plan_t *plan, int direction, int tensor_kind, int H
                     int row_elems, int elem_bytes, const void *in, void *out,
                     cudaStream_t stream);
 
+/* Several Ulysses reshards of one plan in one kernel launch, e.g. the Q, K,
+ * V exchange before attention or the O and LSE exchange after it (the same
+ * permutations as ulysses_reshard, one launch instead of one per tensor;
+ * jobs whose blocks need 4-byte words go in a second launch).  jobs (host,
+ * n_jobs entries, 1 .. CP_RESHARD_MAX_JOBS) hold ulysses_reshard's
+ * arguments; the same rules apply to each, and in addition no job's output
+ * may overlap any job's input or another job's output (CP_ERR_INVALID_ARG).
+ * Bit-exact. */
+#define CP_RESHARD_MAX_JOBS 8
+typedef struct {
+  int direction;   /* CP_SEQ_TO_HEAD | CP_HEAD_TO_SEQ */
+  int tensor_kind; /* CP_TOKEN_MAJOR | CP_HEAD_MAJOR */
+  int H;           /* heads of the tensor (U divides H) */
+  int row_elems;   /* E: elements per (token, head) row; 1 for CP_HEAD_MAJOR */
+  int elem_bytes;
+  const void *in;  /* device */
+  void *out;       /* device */
+} cp_reshard_job_t;
+int ulysses_reshard_batch(const cp_plan_t *plan, int n_jobs, const cp_reshard_job_t *jobs,
+                          cudaStream_t stream);
+
 /* Causal CP attention forward for all P emulated ranks.
  *   q  [P][n][Hq][d]  bf16, sequence-sharded (slot order of cp_index_map)
  *   k,v[P][n][Hkv][d] bf16

@@ -56,6 +56,31 @@ def test_debug_library_exports_and_flag(cpa):
     assert cpa._L().cp_debug_build() == (1 if cpa.DEBUG else 0)
 
 
+def test_reshard_batch_argument_checks(cpa):
+    """ulysses_reshard_batch rejects bad job counts, misaligned pointers and
+    overlapping buffers before touching the device (fake addresses)."""
+    p = cpa.Plan(1024, 8, 4, 64, ulysses_degree=4, ring_degree=2, layout=1)
+    nbytes = 1024 * 8 * 64 * 2
+    base = 1 << 36
+    job = lambda i, o: (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, 8, 64, 2, i, o)
+    L = cpa._L()
+
+    def call(jobs, n=None):
+        arr = (cpa.cp_reshard_job_t * max(1, len(jobs)))()
+        for i, j in enumerate(jobs):
+            arr[i] = cpa.cp_reshard_job_t(*j[:5], j[5], j[6])
+        return L.ulysses_reshard_batch(p.handle, len(jobs) if n is None else n, arr, None)
+    a, b, c, d = base, base + 4 * nbytes, base + 8 * nbytes, base + 12 * nbytes
+    assert call([job(a, b)], n=0) == cpa.CP_ERR_INVALID_ARG
+    assert call([job(a, b)] * 9) == cpa.CP_ERR_INVALID_ARG
+    assert call([job(a + 8, b)]) == cpa.CP_ERR_ALIGNMENT
+    assert call([job(a, b), job(c, b + 256)]) == cpa.CP_ERR_INVALID_ARG      # two outputs overlap
+    assert call([job(a, b), job(b + 512, d)]) == cpa.CP_ERR_INVALID_ARG      # an input inside an output
+    assert call([job(a, a + 256)]) == cpa.CP_ERR_INVALID_ARG                 # in and out overlap
+    assert call([(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, 6, 64, 2, a, b)]) == cpa.CP_ERR_INVALID_ARG  # U does not divide H
+    assert L.ulysses_reshard_batch(p.handle, 1, None, None) == cpa.CP_ERR_INVALID_ARG
+
+
 def test_tile_classes_argument_checks(cpa):
     import ctypes
     p = cpa.Plan(512, 4, 2, 64, ring_degree=2, layout=1)

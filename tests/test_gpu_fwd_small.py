@@ -211,6 +211,37 @@ def test_reshard_bit_exact(cpa, R, U, n, H, E, eb):
     assert np.array_equal(ref_l, lse.numpy())
 
 
+@pytest.mark.parametrize("R,U,n", [(2, 4, 48), (3, 2, 10), (1, 4, 4096)])
+def test_reshard_batch_equals_single_calls(cpa, R, U, n):
+    """One batched launch (Q, K, V and an odd-sized tensor that needs 4-byte
+    words, then O and LSE back) gives the bytes of one call per tensor."""
+    L = R * U * n
+    plan = cpa.Plan(L, 8, 4, 64, ulysses_degree=U, ring_degree=R)
+    g = torch.Generator().manual_seed(7 * R + U)
+    q = torch.randint(-30000, 30000, (L, 8, 64), generator=g).to(torch.int16).cuda()
+    k = torch.randint(-30000, 30000, (L, 4, 64), generator=g).to(torch.int16).cuda()
+    v = torch.randint(-30000, 30000, (L, 4, 64), generator=g).to(torch.int16).cuda()
+    odd = torch.randint(-2**30, 2**30, (L, 4, 3), generator=g).to(torch.int32).cuda()   # 12-byte rows
+    lse = torch.randn(R * U, 8, n, generator=g).cuda()
+    specs = [(8, 64, 2, q), (4, 64, 2, k), (4, 64, 2, v), (4, 3, 4, odd)]
+    singles = [torch.empty_like(t) for *_, t in specs]
+    batch = [torch.empty_like(t) for *_, t in specs]
+    for (H, E, eb, t), y in zip(specs, singles):
+        cpa.ulysses_reshard(plan, cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, H, E, eb, t, y)
+    cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, H, E, eb, t, y)
+                                     for (H, E, eb, t), y in zip(specs, batch)])
+    for a, b in zip(singles, batch):
+        assert torch.equal(a, b)
+    lh1, lh2 = torch.empty_like(lse), torch.empty_like(lse)
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, 8, 64, 2, singles[0], o1)
+    cpa.ulysses_reshard(plan, cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, 8, 1, 4, lse, lh1)
+    cpa.ulysses_reshard_batch(plan, [(cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, 8, 64, 2, batch[0], o2),
+                                     (cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, 8, 1, 4, lse, lh2)])
+    assert torch.equal(o1, o2) and torch.equal(o2, q)
+    assert torch.equal(lh1, lh2)
+
+
 @pytest.mark.parametrize("n_parts,rows,H,d", [(4, 256, 4, 64), (3, 77, 2, 128), (1, 5, 3, 64), (8, 130, 1, 128)])
 def test_merge_matches_oracle(cpa, n_parts, rows, H, d):
     g = torch.Generator().manual_seed(n_parts * 7 + rows)
