@@ -73,7 +73,8 @@ def assert_close(O, LSE, O_ref, LSE_ref, what="", bf16_out=False):
 
 
 def grad_tolerance(ref: np.ndarray):
-    """Gradient bounds (the workload spec gives none; derivation in the design doc).
+    """Gradient bounds (the workload spec states none for gradients; they
+    follow from the arithmetic below).
 
     dV = P^T dO, dK = scale dS^T Q and dQ = scale dS K are unnormalised sums
     whose operands P and dS are rounded to bf16 (unit roundoff 2^-8) before
