@@ -81,6 +81,18 @@ def rank_work_spread(index_map, R: int, offsets) -> float:
     return round(float(work.max() / work.mean()), 4)
 
 
+def secondary_bounds(ex2_per_clk, mma_clk, n_sm, clock_rec, d):
+    """The exp2 (MUFU) bound and the tensor rate of a plain MMA stream, at the
+    GPU's maximum SM clock: every visible (query, key) pair of a head costs one
+    exp2 and 4*d useful FLOPs."""
+    mhz = (clock_rec or {}).get("sm_max_mhz") or 2070.0
+    hz = float(mhz) * 1e6
+    return {"ex2_per_clk_per_sm": round(ex2_per_clk, 2), "mma_clk_m128n128k16": round(mma_clk, 2),
+            "sm_count": n_sm, "sm_clock_mhz": mhz,
+            "exp2_bound_tflops": round(ex2_per_clk * n_sm * hz * 4 * d / 1e12, 1),
+            "mma_stream_tflops": round(n_sm * hz * 2 * 128 * 128 * 16 / mma_clk / 1e12, 1)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if not os.path.exists(path):
@@ -287,6 +299,10 @@ def main():
         ws_bwd = cpa.alloc_workspace(plan, cpa.CP_OP_BWD, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # The rates behind the secondary bounds: exp2 per SM clock (one per
+    # visible pair and head) and clocks per M128 N128 K16 MMA, measured here.
+    ex2_per_clk, mma_clk = cpa.cp_measure_rates(stream=stream)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def fwd():
         cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws, stream=stream)
@@ -531,6 +547,7 @@ def main():
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
             "hbm_peak_gbs": peaks["hbm_gbs"],
+            "secondary": secondary_bounds(ex2_per_clk, mma_clk, n_sm, clock_rec, w.d),
             "clocks": clock_rec,
             "wall_s_timed": round(t_wall, 3),
         }

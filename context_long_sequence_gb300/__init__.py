@@ -114,6 +114,7 @@ def _L():
     lib.cp_tile_classes.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64,
                                     ctypes.POINTER(ctypes.c_int64), _vp]
     lib.cp_debug_build.argtypes = []
+    lib.cp_measure_rates.argtypes = [ctypes.POINTER(ctypes.c_double), _vp]
     lib.cp_strerror.argtypes = [_i]
     lib.cp_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -124,7 +125,7 @@ EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_s
             "ulysses_reshard_batch",
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
             "cp_merge_lse", "cp_get_status", "cp_get_status_detail", "cp_debug_build", "cp_strerror",
-            "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes"]
+            "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes", "cp_measure_rates"]
 
 
 class CPError(RuntimeError):
@@ -312,6 +313,13 @@ def cp_get_status_detail(stream=None):
     out = (ctypes.c_int32 * 4)()
     _check(_L().cp_get_status_detail(_stream(stream), out), "cp_get_status_detail")
     return tuple(int(x) for x in out)
+
+
+def cp_measure_rates(stream=None):
+    """(ex2 results per SM clock, SM clocks per M128 N128 K16 bf16 MMA)."""
+    out = (ctypes.c_double * 2)()
+    _check(_L().cp_measure_rates(out, _stream(stream)), "cp_measure_rates")
+    return float(out[0]), float(out[1])
 
 
 def cp_debug_build() -> bool:

@@ -957,6 +957,124 @@ extern "C" int cp_selftest_bounds(int32_t block, int32_t* line, cudaStream_t str
 }
 
 // ---------------------------------------------------------------------------
+// Rates behind the kernels' rooflines (cp_measure_rates): exp2 results per
+// SM clock on the MUFU pipe (the softmax's one exponential per visible pair)
+// and SM clocks per tcgen05.mma M128 N128 K16 (bf16, A in TMEM, B in shared
+// memory: the PV form), each timed with clock64 inside one CTA per SM.
+namespace {
+constexpr int kRateEx2Threads = 512, kRateEx2Chains = 16, kRateEx2Iters = 1000;
+constexpr int kRateMmaGroups = 200;
+
+__global__ void __launch_bounds__(kRateEx2Threads) rate_ex2_kernel(unsigned long long* cyc, float* sink) {
+  float a[kRateEx2Chains];
+#pragma unroll
+  for (int i = 0; i < kRateEx2Chains; ++i) a[i] = -1e-3f * static_cast<float>(threadIdx.x + i);
+  __syncthreads();
+  const unsigned long long t0 = clock64();
+  for (int it = 0; it < kRateEx2Iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kRateEx2Chains; ++i) a[i] = cpattn::ex2_approx(a[i]) - 1.0f;  // stays in (-1, 0]
+  }
+  __syncthreads();
+  const unsigned long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRateEx2Chains; ++i) acc += a[i];
+  if (acc == 1.0f) sink[threadIdx.x] = acc;  // never true; keeps the chains live
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+constexpr uint32_t kRateMmaSmem = 120 * 1024;  // one CTA per SM
+
+__global__ void __launch_bounds__(128, 1) rate_mma_kernel(unsigned long long* cyc, int32_t* status) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sB = cpattn::smem_u32(sm);  // 32 KB: a 128 x 128 bf16 tile, two 64-column halves
+  const uint32_t bar = cpattn::smem_u32(sm + 32768);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + 32768 + 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32768 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sm)[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+  if (threadIdx.x == 0) {
+    cpattn::mbar_init(bar, 1);
+    cpattn::fence_mbar_init();
+  }
+  if (warp == 0) {
+    cpattn::tmem_alloc(cpattn::smem_u32(slot), 512);
+    cpattn::tmem_relinquish();
+  }
+  cpattn::fence_proxy_async_smem();
+  cpattn::tc_fence_before();
+  __syncthreads();
+  cpattn::tc_fence_after();
+  const uint32_t tm = *slot;
+  if (warp == 1) {
+    constexpr uint32_t idesc = cpattn::idesc_bf16_f32(128, 128, 1);
+    const uint64_t b = cpattn::smem_desc_sw128(sB, 128 * 128, 1024);
+    const unsigned long long t0 = clock64();
+    for (int it = 0; it < kRateMmaGroups; ++it) {
+      cpattn::mma_bf16_ts_k64_warp(tm, tm + 256, b, idesc, 1u);
+      cpattn::mma_bf16_ts_k64_warp(tm, tm + 256 + 32, b + 512, idesc, 1u);
+    }
+    cpattn::mma_commit_warp(bar);
+    cpattn::mbar_wait(bar, 0, nullptr, status);
+    if (lane == 0) cyc[blockIdx.x] = clock64() - t0;
+  }
+  cpattn::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    cpattn::tc_fence_after();
+    cpattn::tmem_dealloc(tm, 512);
+  }
+}
+}  // namespace
+
+extern "C" int cp_measure_rates(double* out2, cudaStream_t stream) {
+  if (!out2) return CP_ERR_INVALID_ARG;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (major != 10 || minor != 3) return CP_ERR_ARCH;
+  int32_t* st = status_ptr();
+  if (!st) return CP_ERR_CUDA;
+  unsigned long long* d_cyc = nullptr;
+  float* d_sink = nullptr;
+  if (cudaMalloc(&d_cyc, 2 * sms * sizeof(unsigned long long)) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMalloc(&d_sink, kRateEx2Threads * sizeof(float)) != cudaSuccess) {
+    cudaFree(d_cyc);
+    return CP_ERR_CUDA;
+  }
+  int rc = CP_OK;
+  if (cudaFuncSetAttribute(rate_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateMmaSmem) !=
+      cudaSuccess)
+    rc = CP_ERR_CUDA;
+  if (rc == CP_OK) {
+    rate_ex2_kernel<<<sms, kRateEx2Threads, 0, stream>>>(d_cyc, d_sink);
+    rate_mma_kernel<<<sms, 128, kRateMmaSmem, stream>>>(d_cyc + sms, st);
+    if (cudaGetLastError() != cudaSuccess) rc = CP_ERR_CUDA;
+  }
+  std::vector<unsigned long long> cyc(2 * sms);
+  if (rc == CP_OK && (cudaMemcpyAsync(cyc.data(), d_cyc, cyc.size() * sizeof(unsigned long long),
+                                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+                      cudaStreamSynchronize(stream) != cudaSuccess))
+    rc = CP_ERR_CUDA;
+  cudaFree(d_cyc);
+  cudaFree(d_sink);
+  if (rc != CP_OK) return rc;
+  double ex2 = 0, mma = 0;
+  for (int i = 0; i < sms; ++i) {
+    ex2 += static_cast<double>(kRateEx2Threads) * kRateEx2Chains * kRateEx2Iters / static_cast<double>(cyc[i]);
+    mma += static_cast<double>(cyc[sms + i]) / (kRateMmaGroups * 8.0);
+  }
+  out2[0] = ex2 / sms;
+  out2[1] = mma / sms;
+  return CP_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Allocation-free emit-partials forward (cp_attn_fwd_noalloc).
 //
 // For callers that cannot allocate device memory (see the header): the

@@ -303,6 +303,16 @@ int cp_selftest_wait_timeout(int32_t limit_us, int32_t *out3, cudaStream_t strea
  * `stream`; the record is left for cp_get_status_detail to read. */
 int cp_selftest_bounds(int32_t block, int32_t *line, cudaStream_t stream);
 
+/* Rates behind the kernels' rooflines (no counterpart in the pages), each
+ * timed with the SM clock inside one CTA per SM on the current device:
+ * out2 (host, 2 doubles): [0] = ex2.approx.f32 results per SM clock (the
+ * softmax's one exponential per visible query-key pair runs on this pipe),
+ * [1] = SM clocks per tcgen05.mma M128 N128 K16 bf16 with A in tensor
+ * memory and B in shared memory, back to back from one issuing warp.
+ * Synchronous (allocates and frees a little device memory).  Returns
+ * CP_ERR_ARCH on a device other than sm_103. */
+int cp_measure_rates(double *out2, cudaStream_t stream);
+
 /* Allocation-free variant of the emit-partials forward (no counterpart in
  * the paper: it exists for callers, not for the method).
  *

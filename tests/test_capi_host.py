@@ -81,6 +81,10 @@ def test_reshard_batch_argument_checks(cpa):
     assert L.ulysses_reshard_batch(p.handle, 1, None, None) == cpa.CP_ERR_INVALID_ARG
 
 
+def test_measure_rates_argument_check(cpa):
+    assert cpa._L().cp_measure_rates(None, None) == cpa.CP_ERR_INVALID_ARG
+
+
 def test_tile_classes_argument_checks(cpa):
     import ctypes
     p = cpa.Plan(512, 4, 2, 64, ring_degree=2, layout=1)

@@ -264,3 +264,12 @@ def test_merge_matches_oracle(cpa, n_parts, rows, H, d):
     # exceeds 1e-2, so the bound is relative.
     err = np.abs(oo.float().cpu().numpy() - ref_o)
     assert (err <= 2.0 ** -8 * np.abs(ref_o) + 1e-5).all(), err.max()
+
+
+def test_measure_rates(cpa):
+    """The rate microbenchmarks behind the secondary bounds return plausible
+    figures: tens of exp2 per SM clock, and a bf16 M128 N128 K16 MMA in well
+    under a few hundred clocks (64 when the tensor core is fed back to back)."""
+    ex2, mma = cpa.cp_measure_rates()
+    assert 4.0 <= ex2 <= 128.0, ex2
+    assert 32.0 <= mma <= 256.0, mma
