@@ -8,6 +8,12 @@ the per-step partials and their merge.  Inputs are seeded synthetic bf16
 N(0,1) tensors resident in HBM; L2 is flushed (a 256 MiB write) before every
 timed step and the flush is outside the step's CUDA-event bracket.
 
+The default workload is the largest one that fits one GPU: USP (Ulysses 4 x
+ring 8, zigzag) over L = 1,048,576 tokens.  After it, the other four
+workloads are measured in the same run (``per_config``): the 1K-token
+emit-partials ring, the 16K Ulysses forward, the 64K zigzag ring forward
+with its backward, and the 128K packed-document ring.
+
 Prints one JSON line.  ``value`` is useful TFLOP/s (4 * d * Hq * visible
 (query, key) pairs per step, summed over ranks, / the max-over-ranks time).
 ``--impl reference`` times the CPU oracle instead, on bounded samples of the
@@ -24,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -33,11 +40,12 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
+DEFAULT_WORKLOAD = "usp_fwd_L1M_U4xR8_zigzag"
 METRIC = "CP causal attn fwd TFLOPS & tokens/s, L=1K-1M, % of GB300 bf16 dense peak"
 BWD_FLOP_RATIO = 2.5   # backward useful FLOPs per forward FLOP (dV, dP, dQ, dK products + recompute of S excluded)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-SUSTAINED_MS = 1000.0  # attention launches this long are compared with the sustained tensor peak
+SUSTAINED_MS = 1000.0  # launches this long run under the power cap: compared with the sustained tensor peak
+TIMED_WORK_S = 5.0     # target seconds of GPU work for secondary repeated measurements
 
 
 def useful_flops(w: workloads.Workload, offsets) -> int:
@@ -58,11 +66,15 @@ def row_visible(pos: np.ndarray, offsets) -> np.ndarray:
     return pos - start + 1
 
 
+LAYOUT_NAMES = ["contiguous", "zigzag", "balanced"]
+
+
 def workload_config(w, offsets, args, world: int, positions) -> dict:
     """The `config` object of the JSON line (both arms print the same one).
     positions: the slot -> global position map of the plan."""
+    layout = LAYOUT_NAMES[w.layout] + (f" (m={args.chunks_per_rank})" if w.layout == 2 else "")
     return {"workload": w.name, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ulysses": w.ulysses, "ring": w.ring,
-            "layout": ["contiguous", "zigzag", f"balanced (m={args.chunks_per_rank})"][w.layout],
+            "layout": layout,
             "rank_work_spread": rank_work_spread(positions, w.ring, offsets),
             "kv_exchange": args.kv_exchange,
             "docs": bool(offsets is not None),
@@ -117,6 +129,14 @@ def load_peaks():
     return out, "measured" if all(k in flat for k in ("hbm_gbs", "bf16_tflops")) else "partly fallback"
 
 
+def tensor_peak(peaks, peak_src, launch_ms):
+    """(peak TFLOP/s, its label) for an attention launch of launch_ms: the
+    sustained peak for launches of a second or more, else the burst one."""
+    sustained = launch_ms >= SUSTAINED_MS
+    return (peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"],
+            f"bf16 dense {'sustained' if sustained else 'burst'}, {peak_src}")
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -145,7 +165,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -156,11 +176,18 @@ class ClockSampler:
                 smax.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, flag in zip(names, f[5:9]):
                 if flag.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        rec = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if power:
+            rec["power_w_median"] = statistics.median(power)
+        return rec
 
 
 def kernel_source_hash() -> str:
@@ -172,20 +199,63 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic(workload: str):
     """DRAM bytes per attention launch from a committed ncu capture, if the
-    kernel source has not changed since (else None)."""
+    kernel source has not changed since (else None), with how it was taken."""
     path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
     if not os.path.exists(path):
-        return None
+        return None, None
     try:
         rec = json.load(open(path))
     except Exception:
-        return None
+        return None, None
     if rec.get("kernel_source_sha") != kernel_source_hash():
-        return None
-    return rec.get("per_launch_bytes", {}).get(workload)
+        return None, "kernel changed since the committed capture"
+    entry = rec.get("per_launch_bytes", {}).get(workload)
+    if isinstance(entry, dict):
+        return entry.get("bytes"), entry.get("how")
+    return entry, rec.get("source")
+
+
+def sha256_tensors(tensors: dict) -> dict:
+    """SHA-256 of each (CPU) tensor's bytes, hashed in parallel threads."""
+    out = {}
+
+    def one(name, t):
+        h = hashlib.sha256()
+        raw = t.contiguous().view(-1).view(dtype=__import__("torch").uint8).numpy()
+        step = 1 << 28
+        for i in range(0, raw.size, step):
+            h.update(memoryview(raw[i:i + step]))
+        out[name] = h.hexdigest()
+
+    threads = [threading.Thread(target=one, args=(n, t)) for n, t in tensors.items()]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    return {n: out[n] for n in tensors}
+
+
+def run_metadata(dev, w):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    meta = {"seed": w.seed, "gpu_name": props.name, "sm_count": props.multi_processor_count,
+            "torch": torch.__version__, "cuda_runtime": torch.version.cuda,
+            "host_cores": len(os.sched_getaffinity(0))}
+    try:
+        drv = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().splitlines()
+        meta["driver"] = drv[0] if drv else None
+    except Exception:
+        meta["driver"] = None
+    return meta
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
+
+
+def oracle_rows_per_call(L: int, cap: int) -> int:
+    """Query rows per oracle call: about 2^22 scores per call (fewer rows at long L)."""
+    return max(1, min(cap, (1 << 22) // L))
 
 
 def time_oracle(w, inputs_cpu, offsets, rows_per_call, heads, seed, min_seconds, max_calls=64):
@@ -206,10 +276,7 @@ def time_oracle(w, inputs_cpu, offsets, rows_per_call, heads, seed, min_seconds,
             return flops, el, calls
 
 
-def cpu_inputs(w, device_inputs=None):
-    import torch
-    if device_inputs is not None:
-        return {k: v.cpu() for k, v in device_inputs.items()}
+def cpu_inputs(w):
     return workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device="cpu", k_scale=w.k_scale)
 
 
@@ -228,6 +295,98 @@ def aggregate_value(flops_per_step_per_rank: int, world: int, ms_per_step_max: f
     return world * flops_per_step_per_rank / (ms_per_step_max * 1e-3) / 1e12
 
 
+def reps_for(step_ms: float, cap: int) -> int:
+    """Repetitions of a secondary measurement: about TIMED_WORK_S of GPU
+    work, at least 3 and at most cap."""
+    return int(max(3, min(cap, math.ceil(TIMED_WORK_S * 1e3 / max(step_ms, 1e-3)))))
+
+
+def make_plan(cpa, w, offsets, chunks_per_rank=8, kv_exchange="ring", out_fp32=False):
+    return cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
+                    doc_offsets=offsets, emit_partials=w.emit_partials, chunks_per_rank=chunks_per_rank,
+                    kv_exchange=cpa.CP_KV_ALLGATHER if kv_exchange == "allgather" else cpa.CP_KV_RING,
+                    out_fp32=out_fp32)
+
+
+class Timer:
+    """CUDA-event timing on the launching stream, L2 flushed before each rep."""
+
+    def __init__(self, torch, dev, stream, flush):
+        self.torch, self.dev, self.stream, self.flush = torch, dev, stream, flush
+
+    def __call__(self, fn, reps):
+        torch = self.torch
+        ts = []
+        for _ in range(reps):
+            self.flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
+
+
+def measure_other_workload(cpa, torch, w, dev, timer, peaks, peak_src):
+    """Forward (and, for the ring fwd+bwd workload, backward) of one more
+    workload, on its own seeded inputs: 3 warm-up calls, then the mean of
+    about TIMED_WORK_S of repetitions, L2 flushed before each."""
+    offsets = workloads.workload_doc_offsets(w)
+    plan = make_plan(cpa, w, offsets)
+    g = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed, device=dev, k_scale=w.k_scale, with_do=w.backward)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
+    q, k, v = (g[n][idx].contiguous() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(plan.P, w.Hq, plan.n, dtype=torch.float32, device=dev)
+    ws = cpa.alloc_workspace(plan, device=dev)
+    stream = timer.stream
+
+    def fwd():
+        cpa.cp_attn_fwd(plan, q, k, v, o, lse, ws, stream=stream)
+
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize(dev)
+    t1 = timer(fwd, 1)
+    fwd_ms = timer(fwd, reps_for(t1, 50))
+    flops = useful_flops(w, offsets)
+    peak, plabel = tensor_peak(peaks, peak_src, fwd_ms)
+    rec = {"L": w.L, "P": w.P, "ulysses": w.ulysses, "ring": w.ring, "layout": LAYOUT_NAMES[w.layout],
+           "docs": 0 if offsets is None else len(offsets) - 1, "useful_flops_fwd": flops,
+           "fwd_ms": round(fwd_ms, 4), "fwd_tflops": round(flops / fwd_ms / 1e9, 2),
+           "fwd_frac": round(flops / fwd_ms / 1e9 / peak, 4), "peak": peak, "peak_source": plabel,
+           "tokens_per_s": round(w.L / (fwd_ms * 1e-3), 1),
+           "step": "emit-partials + merge" if w.emit_partials else
+                   ("reshard in, attention, reshard out" if w.ulysses > 1 else "attention (fused merge)")}
+    if w.backward:
+        do = g["do"][idx].contiguous()
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        ws_b = cpa.alloc_workspace(plan, cpa.CP_OP_BWD, device=dev)
+
+        def bwd():
+            cpa.cp_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws_b, stream=stream)
+
+        for _ in range(2):
+            bwd()
+        torch.cuda.synchronize(dev)
+        bwd_ms = timer(bwd, reps_for(timer(bwd, 1), 30))
+        bflops = flops * BWD_FLOP_RATIO
+        bpeak, bplabel = tensor_peak(peaks, peak_src, bwd_ms)
+        rec.update({"bwd_ms": round(bwd_ms, 4), "bwd_tflops": round(bflops / bwd_ms / 1e9, 2),
+                    "bwd_frac": round(bflops / bwd_ms / 1e9 / bpeak, 4), "bwd_peak_source": bplabel,
+                    "fwd_bwd_ms": round(fwd_ms + bwd_ms, 4),
+                    "fwd_bwd_tflops": round((flops + bflops) / (fwd_ms + bwd_ms) / 1e9, 2)})
+        del do, dq, dk, dv, ws_b
+    if cpa.cp_get_status(stream) != 0:
+        raise RuntimeError(f"device status set while measuring {w.name}")
+    del q, k, v, o, lse, ws, g
+    torch.cuda.empty_cache()
+    return rec
+
+
 # ---------------------------------------------------------------------------- main
 
 
@@ -239,6 +398,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the measurements of the other four workloads after the main one")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-hash", action="store_true", help="skip the SHA-256 of the inputs")
     ap.add_argument("--layout", choices=["workload", "contiguous", "zigzag", "balanced"], default="workload",
                     help="token layout of the ring shards (default: the workload's own)")
     ap.add_argument("--chunks-per-rank", type=int, default=8, help="chunks per ring rank of the balanced layout")
@@ -279,9 +442,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
 
-    plan = cpa.Plan(w.L, w.Hq, w.Hkv, w.d, ulysses_degree=w.ulysses, ring_degree=w.ring, layout=w.layout,
-                    doc_offsets=offsets, emit_partials=w.emit_partials, chunks_per_rank=args.chunks_per_rank,
-                    kv_exchange=cpa.CP_KV_ALLGATHER if args.kv_exchange == "allgather" else cpa.CP_KV_RING)
+    plan = make_plan(cpa, w, offsets, args.chunks_per_rank, args.kv_exchange)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
     # each rank draws its own sequence.
     g_inputs = workloads.make_inputs(w.L, w.Hq, w.Hkv, w.d, w.seed + 7919 * rank, device=dev, k_scale=w.k_scale,
@@ -299,6 +460,7 @@ def main():
         ws_bwd = cpa.alloc_workspace(plan, cpa.CP_OP_BWD, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    timer = Timer(torch, dev, stream, flush)
     # The rates behind the secondary bounds: exp2 per SM clock (one per
     # visible pair and head) and clocks per M128 N128 K16 MMA, measured here.
     ex2_per_clk, mma_clk = cpa.cp_measure_rates(stream=stream)
@@ -343,6 +505,7 @@ def main():
     barrier()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     total_ms = sum(step_ms)
+    mean_step_ms = total_ms / max(1, args.steps)
     if cpa.cp_get_status(stream) != 0:
         raise RuntimeError("device status set during the timed region")
 
@@ -358,72 +521,73 @@ def main():
     set0 = {"q": q, "k": k, "v": v, "o": o, "lse": lse}
     if w.backward:
         set0.update(do=do, dq=dq, dk=dk, dv=dv)
-    sets = [set0, {n: torch.empty_like(t) for n, t in set0.items()}]
-    host_in = {n: set0[n].cpu().pin_memory() for n in in_names}
-    host_out = [{n: torch.empty(set0[n].shape, dtype=set0[n].dtype).pin_memory() for n in out_names}
-                for _ in range(2)]
-
-    def step_on(b):
-        S = sets[b]
-        cpa.cp_attn_fwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], ws, stream=stream)
-        if w.backward:
-            cpa.cp_attn_bwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], S["do"], S["dq"], S["dk"], S["dv"],
-                            ws_bwd, stream=stream)
-
-    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
-
-    def pipelined(nsteps):
-        s_h2d.wait_stream(stream)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e0.record(s_h2d)
-        for i in range(nsteps):
-            b = i % 2
-            if i >= 2:
-                s_h2d.wait_event(ev_comp[b])     # step i-2 no longer reads these inputs
-            with torch.cuda.stream(s_h2d):
-                for n in in_names:
-                    sets[b][n].copy_(host_in[n], non_blocking=True)
-            ev_in[b].record(s_h2d)
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_out[b])     # step i-2's results have left these buffers
-            step_on(b)
-            ev_comp[b].record(stream)
-            s_d2h.wait_event(ev_comp[b])
-            with torch.cuda.stream(s_d2h):
-                for n in out_names:
-                    host_out[b][n].copy_(sets[b][n], non_blocking=True)
-            ev_out[b].record(s_d2h)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e1.record(s_d2h)                         # after the last copy, which follows everything
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1)
-
-    def serial_step():
-        for n in in_names:
-            set0[n].copy_(host_in[n], non_blocking=True)
-        step_on(0)
-        for n in out_names:
-            host_out[0][n].copy_(set0[n], non_blocking=True)
-
-    e2e_steps = max(3, min(args.steps, 10))
-    pipelined(2)
-    barrier()
-    e2e_ms = pipelined(e2e_steps) / e2e_steps
-    for _ in range(2):
-        serial_step()
-    barrier()
-    ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ee0.record(stream)
-    for _ in range(e2e_steps):
-        serial_step()
-    ee1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_serial_ms = ee0.elapsed_time(ee1) / e2e_steps
-    h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in in_names)
+    e2e_steps = reps_for(mean_step_ms, 10)
+    e2e_ms = e2e_serial_ms = float("nan")
+    h2d = sum(set0[n].numel() * set0[n].element_size() for n in in_names)
     d2h = sum(set0[n].numel() * set0[n].element_size() for n in out_names)
-    del sets[1]
+    if not args.no_e2e:
+        sets = [set0, {n: torch.empty_like(t) for n, t in set0.items()}]
+        host_in = {n: set0[n].cpu().pin_memory() for n in in_names}
+        host_out = [{n: torch.empty(set0[n].shape, dtype=set0[n].dtype).pin_memory() for n in out_names}
+                    for _ in range(2)]
+
+        def step_on(b):
+            S = sets[b]
+            cpa.cp_attn_fwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], ws, stream=stream)
+            if w.backward:
+                cpa.cp_attn_bwd(plan, S["q"], S["k"], S["v"], S["o"], S["lse"], S["do"], S["dq"], S["dk"], S["dv"],
+                                ws_bwd, stream=stream)
+
+        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+        def pipelined(nsteps):
+            s_h2d.wait_stream(stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(s_h2d)
+            for i in range(nsteps):
+                b = i % 2
+                if i >= 2:
+                    s_h2d.wait_event(ev_comp[b])     # step i-2 no longer reads these inputs
+                with torch.cuda.stream(s_h2d):
+                    for n in in_names:
+                        sets[b][n].copy_(host_in[n], non_blocking=True)
+                ev_in[b].record(s_h2d)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_out[b])     # step i-2's results have left these buffers
+                step_on(b)
+                ev_comp[b].record(stream)
+                s_d2h.wait_event(ev_comp[b])
+                with torch.cuda.stream(s_d2h):
+                    for n in out_names:
+                        host_out[b][n].copy_(sets[b][n], non_blocking=True)
+                ev_out[b].record(s_d2h)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(s_d2h)                         # after the last copy, which follows everything
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1)
+
+        def serial_step():
+            for n in in_names:
+                set0[n].copy_(host_in[n], non_blocking=True)
+            step_on(0)
+            for n in out_names:
+                host_out[0][n].copy_(set0[n], non_blocking=True)
+
+        pipelined(2)
+        barrier()
+        e2e_ms = pipelined(e2e_steps) / e2e_steps
+        serial_step()
+        barrier()
+        ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ee0.record(stream)
+        for _ in range(e2e_steps):
+            serial_step()
+        ee1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_serial_ms = ee0.elapsed_time(ee1) / e2e_steps
+        del sets, host_in, host_out
 
     # ---- per-kernel breakdown (the dominant kernel's roofline)
     kern = {}
@@ -439,30 +603,18 @@ def main():
         if args.kv_exchange == "allgather":  # the attention alone reads the gathered K/V (position order)
             kh, vh = g_inputs["k"], g_inputs["v"]
 
-    def timed(fn, reps):
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            ts.append(a.elapsed_time(b))
-        return statistics.mean(ts)
-
-    reps = max(3, min(args.steps, 10))
-    attn_ms = timed(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
-    kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9}
+    reps = reps_for(mean_step_ms, 10)
+    attn_ms = timer(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
+    kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9, "reps": reps}
     if U == 1 and not w.emit_partials:
         # Each ring rank's share alone (cp_attn_fwd_rank): the forward time of
         # one GPU per rank, communication aside, is the slowest rank's.
-        per_rank = [timed(lambda r=r: cpa.cp_attn_fwd_rank(plan, r, q, kh, vh, o, lse, stream=stream), reps)
+        per_rank = [timer(lambda r=r: cpa.cp_attn_fwd_rank(plan, r, q, kh, vh, o, lse, stream=stream), reps)
                     for r in range(R)]
         kern["attn_fwd_per_rank"] = {"ms": [round(t, 4) for t in per_rank], "max_ms": max(per_rank),
                                      "max_over_mean": max(per_rank) / statistics.mean(per_rank)}
     if w.backward:
-        bwd_ms = timed(bwd, reps)
+        bwd_ms = timer(bwd, reps)
         kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,
                             "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"
                                        + (" and 2 batched Ulysses reshards (6 tensors in, 3 out)" if U > 1 else "")}
@@ -481,10 +633,11 @@ def main():
                                       stream=stream)
         bytes_in = 2 * 2 * w.L * w.d * (w.Hq + 2 * w.Hkv)
         bytes_out = 2 * (2 * w.L * w.d * w.Hq + 4 * w.L * w.Hq)
-        t_in = timed(rin, reps)
-        t_out = timed(rout, reps)
+        t_in = timer(rin, 10)
+        t_out = timer(rout, 10)
         kern["reshard_seq_to_head"] = {"ms": t_in, "gbs": bytes_in / t_in / 1e6, "bytes": bytes_in}
         kern["reshard_head_to_seq"] = {"ms": t_out, "gbs": bytes_out / t_out / 1e6, "bytes": bytes_out}
+    del qh, kh, vh, oh, lh
 
     # Standalone LSE merge at one ring rank's shape of the 64K ring workload
     # (8 ring-step partials of 8192 rows x 32 heads x 128): HBM-bound.
@@ -493,7 +646,7 @@ def main():
     lse_parts = torch.randn(mp, mh, mr, dtype=torch.float32, device=dev)
     o_m = torch.empty(mr, mh, md, dtype=torch.bfloat16, device=dev)
     lse_m = torch.empty(mh, mr, dtype=torch.float32, device=dev)
-    t_merge = timed(lambda: cpa.cp_merge_lse(mp, mr, mh, md, o_parts, lse_parts, o_m, lse_m, stream=stream), reps)
+    t_merge = timer(lambda: cpa.cp_merge_lse(mp, mr, mh, md, o_parts, lse_parts, o_m, lse_m, stream=stream), 10)
     merge_bytes = mp * mr * mh * (4 * md + 4) + mr * mh * (2 * md + 4)
     kern["merge_8x8192x32x128"] = {"ms": t_merge, "gbs": merge_bytes / t_merge / 1e6, "bytes": merge_bytes}
     del o_parts, lse_parts, o_m, lse_m
@@ -501,6 +654,32 @@ def main():
     peaks, peak_src = load_peaks()
     total_ms, e2e_ms_max, e2e_serial_ms_max, attn_ms_max = max_over_ranks(
         [total_ms, e2e_ms, e2e_serial_ms, attn_ms], dist, dev)
+
+    # Host copies of the global-order inputs: their SHA-256 and the oracle's
+    # sample (rank 0 only).
+    meta = None
+    cpu = None
+    if rank == 0:
+        meta = run_metadata(dev, w)
+        meta["seed"] = w.seed + 7919 * rank
+        want_baseline = world == 1 and not args.no_cpu_baseline
+        if want_baseline or not args.no_hash:
+            cpu = {n: t.cpu() for n, t in g_inputs.items()}
+        if not args.no_hash:
+            meta["input_sha256"] = sha256_tensors(cpu)
+            meta["input_sha256_of"] = "global-order bf16 tensors as drawn (before sharding), raw bytes"
+
+    # Free the main workload before the others are measured.
+    del q, k, v, o, lse, ws, g_inputs, set0
+    if w.backward:
+        del do, dq, dk, dv, ws_bwd
+    torch.cuda.empty_cache()
+    per_config = {}
+    if not args.no_per_config and not args.L and rank == 0:
+        for ow in workloads.WORKLOADS:
+            if ow.name == w.name:
+                continue
+            per_config[ow.name] = measure_other_workload(cpa, torch, ow, dev, timer, peaks, peak_src)
 
     result = None
     if rank == 0:
@@ -514,10 +693,13 @@ def main():
                              + (2 if args.kv_exchange == "allgather" else 0)
                              + ((3 + (2 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
-        # A launch of a second or more runs under the power cap: its peak is
-        # the sustained one; shorter launches are compared with the burst peak.
-        sustained = attn_ms >= SUSTAINED_MS
-        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak, plabel = tensor_peak(peaks, peak_src, attn_ms)
+        traffic, traffic_how = (None, None) if args.L else profiled_traffic(w.name)
+        roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": plabel,
+                    "traffic": traffic}
+        if traffic_how:
+            roofline["traffic_source"] = traffic_how
         result = {
             "metric": METRIC,
             "value": round(value, 3),
@@ -534,25 +716,29 @@ def main():
             "config": workload_config(w, offsets, args, world, plan.index_map()),
             "tokens_per_s": round(world * w.L / (ms_per_step * 1e-3), 1),
             "useful_flops_per_step": flops_step,
-            "e2e": {"value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
-                    "overlap": "2 device buffer sets; H2D and D2H of neighbouring steps overlap compute",
-                    "serial_value": round(world * flops_step / (e2e_serial_ms_max * 1e-3) / 1e12, 3),
-                    "serial_ms_per_step": round(e2e_serial_ms_max, 4)},
             "gpu_launches": launches_per_step * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d>" % w.d, "achieved": round(achieved, 2),
-                         "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"bf16 dense {'sustained' if sustained else 'burst'}, {peak_src}",
-                         "traffic": None if args.L else profiled_traffic(w.name)},
-            "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
-                        for k, v in kern.items()},
+            "roofline": roofline,
+            "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v_.items()}
+                        for k_, v_ in kern.items()},
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "secondary": secondary_bounds(ex2_per_clk, mma_clk, n_sm, clock_rec, w.d),
             "clocks": clock_rec,
             "wall_s_timed": round(t_wall, 3),
         }
-        if world == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(w, g_inputs, offsets)
+        if not args.no_e2e:
+            result["e2e"] = {
+                "value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
+                "steps": e2e_steps,
+                "overlap": "2 device buffer sets; H2D and D2H of neighbouring steps overlap compute",
+                "serial_value": round(world * flops_step / (e2e_serial_ms_max * 1e-3) / 1e12, 3),
+                "serial_ms_per_step": round(e2e_serial_ms_max, 4)}
+        if per_config:
+            result["per_config"] = per_config
+        if meta is not None:
+            result["run"] = meta
+        if world == 1 and not args.no_cpu_baseline and cpu is not None:
+            result["cpu_baseline"] = cpu_baseline(w, cpu, offsets, flops_fwd)
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.barrier()
@@ -560,25 +746,31 @@ def main():
     return 0
 
 
-def cpu_baseline(w, g_inputs, offsets):
-    """The oracle, as it stands, on a bounded seeded sample of the workload."""
-    cpu = cpu_inputs(w, g_inputs)
+def cpu_baseline(w, cpu, offsets, flops_full):
+    """The oracle, as it stands, on a bounded seeded sample of the workload,
+    with the time a full run would take at the sampled rate."""
     heads = list(range(w.Hq))
-    rows = 64
+    rows = oracle_rows_per_call(w.L, 64)
     flops, el, calls = time_oracle(w, cpu, offsets, rows, heads, seed=0, min_seconds=10.0, max_calls=16)
     cores = len(os.sched_getaffinity(0))
-    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    rate = flops / el
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} x {rows} seeded random query rows x {len(heads)} heads of {w.name} "
-                      f"(fp64 numpy, {el:.1f} s)"}
+                      f"(fp64 numpy, {el:.1f} s)",
+            "sample_rows_per_s": round(calls * rows / el, 3),
+            "full_run_flops": flops_full,
+            "full_run_s_extrapolated": round(flops_full / rate, 1),
+            "full_run_note": "extrapolated: the full forward's useful FLOPs at the sampled rate, not a measured run"}
 
 
 def run_reference(args, w, offsets, flops_step, warmup, world):
     """The CPU oracle as the reference arm: each step is a bounded sample (a
-    fixed number of seeded random query rows over all heads)."""
+    fixed number of seeded random query rows over all heads, fewer rows at
+    longer L so that a step stays near a second or two)."""
     import oracle
     cpu = cpu_inputs(w)
     heads = list(range(w.Hq))
-    rows = 16 if w.L >= 65536 else 32
+    rows = oracle_rows_per_call(w.L, 32)
     rng_seed = 0
     for i in range(warmup):
         time_oracle(w, cpu, offsets, rows, heads, seed=rng_seed + i, min_seconds=0.0, max_calls=1)

@@ -6,6 +6,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -65,16 +66,20 @@ namespace {
 
 constexpr int kTile = 128;
 
+// Device address of the status words on the current device, resolved once
+// per device (an atomic cache: concurrent first calls store the same value).
 int32_t* status_ptr() {
-  static int32_t* ptrs[64] = {nullptr};
+  static std::atomic<int32_t*> ptrs[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
+  int32_t* cached = ptrs[dev].load(std::memory_order_acquire);
+  if (!cached) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_cp_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int32_t*>(p);
+    cached = static_cast<int32_t*>(p);
+    ptrs[dev].store(cached, std::memory_order_release);
   }
-  return ptrs[dev];
+  return cached;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1091,19 +1096,24 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_noalloc_addr[kMaxDevices] = {nullptr};
+// Per-device cache of the resolved address.  Atomic, so that host threads
+// making their first call on one device at the same time are well defined:
+// each resolves the same address and stores the same value.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
 
 // Device address of g_noalloc_scratch on the current device (set-up on the
 // first call per device; nullptr if it could not be resolved).
 void* noalloc_scratch_addr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_noalloc_addr[dev]) {
+  void* cached = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!cached) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_noalloc_addr[dev] = ptr;
+    g_noalloc_addr[dev].store(ptr, std::memory_order_release);
+    cached = ptr;
   }
-  return g_noalloc_addr[dev];
+  return cached;
 }
 
 }  // namespace

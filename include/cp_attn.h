@@ -329,7 +329,8 @@ int cp_measure_rates(double *out2, cudaStream_t stream);
  *  - Every GPU that loads the library holds the array until the process exits.
  *  - The first call on a device resolves the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The per-device address cache is atomic, so
+ *    first calls from several host threads at once are safe.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
  *    (different streams, no ordering between them) race on it.  Every
  *    partial a call reads was written earlier by the same call, so nothing

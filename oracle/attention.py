@@ -196,7 +196,7 @@ def attention_bwd(q, k, v, do, offsets=None, causal=True, scale=None):
 
 
 def attention_bwd_rows(q, k, v, do, q_rows=(), key_rows=(), offsets=None, causal=True, scale=None,
-                       q_heads=None, kv_heads=None):
+                       q_heads=None, kv_heads=None, row_block=None):
     """Selected gradient rows, fp64, from the same definition as
     attention_bwd: dQ at query rows ``q_rows`` for ``q_heads`` and dK, dV at
     key rows ``key_rows`` for ``kv_heads`` (global order, positions 0..L-1).
@@ -205,9 +205,13 @@ def attention_bwd_rows(q, k, v, do, q_rows=(), key_rows=(), offsets=None, causal
     query head h and KV head j = floor(h/G), with P = exp(S - LSE) over the
     visible pairs, dP = dO V^T, D = rowsum(dO * O), dS = P (dP - D):
     dQ_i = scale sum_k dS_ik K_k,  dV_k = sum_h sum_i P_ik dO_i,
-    dK_k = scale sum_h sum_i dS_ik Q_i.  The queries that see a key are
-    all later positions of its document, so key rows near a document's end
-    are cheap.  Returns (dq [nq, len(q_heads), d], dk, dv [nk, len(kv_heads), d]).
+    dK_k = scale sum_h sum_i dS_ik Q_i.  A dQ row needs P and dS against
+    every key; a dK/dV row needs them only in its own column, for every
+    query that sees the key (all later positions of its document), so P and
+    dS are formed only for those columns.  Query rows are taken
+    ``row_block`` at a time (default: about 2^24 scores per block) to bound
+    memory; rows are independent, so this is the definition itself.
+    Returns (dq [nq, len(q_heads), d], dk, dv [nk, len(kv_heads), d]).
     """
     L, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -221,33 +225,37 @@ def attention_bwd_rows(q, k, v, do, q_rows=(), key_rows=(), offsets=None, causal
     dk = np.zeros((len(key_rows), len(kv_heads), d))
     dv = np.zeros((len(key_rows), len(kv_heads), d))
     all_pos = np.arange(L)
+    blk = row_block or max(1, min(1024, (1 << 24) // max(L, 1)))
 
-    def row_terms(rows, h):
-        """P, dS over all keys for query rows `rows` of head h."""
+    def row_terms(rows, h, cols):
+        """P, dS of query rows `rows` of head h against the keys `cols`."""
         j = h // G
         O, LSE = attention_rows(q, k, v, rows=rows, offsets=offsets, causal=causal, scale=scale, heads=[h])
-        Kj, Vj = _f64(k[:, j, :]), _f64(v[:, j, :])
+        Kc, Vc = _f64(k[cols, j, :]), _f64(v[cols, j, :])
         Qr, dOr = _f64(q[rows, h, :]), _f64(do[rows, h, :])
-        M = visible(rows, all_pos, offsets, causal)
-        S = sc * (Qr @ Kj.T)
+        M = visible(rows, cols, offsets, causal)
+        S = sc * (Qr @ Kc.T)
         P = np.where(M, np.exp(S - LSE[0][:, None]), 0.0)
-        dP = dOr @ Vj.T
+        dP = dOr @ Vc.T
         D = (dOr * O[:, 0, :]).sum(axis=1)
         dS = P * (dP - D[:, None])
-        return P, dS, Qr, dOr, Kj
+        return P, dS, Qr, dOr, Kc
 
     if len(q_rows):
         for hi, h in enumerate(q_heads):
-            _, dS, _, _, Kj = row_terms(q_rows, h)
-            dq[:, hi, :] = sc * (dS @ Kj)
+            for b0 in range(0, len(q_rows), blk):
+                rb = q_rows[b0:b0 + blk]
+                _, dS, _, _, Kc = row_terms(rb, h, all_pos)
+                dq[b0:b0 + len(rb), hi, :] = sc * (dS @ Kc)
     if len(key_rows):
         vis = visible(all_pos, key_rows, offsets, causal)          # [L, nk]: query sees key
         need = np.nonzero(vis.any(axis=1))[0]
         for ji, j in enumerate(kv_heads):
             for h in range(j * G, (j + 1) * G):
-                P, dS, Qr, dOr, _ = row_terms(need, h)
-                dv[:, ji, :] += P[:, key_rows].T @ dOr
-                dk[:, ji, :] += sc * (dS[:, key_rows].T @ Qr)
+                for b0 in range(0, len(need), blk):
+                    P, dS, Qr, dOr, _ = row_terms(need[b0:b0 + blk], h, key_rows)
+                    dv[:, ji, :] += P.T @ dOr
+                    dk[:, ji, :] += sc * (dS.T @ Qr)
     return dq, dk, dv
 
 

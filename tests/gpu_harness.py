@@ -3,6 +3,9 @@ sequence-sharded layout with the plan's index map, call the C ABI, and map
 the outputs back to global order.  (Input arrangement and comparison only.)"""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -109,10 +112,38 @@ def bwd(plan: cpa.Plan, q_g, k_g, v_g, do_g, device="cuda"):
     return out
 
 
+def rms_tolerance(ref: np.ndarray):
+    """The stricter gradient bounds proposed for comparison, scaled by the
+    tensor's RMS only: max-abs <= 1e-2 * max(1, RMS(ref)) and
+    mean-abs <= 1e-3 * max(1, RMS(ref))."""
+    rms = float(np.sqrt(np.mean(np.square(ref))))
+    return 1e-2 * max(1.0, rms), 1e-3 * max(1.0, rms)
+
+
+def record_grad_errors(what, name, err: np.ndarray, ref: np.ndarray):
+    """Append the observed gradient errors, beside both tolerance forms, to
+    the JSON-lines file named by CP_GRAD_ERR_LOG (if set)."""
+    path = os.environ.get("CP_GRAD_ERR_LOG")
+    if not path:
+        return
+    mx_tol, mean_tol = grad_tolerance(ref)
+    rmx_tol, rmean_tol = rms_tolerance(ref)
+    rec = {"case": what, "tensor": name, "n": int(err.size), "max_err": float(err.max()),
+           "mean_err": float(err.mean()), "max_ref": float(np.abs(ref).max()),
+           "rms_ref": float(np.sqrt(np.mean(np.square(ref)))), "tol_max": mx_tol, "tol_mean": mean_tol,
+           "rms_tol_max": rmx_tol, "rms_tol_mean": rmean_tol,
+           "passes_rms_form": bool(err.max() <= rmx_tol and err.mean() <= rmean_tol)}
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
 def assert_grads_close(got, ref, what=""):
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         g = np.asarray(g, dtype=np.float64)
+        if g.size == 0:
+            continue
         e = np.abs(g - r)
+        record_grad_errors(what, name, e, r)
         mx_tol, mean_tol = grad_tolerance(r)
         at = np.unravel_index(np.argmax(e), e.shape)
         assert e.max() <= mx_tol and e.mean() <= mean_tol, \

@@ -414,11 +414,13 @@ def pin_backward_rows_autograd(orc):
         vt.repeat_interleave(G, 1).permute(1, 0, 2)[None], attn_mask=m, scale=1 / math.sqrt(d))
     (o[0].permute(1, 0, 2) * torch.from_numpy(do)).sum().backward()
     qr, kr = [0, 5, 9, 10, 22], [0, 3, 9, 12, 21, 22]
-    dq, dk, dv = orc.attention_bwd_rows(q, k, v, do, q_rows=qr, key_rows=kr, offsets=offs, q_heads=[1, 3],
-                                        kv_heads=[1])
-    np.testing.assert_allclose(dq, qt.grad.numpy()[qr][:, [1, 3]], rtol=1e-9, atol=1e-11)
-    np.testing.assert_allclose(dk, kt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
-    np.testing.assert_allclose(dv, vt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
+    # Default blocking, and two rows per block (several blocks, a ragged last one).
+    for blk in (None, 2):
+        dq, dk, dv = orc.attention_bwd_rows(q, k, v, do, q_rows=qr, key_rows=kr, offsets=offs, q_heads=[1, 3],
+                                            kv_heads=[1], row_block=blk)
+        np.testing.assert_allclose(dq, qt.grad.numpy()[qr][:, [1, 3]], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(dk, kt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(dv, vt.grad.numpy()[kr][:, [1]], rtol=1e-9, atol=1e-11)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

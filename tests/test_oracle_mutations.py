@@ -25,7 +25,7 @@ MUTATIONS = {
     "doc_boundary": ('idx = np.searchsorted(offsets, pos, side="right") - 1', 'idx = np.searchsorted(offsets, pos, side="left") - 1'),
     "bwd_sign": ("dS = P * (dP - D[:, None])\n        dq[:, h, :]", "dS = P * (dP + D[:, None])\n        dq[:, h, :]"),
     "bwd_rows_sign": ("dS = P * (dP - D[:, None])\n        return", "dS = P * (dP + D[:, None])\n        return"),
-    "bwd_rows_dv_operand": ("dv[:, ji, :] += P[:, key_rows].T @ dOr", "dv[:, ji, :] += P[:, key_rows].T @ Qr"),
+    "bwd_rows_dv_operand": ("dv[:, ji, :] += P.T @ dOr", "dv[:, ji, :] += P.T @ Qr"),
     "bwd_gqa_overwrite": ("dk[:, j, :] += sc * (dS.T @ q[:, h, :])", "dk[:, j, :] = sc * (dS.T @ q[:, h, :])"),
     "bwd_dropped_scale": ("dq[:, h, :] = sc * (dS @ k[:, j, :])", "dq[:, h, :] = (dS @ k[:, j, :])"),
     "balanced_ascending": ("key=lambda j: (-int(work[j]), j)", "key=lambda j: (int(work[j]), j)"),
