@@ -409,6 +409,9 @@ def main():
                     help="how ranks obtain the other ranks' K/V (all-gather: ring plans with U == 1 only)")
     ap.add_argument("--backward", action="store_true",
                     help="add the backward to every step (the ring fwd+bwd workload always has it)")
+    ap.add_argument("--transport", action="store_true",
+                    help="with one GPU: run the multi-GPU ring-transport step (per-step launches, chunks "
+                         "rotated through a loopback) instead of the single-launch step")
     ap.add_argument("--L", type=int, default=0,
                     help="override the workload's sequence length (small cases for profiling); 0 keeps it")
     args = ap.parse_args()
@@ -441,6 +444,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
+    if (world > 1 or args.transport) and transport_eligible(w, args, world):
+        return run_transport(args, w, offsets, flops_fwd, flops_step, warmup, world, rank, dev, dist)
 
     plan = make_plan(cpa, w, offsets, args.chunks_per_rank, args.kv_exchange)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
@@ -739,6 +744,182 @@ def main():
             result["run"] = meta
         if world == 1 and not args.no_cpu_baseline and cpu is not None:
             result["cpu_baseline"] = cpu_baseline(w, cpu, offsets, flops_fwd)
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def transport_eligible(w, args, world) -> bool:
+    """One sequence over `world` GPUs through the ring transport: ring plans
+    (no emit-partials, no all-gather) whose ring degree the GPU count divides.
+    Other cases run independent replicas."""
+    return (not w.emit_partials and args.kv_exchange == "ring" and w.ring % world == 0 and not args.L)
+
+
+def run_transport(args, w, offsets, flops_fwd, flops_step, warmup, world, rank, dev, dist):
+    """N GPUs share one sequence (strong scaling): process p holds ring ranks
+    [p*R/N, (p+1)*R/N) with all their Ulysses members; the Ulysses exchange is
+    the library's reshard on the process's own slice, and the ring passes
+    K/V chunks (and in the backward dK/dV) between processes through
+    context_long_sequence_gb300.transport (NCCL point-to-point)."""
+    import torch
+    import context_long_sequence_gb300 as cpa
+    from context_long_sequence_gb300 import transport as tr
+    R, U, Rl = w.ring, w.ulysses, w.ring // world
+    T, d = w.L // R, w.d
+    plan = make_plan(cpa, w, offsets)
+    # The reshard geometry of this process's slice: Rl ring groups of U members.
+    local = cpa.Plan(Rl * T, w.Hq, w.Hkv, d, ulysses_degree=U, ring_degree=Rl)
+    g = workloads.make_inputs(w.L, w.Hq, w.Hkv, d, w.seed, device=dev, k_scale=w.k_scale, with_do=w.backward)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64)).to(dev)
+    sl = idx[rank * Rl * T:(rank + 1) * Rl * T]          # this process's slots (ring-rank major)
+    q, k, v = (g[n][sl].contiguous() for n in ("q", "k", "v"))
+    do = g["do"][sl].contiguous() if w.backward else None
+    del g
+    stream = torch.cuda.current_stream(dev)
+    Hl, Hkl = w.Hq // U, w.Hkv // U
+    qh = torch.empty(Rl, U, T, Hl, d, dtype=torch.bfloat16, device=dev)
+    kh = torch.empty(Rl, U, T, Hkl, d, dtype=torch.bfloat16, device=dev)
+    vh = torch.empty_like(kh)
+    oh = torch.empty_like(qh)
+    lh = torch.empty(Rl, U, Hl, T, dtype=torch.float32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(Rl * U, w.Hq, T // U, dtype=torch.float32, device=dev)
+    comm = tr.DistComm(timeout_s=600.0) if world > 1 else tr.LocalComm()
+    kern = tr.CudaRingKernels(plan, stream=stream)
+    place = tr.RingPlacement(R=R, U=U, world=world, rank=rank)
+    if w.backward:
+        doh = torch.empty_like(qh)
+        dqh = torch.empty(Rl, U, T, Hl, d, dtype=torch.float32, device=dev)
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+
+    def reshard(jobs):
+        if U > 1:
+            cpa.ulysses_reshard_batch(local, jobs, stream=stream)
+
+    def views(x):                                         # [Rl][U][T][..] per local ring rank
+        return [x[i] for i in range(Rl)]
+
+    if U == 1:                                            # head-sharded == sequence-sharded
+        qh, oh = (x.view(Rl, 1, T, x.shape[1], d) for x in (q, o))
+        lh = lse.view(Rl, 1, w.Hq, T)
+        if w.backward:
+            doh = do.view(Rl, 1, T, w.Hq, d)
+            dqh = dq.view(Rl, 1, T, w.Hq, d)
+
+    def stage_kv(extra=()):
+        """K/V (and `extra` jobs) into the head-sharded chunk buffers, which
+        the ring rotates (with U == 1 K/V travel in copies, not in the
+        caller's own buffers)."""
+        if U > 1:
+            reshard([(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, d, 2, k, kh),
+                     (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, d, 2, v, vh)] + list(extra))
+        else:
+            kh.view(k.shape).copy_(k)
+            vh.view(v.shape).copy_(v)
+
+    def step():
+        stage_kv([(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, d, 2, q, qh)])
+        kv = [(kh[i], vh[i]) for i in range(Rl)]
+        tr.ring_forward(comm, kern, place, views(qh), kv, views(oh), views(lh))
+        reshard([(cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hq, d, 2, oh, o),
+                 (cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, w.Hq, 1, 4, lh, lse)])
+        if w.backward:
+            # K/V again in their owners' buffers (the forward rotated them).
+            stage_kv([(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, d, 2, do, doh)])
+            kv = [(kh[i], vh[i]) for i in range(Rl)]
+            dkv = tr.ring_backward(comm, kern, place, views(qh), kv, views(oh), views(lh), views(doh), views(dqh))
+            dkh = torch.stack([x[0] for x in dkv]) if Rl > 1 else dkv[0][0].unsqueeze(0)
+            dvh = torch.stack([x[1] for x in dkv]) if Rl > 1 else dkv[0][1].unsqueeze(0)
+            if U > 1:
+                reshard([(cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hq, d, 4, dqh, dq),
+                         (cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hkv, d, 4, dkh, dk),
+                         (cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, w.Hkv, d, 4, dvh, dv)])
+            else:
+                dk.copy_(dkh.view(dk.shape))
+                dv.copy_(dvh.view(dv.shape))
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    barrier()
+    clocks.start()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    clock_rec = clocks.stop()
+    barrier()
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if cpa.cp_get_status(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+    # End to end: this process's input slice from pinned host memory, its
+    # output slice back, serially around each step.
+    in_t = [q, k, v] + ([do] if w.backward else [])
+    out_t = [o, lse] + ([dq, dk, dv] if w.backward else [])
+    host_in = [t.cpu().pin_memory() for t in in_t]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in out_t]
+    e2e_steps = reps_for(total_ms / args.steps, 10)
+    barrier()
+    ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ee0.record(stream)
+    for _ in range(e2e_steps):
+        for t, h in zip(in_t, host_in):
+            t.copy_(h, non_blocking=True)
+        step()
+        for t, h in zip(out_t, host_out):
+            h.copy_(t, non_blocking=True)
+    ee1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
+    if rank == 0:
+        ms_per_step = total_ms / args.steps
+        per_step_launches = ((2 if U > 1 else 0) + Rl * U * (R + 1)
+                             + ((3 if U > 1 else 0) + Rl * U * (1 + R) if w.backward else 0))
+        peaks, peak_src = load_peaks()
+        value = flops_step / (ms_per_step * 1e-3) / 1e12
+        cfg = workload_config(w, offsets, args, world, plan.index_map())
+        cfg["parallelism"] = (f"one sequence over {world} GPUs: ring transport (NCCL point-to-point), "
+                              f"{Rl} ring rank(s) x {U} Ulysses member(s) per GPU" if world > 1 else
+                              "ring transport on one GPU: per-step launches, chunks rotated through a loopback")
+        peak, plabel = tensor_peak(peaks, peak_src, ms_per_step)
+        result = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "tokens_per_s": round(w.L / (ms_per_step * 1e-3), 1), "useful_flops_per_step": flops_step,
+            "gpu_launches": per_step_launches * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<%d> (one ring step per launch)" % d,
+                         "achieved": round(value / world, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(value / world / peak, 4), "peak_source": plabel + ", per GPU",
+                         "traffic": None},
+            "e2e": {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in in_t) * world,
+                    "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in out_t) * world,
+                    "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                    "overlap": "serial per step (copy in, step, copy out) on every GPU"},
+            "clocks": clock_rec,
+        }
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.barrier()

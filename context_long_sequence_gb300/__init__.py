@@ -106,6 +106,9 @@ def _L():
     lib.cp_attn_fwd_rank.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
+    lib.cp_attn_fwd_step.argtypes = [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_bwd_delta.argtypes = [_vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_bwd_step.argtypes = [_vp, _i, _i] + [_vp] * 9 + [_vp]
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
     lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
     lib.cp_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), _vp]
@@ -124,6 +127,7 @@ def _L():
 EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_size", "ulysses_reshard",
             "ulysses_reshard_batch",
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
+            "cp_attn_fwd_step", "cp_attn_bwd_delta", "cp_attn_bwd_step",
             "cp_merge_lse", "cp_get_status", "cp_get_status_detail", "cp_debug_build", "cp_strerror",
             "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes", "cp_measure_rates"]
 
@@ -275,6 +279,23 @@ def cp_attn_bwd(plan: Plan, q, k, v, o, lse, dO, dq, dk, dv, workspace=None, wor
     _check(_L().cp_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                             _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "cp_attn_bwd")
+
+
+def cp_attn_fwd_step(plan: Plan, rank, step, q_rank, k_chunk, v_chunk, o_part, lse_part, stream=None):
+    _check(_L().cp_attn_fwd_step(plan.handle, int(rank), int(step), _ptr(q_rank), _ptr(k_chunk), _ptr(v_chunk),
+                                 _ptr(o_part), _ptr(lse_part), _stream(stream)), "cp_attn_fwd_step")
+
+
+def cp_attn_bwd_delta(plan: Plan, o_rank, do_rank, delta_rank, stream=None):
+    _check(_L().cp_attn_bwd_delta(plan.handle, _ptr(o_rank), _ptr(do_rank), _ptr(delta_rank), _stream(stream)),
+           "cp_attn_bwd_delta")
+
+
+def cp_attn_bwd_step(plan: Plan, rank, step, q_rank, do_rank, lse_rank, delta_rank, k_chunk, v_chunk, dq_rank,
+                     dk_chunk, dv_chunk, stream=None):
+    _check(_L().cp_attn_bwd_step(plan.handle, int(rank), int(step), _ptr(q_rank), _ptr(do_rank), _ptr(lse_rank),
+                                 _ptr(delta_rank), _ptr(k_chunk), _ptr(v_chunk), _ptr(dq_rank), _ptr(dk_chunk),
+                                 _ptr(dv_chunk), _stream(stream)), "cp_attn_bwd_step")
 
 
 def cp_merge_lse(n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream=None):

@@ -122,9 +122,10 @@ struct DqSmem {
 };
 
 template <typename F>
-__device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int lo_min, int qpos_last, F&& f) {
+__device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end, int lo_min,
+                                                 int qpos_last, F&& f) {
   const int nchunks = g.nchunks;
-  for (int s = 0; s < g.R; ++s) {
+  for (int s = s_begin; s < s_end; ++s) {
     const int src = (r - s + g.R) % g.R;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int cslot0 = ch * g.chunk;
@@ -164,9 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
                         it.q0 + it.len <= g.T, status))
     return;
-  [[maybe_unused]] const int rows = g.R * g.U * g.T;  // rows of Q, dO, K, V, dQ
+  const bool rank_local = args.rank_local != 0;
+  [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dQ
   const int h = blockIdx.x % Hq;
   const int a = it.a, r = a / g.U, u = a % g.U;  // rank a = ring rank r, Ulysses member u
+  const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
+  // Rank-local mode: the rank's rows start at 0, and so do the visiting chunk's.
+  const int q_row0 = rank_local ? 0 : a * g.T;
+  const int kv_sub = rank_local ? (((r - s_begin + g.R) % g.R) * g.U + u) * g.T : 0;
   const int qpos0 = slot_pos(g, r, it.q0);
   const int qpos_last = qpos0 + it.len - 1;
   if (!CP_IN_BOUNDS(qpos0 >= 0 && qpos_last < g.L, status)) return;
@@ -210,15 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(DQ_QD_FULL), 2 * SM::kT);
-      const int qrow = a * g.T + it.q0;
+      const int qrow = q_row0 + it.q0;
       (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows, status);
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
         tma_load_2d(sDO + hh * HALF_BYTES, &tm_do, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
       }
       int nk = 0, nv = 0;
-      for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int kv_row, int, int) {
+      for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
+        const int kv_row = kv_row_all - kv_sub;
         const int ks = nk % kKStages, vs = nv % kVStages;
         if (!mbar_wait(bar(DQ_K_EMPTY + ks), ((nk / kKStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(DQ_K_FULL + ks), SM::kT);
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int n = 0;
       if (warp_all(mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status))) {
-        for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int, int) {
+        for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) {
           if (warp_all(*abort_flag != 0)) return;
           const int ks = n % kKStages, vs = n % kVStages, sb = n & 1;
           if (!warp_all(mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status))) return;
@@ -300,14 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = row < it.len;
     const int my_pos = row_valid ? qpos0 + row : -1;
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
-    const size_t lrow = (static_cast<size_t>(a) * Hq + h) * g.T + it.q0 + row;
+    const size_t lrow = (static_cast<size_t>(rank_local ? 0 : a) * Hq + h) * g.T + it.q0 + row;
     const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rows) * Hq, status);
     const float lse2 = (row_valid && ld_ok) ? args.lse[lrow] * kLog2e : INFINITY;
     const float dlt = (row_valid && ld_ok) ? args.delta[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
     int n = 0;
     bool ok = true;
-    for_each_kv_tile(g, r, u, lo_min, qpos_last, [&](int, int kpos0, int klen) {
+    for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int kpos0, int klen) {
       if (!ok) return;
       const int sb = n & 1;
       ok = warp_all(mbar_wait(bar(DQ_S_FULL + sb), (n >> 1) & 1, abort_flag, status));
@@ -384,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_all(mbar_wait(bar(DQ_DONE), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
-    if (ok) {
-      float* dst = args.dq + (static_cast<size_t>(a * g.T + it.q0 + row) * Hq + h) * D;
-      const bool store_ok = !row_valid || CP_IN_BOUNDS(a * g.T + it.q0 + row < rows, status);
+    // Accumulate mode adds to dQ (nothing to add when no key tile was seen).
+    if (ok && !(args.accumulate && n == 0)) {
+      float* dst = args.dq + (static_cast<size_t>(q_row0 + it.q0 + row) * Hq + h) * D;
+      const bool store_ok = !row_valid || CP_IN_BOUNDS(q_row0 + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32];
         if (n > 0) {
@@ -396,11 +404,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!row_valid || !store_ok) continue;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + c4 * 32 + e) =
-              n > 0 ? make_float4(__uint_as_float(v[e]) * g.scale, __uint_as_float(v[e + 1]) * g.scale,
-                                  __uint_as_float(v[e + 2]) * g.scale, __uint_as_float(v[e + 3]) * g.scale)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 32; e += 4) {
+          float4 x = n > 0 ? make_float4(__uint_as_float(v[e]) * g.scale, __uint_as_float(v[e + 1]) * g.scale,
+                                         __uint_as_float(v[e + 2]) * g.scale, __uint_as_float(v[e + 3]) * g.scale)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4* p4 = reinterpret_cast<float4*>(dst + c4 * 32 + e);
+          if (args.accumulate) {
+            const float4 y = *p4;
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+          }
+          *p4 = x;
+        }
       }
     }
   }
@@ -435,9 +452,10 @@ struct DkvSmem {
 // Every query tile (of every ring rank, in ring order from the owner) and
 // every query head of KV head jh that may see the key tile [kpos0, hi_max].
 template <typename F>
-__device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int kpos0, int hi_max, int jh, F&& f) {
+__device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int s_begin, int s_end, int kpos0,
+                                                int hi_max, int jh, F&& f) {
   const int nchunks = g.nchunks;
-  for (int s = 0; s < g.R; ++s) {
+  for (int s = s_begin; s < s_end; ++s) {
     const int rr = (src + s) % g.R;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int cslot0 = ch * g.chunk;
@@ -461,11 +479,11 @@ struct QTile {
 
 struct QTileWalk {
   const AttnGeom& g;
-  int src, kpos0, hi_max, jh;
-  int s = 0, ch = 0, t = 0, t1 = -1, hh = 0, rr = 0, cslot0 = 0, cpos0 = 0;
+  int src, s_end, kpos0, hi_max, jh;
+  int s, ch = 0, t = 0, t1 = -1, hh = 0, rr = 0, cslot0 = 0, cpos0 = 0;
   bool in_chunk = false;
-  __device__ QTileWalk(const AttnGeom& g_, int src_, int kpos0_, int hi_max_, int jh_)
-      : g(g_), src(src_), kpos0(kpos0_), hi_max(hi_max_), jh(jh_) {}
+  __device__ QTileWalk(const AttnGeom& g_, int src_, int s_begin_, int s_end_, int kpos0_, int hi_max_, int jh_)
+      : g(g_), src(src_), s_end(s_end_), kpos0(kpos0_), hi_max(hi_max_), jh(jh_), s(s_begin_) {}
   __device__ bool next(QTile& q) {
     for (;;) {
       if (in_chunk) {
@@ -487,7 +505,7 @@ struct QTileWalk {
         ch = 0;
         ++s;
       }
-      if (s >= g.R) return false;
+      if (s >= s_end) return false;
       rr = (src + s) % g.R;
       cslot0 = ch * g.chunk;
       cpos0 = slot_pos(g, rr, cslot0);
@@ -532,9 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
                         it.q0 + it.len <= g.T, status))
     return;
-  [[maybe_unused]] const int rows = g.R * g.U * g.T;  // rows of Q, dO, K, V, dK, dV
+  const bool rank_local = args.rank_local != 0;
+  [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dK, dV
   const int jh = blockIdx.x % Hkv;
   const int a = it.a, src = a / g.U, u = a % g.U;  // key tile of rank a = ring rank src, member u
+  const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
+  // Rank-local mode: the chunk's rows start at 0, and so do the holder's.
+  const int k_row0 = rank_local ? 0 : a * g.T;
   const int kpos0 = slot_pos(g, src, it.q0);
   const int kpos_last = kpos0 + it.len - 1;
   if (!CP_IN_BOUNDS(kpos0 >= 0 && kpos_last < g.L, status)) return;
@@ -574,17 +596,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(KV_FULL), 2 * SM::kT);
-      const int krow = a * g.T + it.q0;
+      const int krow = k_row0 + it.q0;
       (void)CP_IN_BOUNDS(krow >= 0 && krow < rows, status);
       for (int hh = 0; hh < NH; ++hh) {
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
       }
       int nq = 0, ndo = 0;  // Q and dO loads issued
-      for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int rr, int qslot0, int, int, int h) {
+      for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int rr, int qslot0, int, int, int h) {
         if (*abort_flag) return;
         const int qs = nq % kQStages, ds = ndo % kDOStages;
-        const int qrow = (rr * g.U + u) * g.T + qslot0;
+        const int qrow = (rank_local ? 0 : (rr * g.U + u) * g.T) + qslot0;
         if (!mbar_wait(bar(KV_Q_EMPTY + qs), ((nq / kQStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(KV_Q_FULL + qs), SM::kT);
         (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows && h < Hq, status);
@@ -635,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int n = 0;
       if (warp_all(mbar_wait(bar(KV_FULL), 0, abort_flag, status))) {
-        for_each_q_tile(g, src, kpos0, hi_max, jh, [&](int, int, int, int, int) {
+        for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int, int, int, int, int) {
           if (warp_all(*abort_flag != 0)) return;
           if (n > 0) {
             if (!warp_all(mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status))) return;
@@ -686,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // LSE and D of the next query tile are loaded (into registers) while the
     // current one is processed, then staged in shared memory for all warps.
-    QTileWalk walk(g, src, kpos0, hi_max, jh);
+    QTileWalk walk(g, src, s_begin, s_end, kpos0, hi_max, jh);
     QTile cur, nxt;
     bool have = walk.next(cur);
     float pf_lse = 0.f, pf_del = 0.f;
@@ -694,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch = [&](const QTile& q) {
       pf_len = q.qlen;
       if (etid < q.qlen) {
-        const size_t li = (static_cast<size_t>(q.rr * g.U + u) * Hq + q.h) * g.T + q.qslot0 + etid;
+        const size_t li = (static_cast<size_t>(rank_local ? 0 : q.rr * g.U + u) * Hq + q.h) * g.T + q.qslot0 + etid;
         if (!CP_IN_BOUNDS(li < static_cast<size_t>(rows) * Hq, status)) return;
         pf_lse = args.lse[li];
         pf_del = args.delta[li];
@@ -800,9 +822,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_all(mbar_wait(bar(KV_ACC_DONE), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
-    if (ok) {
-      const size_t orow = (static_cast<size_t>(a * g.T + it.q0 + row) * Hkv + jh) * D;
-      const bool store_ok = !key_valid || CP_IN_BOUNDS(a * g.T + it.q0 + row < rows, status);
+    // Accumulate mode adds to dK and dV (nothing to add when no query tile was seen).
+    if (ok && !(args.accumulate && n == 0)) {
+      const size_t orow = (static_cast<size_t>(k_row0 + it.q0 + row) * Hkv + jh) * D;
+      const bool store_ok = !key_valid || CP_IN_BOUNDS(k_row0 + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32], k[32];
         if (n > 0) {
@@ -822,8 +845,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             fk = make_float4(__uint_as_float(k[e]) * g.scale, __uint_as_float(k[e + 1]) * g.scale,
                              __uint_as_float(k[e + 2]) * g.scale, __uint_as_float(k[e + 3]) * g.scale);
           }
-          *reinterpret_cast<float4*>(args.dv + orow + c4 * 32 + e) = fv;
-          *reinterpret_cast<float4*>(args.dk + orow + c4 * 32 + e) = fk;
+          float4* pv = reinterpret_cast<float4*>(args.dv + orow + c4 * 32 + e);
+          float4* pk = reinterpret_cast<float4*>(args.dk + orow + c4 * 32 + e);
+          if (args.accumulate) {
+            const float4 ov = *pv, ok4 = *pk;
+            fv.x += ov.x;
+            fv.y += ov.y;
+            fv.z += ov.z;
+            fv.w += ov.w;
+            fk.x += ok4.x;
+            fk.y += ok4.y;
+            fk.z += ok4.z;
+            fk.w += ok4.w;
+          }
+          *pv = fv;
+          *pk = fk;
         }
       }
     }
@@ -840,7 +876,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const AttnGeom& g = a.g;
-  const uint64_t rows = static_cast<uint64_t>(g.R) * g.U * g.T;
+  // Rows of every tensor: all ranks' slots, or (one ring step) one rank's
+  // and one chunk's T rows.
+  const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T) : static_cast<uint64_t>(g.R) * g.U * g.T;
+  const int phases = a.phases ? a.phases : 7;
   CUtensorMap mq, mdo, mk, mv;
   if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
       !make_tile_map(&mdo, a.dO, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
@@ -858,7 +897,7 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   }
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  {
+  if (phases & 1) {
     const long long warps = rows * g.Hq_loc;
     long long grid = (warps * 32 + 255) / 256;
     if (grid > sms * 16LL) grid = sms * 16LL;
@@ -874,10 +913,10 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const long long grid_kv = static_cast<long long>(a.n_items_kv) * g.Hkv_loc;
   const long long grid_q = static_cast<long long>(a.n_items_q) * g.Hq_loc;
   if (grid_kv > 0x7fffffffLL || grid_q > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
-  if (grid_kv > 0)
+  if ((phases & 2) && grid_kv > 0)
     attn_bwd_dkv_kernel<D><<<static_cast<unsigned>(grid_kv), kThreads, DkvSmem<D>::kBytes, stream>>>(mq, mdo, mk,
                                                                                                       mv, a);
-  if (grid_q > 0)
+  if ((phases & 4) && grid_q > 0)
     attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid_q), kThreads, DqSmem<D>::kBytes, stream>>>(mq, mdo, mk, mv,
                                                                                                  a);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;

@@ -177,16 +177,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int item_idx = blockIdx.x / g.Hq_loc;
   const int h = blockIdx.x % g.Hq_loc;
   if (!CP_IN_BOUNDS(item_idx < args.n_items, status)) return;
-  const WorkItem it = args.items[item_idx];
+  WorkItem it = args.items[item_idx];
+  const bool rank_local = args.rank_local != 0;  // one ring step; Q and K/V are local buffers
+  if (rank_local) it.step = args.step;
   // A work item lies inside its attention rank's slots.
   if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= 2 * BM &&
                         it.q0 + it.len <= g.T && it.step < g.R, status))
     return;
-  [[maybe_unused]] const int q_rows = g.R * g.U * g.T;              // rows of Q (and of ring-mode K/V)
-  [[maybe_unused]] const int kv_rows = g.kv_global ? g.L : q_rows;  // rows of K/V
   const int a = it.a, r = a / g.U, u = a % g.U;
   const int s_begin = it.step < 0 ? 0 : it.step;
   const int s_end = it.step < 0 ? g.R : it.step + 1;
+  // Rank-local mode: Q row a*T + t is row t of the rank's buffer, and K/V
+  // row a_src*T + t of the visiting chunk (a_src = ((r - step) mod R)*U + u)
+  // is row t of the chunk buffer.
+  const int q_row0 = rank_local ? 0 : a * g.T;
+  const int kv_sub = rank_local ? (((r - s_begin + g.R) % g.R) * g.U + u) * g.T : 0;
+  [[maybe_unused]] const int q_rows = rank_local ? g.T : g.R * g.U * g.T;       // rows of Q
+  [[maybe_unused]] const int kv_rows = rank_local ? g.T : g.kv_global ? g.L : g.R * g.U * g.T;  // rows of K/V
   const int hkv = h / g.G;
 
   // The two query tiles' windows; the block walks the keys in [lo_min of
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(BAR_Q), 2 * SM::kQ);
-      const int qrow = a * g.T + it.q0;
+      const int qrow = q_row0 + it.q0;
       for (int t = 0; t < 2; ++t) {
         (void)CP_IN_BOUNDS(t * BM >= it.len || (qrow + t * BM >= 0 && qrow + t * BM < q_rows), status);
         for (int hh = 0; hh < NH; ++hh)
@@ -240,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile barrier nt % 3 was last used by tile nt-3, whose wait is done.
       int n = 0;   // loads issued
       int nt = 0;  // key tiles issued
-      for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row, int, int) {
+      for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
+        const int kv_row = kv_row_all - kv_sub;
         const int slk = slot_of(n), slv = slot_of(n + 1);
         if (!mbar_wait(bar(BAR_KV_EMPTY + slk), parity_of(n) ^ 1, abort_flag, status)) return;
         if (!mbar_wait(bar(BAR_KV_EMPTY + slv), parity_of(n + 1) ^ 1, abort_flag, status)) return;
@@ -468,8 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = (k > 0) ? __uint_as_float(ov[e]) * inv_l : 0.f;
         if (partial) {
-          float* dst = args.o_part +
-                       ((static_cast<size_t>(r * g.R + s_begin) * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
+          const size_t part_row = rank_local ? static_cast<size_t>(q_slot)
+                                             : static_cast<size_t>(r * g.R + s_begin) * g.T + q_slot;
+          float* dst = args.o_part + (part_row * g.Hq_loc + h) * D + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         } else if (args.o_fp32) {
@@ -487,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid && CP_IN_BOUNDS(q_slot < g.T, status)) {
-        if (partial)
+        if (partial && rank_local)
+          args.lse_part[static_cast<size_t>(h) * g.T + q_slot] = lse;
+        else if (partial)
           args.lse_part[(static_cast<size_t>(r * g.R + s_begin) * g.Hq_loc + h) * g.T + q_slot] = lse;
         else
           args.lse[(static_cast<size_t>(a) * g.Hq_loc + h) * g.T + q_slot] = lse;
@@ -506,11 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_d(const FwdArgs& a, cudaStream_t stream) {
   const AttnGeom& g = a.g;
-  const uint64_t rows = static_cast<uint64_t>(g.R) * g.U * g.T;
+  // Rows of Q and of K/V: every rank's slots, or (one ring step of one rank)
+  // that rank's T rows and the visiting chunk's T rows.
+  const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T) : static_cast<uint64_t>(g.R) * g.U * g.T;
+  const uint64_t kv_rows = a.rank_local ? rows : g.kv_global ? static_cast<uint64_t>(g.L) : rows;
   CUtensorMap mq, mk, mv;
   if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
-      !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, rows) ||
-      !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, rows))
+      !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows) ||
+      !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows))
     return CP_ERR_CUDA;
   const uint32_t smem = FwdSmem<D>::kBytes;
   static bool attr_set = false;

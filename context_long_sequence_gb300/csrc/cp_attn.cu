@@ -60,6 +60,10 @@ struct cp_plan {
   int n_items_kv;
   WorkItem* d_items_rank;        // the fused list grouped by attention rank (cp_attn_fwd_rank)
   std::vector<int> rank_item_off;  // [P + 1] offsets into d_items_rank
+  WorkItem* d_items_q_rank;      // backward query tiles grouped by attention rank (cp_attn_bwd_step)
+  std::vector<int> q_rank_off;   // [P + 1]
+  WorkItem* d_items_kv_rank;     // backward key tiles grouped by owner rank (cp_attn_bwd_step)
+  std::vector<int> kv_rank_off;  // [P + 1]
 };
 
 namespace {
@@ -245,6 +249,17 @@ std::vector<WorkItem> build_kv_items(const cp_plan* p) {
   return out;
 }
 
+// A copy of `items` grouped by attention rank (stable: each group keeps the
+// list's order), with the group offsets [P + 1].
+std::vector<WorkItem> group_by_rank(const std::vector<WorkItem>& items, int P, std::vector<int>* off) {
+  std::vector<WorkItem> by_rank(items);
+  std::stable_sort(by_rank.begin(), by_rank.end(), [](const WorkItem& x, const WorkItem& y) { return x.a < y.a; });
+  off->assign(P + 1, 0);
+  for (const WorkItem& it : by_rank) ++(*off)[it.a + 1];
+  for (int a = 0; a < P; ++a) (*off)[a + 1] += (*off)[a];
+  return by_rank;
+}
+
 template <typename T>
 int upload(const std::vector<T>& h, T** d) {
   *d = nullptr;
@@ -387,6 +402,7 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
   p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = p->d_items_rank = nullptr;
+  p->d_items_q_rank = p->d_items_kv_rank = nullptr;
   p->n_items_fused = p->n_items_q = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
@@ -419,19 +435,13 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     std::vector<WorkItem> fused = build_items(p, false, 2 * kTile);
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
-    if (rc == CP_OK) {
-      // The same items grouped by rank, each group keeping the longest-first order.
-      std::vector<WorkItem> by_rank(fused);
-      std::stable_sort(by_rank.begin(), by_rank.end(), [](const WorkItem& x, const WorkItem& y) { return x.a < y.a; });
-      p->rank_item_off.assign(p->P + 1, 0);
-      for (const WorkItem& it : by_rank) ++p->rank_item_off[it.a + 1];
-      for (int a = 0; a < p->P; ++a) p->rank_item_off[a + 1] += p->rank_item_off[a];
-      rc = upload(by_rank, &p->d_items_rank);
-    }
+    // The same items grouped by rank, each group keeping the longest-first order.
+    if (rc == CP_OK) rc = upload(group_by_rank(fused, p->P, &p->rank_item_off), &p->d_items_rank);
     if (rc == CP_OK) {
       std::vector<WorkItem> qt = build_items(p, false, kTile);
       p->n_items_q = static_cast<int>(qt.size());
       rc = upload(qt, &p->d_items_q);
+      if (rc == CP_OK) rc = upload(group_by_rank(qt, p->P, &p->q_rank_off), &p->d_items_q_rank);
     }
     if (rc == CP_OK && d.emit_partials) {
       std::vector<WorkItem> steps = build_items(p, true, 2 * kTile);
@@ -442,8 +452,11 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       std::vector<WorkItem> kv = build_kv_items(p);
       p->n_items_kv = static_cast<int>(kv.size());
       rc = upload(kv, &p->d_items_kv);
+      if (rc == CP_OK) rc = upload(group_by_rank(kv, p->P, &p->kv_rank_off), &p->d_items_kv_rank);
     }
     if (rc != CP_OK) {
+      cudaFree(p->d_items_q_rank);
+      cudaFree(p->d_items_kv_rank);
       cudaFree(p->d_items_rank);
       cudaFree(p->d_chunk_pos);
       cudaFree(p->d_doc_start);
@@ -464,6 +477,8 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
 void cp_plan_destroy(cp_plan_t* p) {
   if (!p) return;
   if (p->on_device) {
+    cudaFree(p->d_items_q_rank);
+    cudaFree(p->d_items_kv_rank);
     cudaFree(p->d_items_rank);
     cudaFree(p->d_chunk_pos);
     cudaFree(p->d_doc_start);
@@ -755,6 +770,104 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
                                       {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk},
                                       {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv}};
   return cpattn::launch_reshard_batch(R, U, n, out, 3, stream, a.status);
+}
+
+int cp_attn_fwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank, const void* k_chunk,
+                     const void* v_chunk, float* o_part, float* lse_part, cudaStream_t stream) {
+  if (!p || !q_rank || !k_chunk || !v_chunk || !o_part || !lse_part) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q_rank) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(o_part) || !aligned16(lse_part))
+    return CP_ERR_ALIGNMENT;
+  if (rank < 0 || rank >= p->P || step < 0 || step >= p->desc.ring_degree) return CP_ERR_INVALID_ARG;
+  if (p->desc.kv_exchange != CP_KV_RING) return CP_ERR_UNSUPPORTED;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  cpattn::FwdArgs a{};
+  a.g = geom(p);
+  a.d = p->desc.d;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  a.q = q_rank;
+  a.k = k_chunk;
+  a.v = v_chunk;
+  a.o = o_part;  // unused in partial mode; non-null for the launcher
+  a.lse = lse_part;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.items = p->d_items_rank + p->rank_item_off[rank];
+  a.n_items = p->rank_item_off[rank + 1] - p->rank_item_off[rank];
+  a.rank_local = 1;
+  a.step = step;
+  NvtxRange call("cp_attn_fwd_step");
+  return cpattn::launch_attn_fwd(a, stream);
+}
+
+int cp_attn_bwd_delta(const cp_plan_t* p, const void* o_rank, const void* do_rank, float* delta_rank,
+                      cudaStream_t stream) {
+  if (!p || !o_rank || !do_rank || !delta_rank) return CP_ERR_INVALID_ARG;
+  if (!aligned16(o_rank) || !aligned16(do_rank) || !aligned16(delta_rank)) return CP_ERR_ALIGNMENT;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  cpattn::BwdArgs a{};
+  a.g = geom(p);
+  a.g.kv_global = 0;
+  a.o = o_rank;
+  a.dO = do_rank;
+  a.o_fp32 = p->desc.out_fp32;
+  a.delta = delta_rank;
+  // The launcher also builds the four tensor maps: point them at valid rows.
+  a.q = a.k = a.v = do_rank;
+  a.d = p->desc.d;
+  a.rank_local = 1;
+  a.phases = 1;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  NvtxRange call("cp_attn_bwd_delta");
+  return cpattn::launch_attn_bwd(a, stream);
+}
+
+int cp_attn_bwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank, const void* do_rank,
+                     const float* lse_rank, const float* delta_rank, const void* k_chunk, const void* v_chunk,
+                     float* dq_rank, float* dk_chunk, float* dv_chunk, cudaStream_t stream) {
+  if (!p || !q_rank || !do_rank || !lse_rank || !delta_rank || !k_chunk || !v_chunk || !dq_rank || !dk_chunk ||
+      !dv_chunk)
+    return CP_ERR_INVALID_ARG;
+  if (!aligned16(q_rank) || !aligned16(do_rank) || !aligned16(lse_rank) || !aligned16(delta_rank) ||
+      !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(dq_rank) || !aligned16(dk_chunk) ||
+      !aligned16(dv_chunk))
+    return CP_ERR_ALIGNMENT;
+  const int R = p->desc.ring_degree, U = p->desc.ulysses_degree;
+  if (rank < 0 || rank >= p->P || step < 0 || step >= R) return CP_ERR_INVALID_ARG;
+  if (p->desc.kv_exchange != CP_KV_RING) return CP_ERR_UNSUPPORTED;
+  int rc = check_device(p);
+  if (rc != CP_OK) return rc;
+  const int r = rank / U, u = rank % U;
+  const int a_src = ((r - step + R) % R) * U + u;  // owner of the visiting chunk
+  cpattn::BwdArgs a{};
+  a.g = geom(p);
+  a.g.kv_global = 0;
+  a.q = q_rank;
+  a.dO = do_rank;
+  a.lse = lse_rank;
+  a.delta = const_cast<float*>(delta_rank);  // read only: phases exclude the delta kernel
+  a.k = k_chunk;
+  a.v = v_chunk;
+  a.o = do_rank;  // not read (the delta phase is excluded)
+  a.dq = dq_rank;
+  a.dk = dk_chunk;
+  a.dv = dv_chunk;
+  a.items_q = p->d_items_q_rank + p->q_rank_off[rank];
+  a.n_items_q = p->q_rank_off[rank + 1] - p->q_rank_off[rank];
+  a.items_kv = p->d_items_kv_rank + p->kv_rank_off[a_src];
+  a.n_items_kv = p->kv_rank_off[a_src + 1] - p->kv_rank_off[a_src];
+  a.d = p->desc.d;
+  a.rank_local = 1;
+  a.step = step;
+  a.accumulate = step > 0;  // step 0 writes every row; later steps add
+  a.phases = 2 | 4;
+  a.status = status_ptr();
+  if (!a.status) return CP_ERR_CUDA;
+  NvtxRange call("cp_attn_bwd_step");
+  return cpattn::launch_attn_bwd(a, stream);
 }
 
 int cp_tile_classes(const cp_plan_t* p, int32_t* host_rows, int64_t capacity, int64_t* n_rows, cudaStream_t stream) {

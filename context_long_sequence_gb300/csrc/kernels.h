@@ -54,6 +54,14 @@ struct FwdArgs {
   int n_items;
   int d;
   int32_t* status;
+  // rank_local = 1: one ring step of one attention rank (the transport
+  // path).  Every item covers ring step `step` (its own step field is
+  // ignored); Q holds only that rank's T rows, K and V only the visiting
+  // chunk's T rows (the slots of rank (r - step) mod R); o_part
+  // [T][Hq_loc][d] and lse_part [Hq_loc][T] receive that step's normalised
+  // partial.  0 (the zero-initialised default): all ranks, as above.
+  int rank_local;
+  int step;
 };
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
@@ -80,6 +88,18 @@ struct BwdArgs {
   int n_items_kv;
   int d;
   int32_t* status;
+  // rank_local = 1: one ring step `step` (the transport path).  dq: items_q
+  // are query tiles of one attention rank a = r*U + u, whose Q, dO, LSE,
+  // delta and dq are that rank's own T-row buffers, against the visiting
+  // chunk of rank ((r - step) mod R)*U + u held in k, v (T rows).  dkv:
+  // items_kv are key tiles of the visiting chunk (its owner rank a), whose
+  // k, v, dk, dv are the chunk's T-row buffers, against the queries of the
+  // holder rank ((a/U + step) mod R)*U + u held in q, dO, lse, delta.
+  // 0 (the zero-initialised default): every rank and ring step.
+  int rank_local;
+  int step;
+  int accumulate;  // 1: dq, dk, dv += this call's contribution (else overwritten)
+  int phases;      // bit 0: delta, bit 1: dkv, bit 2: dq; 0 means all three
 };
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -248,6 +248,51 @@ int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void 
                 float *dq, float *dk, float *dv, void *workspace, size_t workspace_bytes,
                 cudaStream_t stream);
 
+/* ---- Ring steps for a transport that moves K/V chunks between processes
+ * ([MTX] "Split heads or rotate KV": each chip keeps its queries, receives
+ * the next KV chunk while it computes with the current one, and merges the
+ * partial results; in the backward the chunk's gradients travel with it).
+ * One call = one ring step s of one attention rank a = r*U + u, reading the
+ * rank's own buffers and a visiting chunk held in separate buffers (the
+ * layout each process keeps per rank):
+ *   q_rank, do_rank [T][Hq/U][d] bf16; o_rank the same (fp32 if out_fp32);
+ *   lse_rank, delta_rank [Hq/U][T] fp32;  T = L/R slots of ring rank r
+ *   k_chunk, v_chunk [T][Hkv/U][d] bf16: the slots of attention rank
+ *   a_src = ((r - s) mod R)*U + u, the chunk that visits rank a at step s.
+ * With U == 1 these are plain sequence shards; with U > 1 they are the
+ * head-sharded layout of ulysses_reshard (rows of rank a in its [T] block).
+ * Plans with CP_KV_ALLGATHER return CP_ERR_UNSUPPORTED; rank outside [0, P)
+ * or s outside [0, R) returns CP_ERR_INVALID_ARG.  No workspace. */
+
+/* Forward partial of ring step s: the normalised attention of rank a's
+ * queries over the keys of the visiting chunk that they see:
+ *   o_part [T][Hq/U][d] fp32 out, lse_part [Hq/U][T] fp32 out
+ * ((0, -inf) for rows that see none of the chunk).  Merging the R partials
+ * with cp_merge_lse in step order gives rank a's rows of cp_attn_fwd_local. */
+int cp_attn_fwd_step(const cp_plan_t *plan, int rank, int step, const void *q_rank,
+                     const void *k_chunk, const void *v_chunk, float *o_part, float *lse_part,
+                     cudaStream_t stream);
+
+/* D = rowsum(dO * O) of one rank's rows (the backward's first pass):
+ * delta_rank [Hq/U][T] fp32 out. */
+int cp_attn_bwd_delta(const cp_plan_t *plan, const void *o_rank, const void *do_rank,
+                      float *delta_rank, cudaStream_t stream);
+
+/* Backward contributions of ring step s (fp32):
+ *   dq_rank [T][Hq/U][d]: rank a's dQ, from the visiting chunk's keys;
+ *   dk_chunk, dv_chunk [T][Hkv/U][d]: the visiting chunk's dK, dV, from
+ *   rank a's queries (the buffers travel with the chunk).
+ * Step 0 (every chunk at its owner) writes all three, zeros where nothing
+ * is visible; steps s > 0 add to them.  After the R steps of every rank,
+ * rank a's dQ equals its
+ * rows of cp_attn_bwd's dq and each chunk's dk/dv equal its owner's rows of
+ * cp_attn_bwd's dk/dv (the same products; the fp32 sums are taken per ring
+ * step, so the results agree within fp32 rounding, not bit for bit). */
+int cp_attn_bwd_step(const cp_plan_t *plan, int rank, int step, const void *q_rank,
+                     const void *do_rank, const float *lse_rank, const float *delta_rank,
+                     const void *k_chunk, const void *v_chunk, float *dq_rank, float *dk_chunk,
+                     float *dv_chunk, cudaStream_t stream);
+
 /* Merge n_parts normalised attention partials over disjoint key sets
  * ([MTX] "Split heads or rotate KV": partial computation and merge):
  *   o_parts   [n_parts][rows][H][d] fp32, lse_parts [n_parts][H][rows] fp32

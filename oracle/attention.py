@@ -472,6 +472,41 @@ def ring_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True
     return np.stack(O), np.stack(LSE)
 
 
+def attention_bwd_partial(q, do, o, lse, k, v, q_pos, k_pos, offsets=None, causal=True, scale=None):
+    """Contribution of one visiting key block to the gradients, fp64: the
+    a7 formulas of attention_bwd restricted to the pairs (i, k) with query i
+    in this block (positions q_pos) and key k in the visiting block
+    (positions k_pos), using the full forward's O and LSE of the queries
+    (P = exp(S - LSE) with the saved LSE, D = rowsum(dO * O)).  This is the
+    backward of one ring step ([MTX] "Split heads or rotate KV": partial
+    results per visiting chunk; the chunk's dK, dV travel with it).
+    q, do, o [nq, Hq, d]; lse [Hq, nq]; k, v [nk, Hkv, d].
+    Returns (dq [nq, Hq, d], dk, dv [nk, Hkv, d]) to be summed over steps."""
+    q, do, o = (np.asarray(x, dtype=np.float64) for x in (_f64(q), _f64(do), _f64(o)))
+    k, v = np.asarray(_f64(k), dtype=np.float64), np.asarray(_f64(v), dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    nq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    sc = _scale_of(d, scale)
+    M = visible(np.asarray(q_pos), np.asarray(k_pos), offsets, causal)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(Hq):
+        j = h // G
+        qh, doh, kj, vj = q[:, h, :], do[:, h, :], k[:, j, :], v[:, j, :]
+        with np.errstate(invalid="ignore"):
+            P = np.where(M, np.exp(sc * (qh @ kj.T) - lse[h][:, None]), 0.0)
+        dv[:, j, :] += P.T @ doh
+        dP = doh @ vj.T
+        D = (doh * o[:, h, :]).sum(axis=1)
+        dS = P * (dP - D[:, None])
+        dq[:, h, :] = sc * (dS @ kj)
+        dk[:, j, :] += sc * (dS.T @ qh)
+    return dq, dk, dv
+
+
 def allgather_forward(q, k, v, R, layout=LAYOUT_CONTIGUOUS, offsets=None, causal=True,
                       scale=None, chunks_per_rank=4):
     """All-gather CP forward ([MTX] "Why KV comes back together": every chip

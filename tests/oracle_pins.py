@@ -395,6 +395,35 @@ def pin_backward_autograd(orc):
     np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=1e-9, atol=1e-11)
 
 
+def pin_backward_partials_sum_to_full(orc):
+    """The per-ring-step backward contributions, summed over the steps of a
+    zigzag ring with documents and GQA (dK/dV accumulated on the chunk),
+    equal the plain-definition backward (itself pinned by finite differences
+    and autograd)."""
+    L, Hq, Hkv, d, R = 36, 4, 2, 8, 3
+    offs = [0, 13, 14, 36]
+    q, k, v = _rand((L, Hq, d), 51), _rand((L, Hkv, d), 52), _rand((L, Hkv, d), 53)
+    do = _rand((L, Hq, d), 54)
+    O, LSE, dq_ref, dk_ref, dv_ref = orc.attention_bwd(q, k, v, do, offsets=offs)
+    pos = orc.ring_positions(L, R, orc.LAYOUT_ZIGZAG, offs)
+    n = L // R
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for r in range(R):
+        qi = pos[r * n:(r + 1) * n]
+        for s in range(R):
+            ki = pos[((r - s) % R) * n:(((r - s) % R) + 1) * n]
+            pq, pk, pv = orc.attention_bwd_partial(q[qi], do[qi], O[qi], LSE[:, qi], k[ki], v[ki], qi, ki,
+                                                   offsets=offs)
+            dq[qi] += pq
+            dk[ki] += pk
+            dv[ki] += pv
+    np.testing.assert_allclose(dq, dq_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, dk_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, dv_ref, rtol=1e-10, atol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -23,7 +23,8 @@ MUTATIONS = {
     "zigzag_chunk": ("(2 * R - 1 - r) * c + np.arange(c)", "(2 * R - 2 - r) * c + np.arange(c)"),
     "reshard_transposed": ("y[u, s * n:(s + 1) * n] = x[s, :, u * Hl:(u + 1) * Hl]", "y[u, s * n:(s + 1) * n] = x[u, :, s * Hl:(s + 1) * Hl]"),
     "doc_boundary": ('idx = np.searchsorted(offsets, pos, side="right") - 1', 'idx = np.searchsorted(offsets, pos, side="left") - 1'),
-    "bwd_sign": ("dS = P * (dP - D[:, None])\n        dq[:, h, :]", "dS = P * (dP + D[:, None])\n        dq[:, h, :]"),
+    "bwd_sign": ("dS = P * (dP - D[:, None])\n        dq[:, h, :] = sc * (dS @ k[:, j, :])",
+                 "dS = P * (dP + D[:, None])\n        dq[:, h, :] = sc * (dS @ k[:, j, :])"),
     "bwd_rows_sign": ("dS = P * (dP - D[:, None])\n        return", "dS = P * (dP + D[:, None])\n        return"),
     "bwd_rows_dv_operand": ("dv[:, ji, :] += P.T @ dOr", "dv[:, ji, :] += P.T @ Qr"),
     "bwd_gqa_overwrite": ("dk[:, j, :] += sc * (dS.T @ q[:, h, :])", "dk[:, j, :] = sc * (dS.T @ q[:, h, :])"),
@@ -31,6 +32,10 @@ MUTATIONS = {
     "balanced_ascending": ("key=lambda j: (-int(work[j]), j)", "key=lambda j: (int(work[j]), j)"),
     "balanced_most_loaded": ("load[r] < load[best]", "load[r] > load[best]"),
     "balanced_ignores_docs": ("per_query = pos - doc_start_of(pos, offsets) + 1", "per_query = pos + 1"),
+    "bwd_partial_sign": ("dS = P * (dP - D[:, None])\n        dq[:, h, :] = sc * (dS @ kj)",
+                         "dS = P * (dP + D[:, None])\n        dq[:, h, :] = sc * (dS @ kj)"),
+    "bwd_partial_lse_unused": ("np.exp(sc * (qh @ kj.T) - lse[h][:, None])", "np.exp(sc * (qh @ kj.T))"),
+    "bwd_partial_dk_operand": ("dk[:, j, :] += sc * (dS.T @ qh)", "dk[:, j, :] += sc * (dS.T @ doh)"),
     "lse_reshard_back": ("out[s, u * Hl:(u + 1) * Hl, :] = lse[u, :, s * n:(s + 1) * n]", "out[s, u * Hl:(u + 1) * Hl, :] = lse[s, :, u * n:(u + 1) * n]"),
 }
 
