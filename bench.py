@@ -608,6 +608,13 @@ def main():
         if args.kv_exchange == "allgather":  # the attention alone reads the gathered K/V (position order)
             kh, vh = g_inputs["k"], g_inputs["v"]
 
+    if U > 1:
+        # The attention alone reads the real head-sharded inputs (tensor-core
+        # power, and so the clock under the power cap, depends on the data).
+        cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh),
+                                         (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh),
+                                         (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, v, vh)],
+                                  stream=stream)
     reps = reps_for(mean_step_ms, 10)
     attn_ms = timer(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
     kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9, "reps": reps}

@@ -41,6 +41,7 @@
 
 #include <climits>
 #include <cmath>
+#include <type_traits>
 
 #define CP_TU_ID ::cpattn::kTuAttnBwd
 #include "debug.cuh"
@@ -105,21 +106,35 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
 
 // ---------------------------------------------------------------- dQ (query-tile outer)
 
-enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = 4, DQ_V_FULL = 7, DQ_V_EMPTY = 9, DQ_S_FULL = 11,
-             DQ_S_EMPTY = 13, DQ_DP_FULL = 15, DQ_DS_FULL = 16, DQ_DONE = 17, DQ_DRAIN = 18, DQ_NUM_BARS = 19 };
+constexpr int kKStages = 4;  // K tiles in flight (K is last read by dQ, issued a tile later)
+constexpr int kVStages = 3;  // V tiles in flight (V is read by dP only)
 
-constexpr int kKStages = 3;  // K tiles in flight (K is last read by dQ, issued a tile later)
-constexpr int kVStages = 2;  // V tiles in flight (V is read by dP only)
+enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = DQ_K_FULL + kKStages, DQ_V_FULL = DQ_K_EMPTY + kKStages,
+             DQ_V_EMPTY = DQ_V_FULL + kVStages, DQ_S_FULL = DQ_V_EMPTY + kVStages, DQ_S_EMPTY, DQ_DP_FULL,
+             DQ_DS_FULL, DQ_DONE, DQ_DRAIN, DQ_NUM_BARS };
 
+// Q and dO live in tensor memory (the A operands of S = Q K^T and dP = dO
+// V^T), so shared memory holds only the streamed K and V tiles.
 template <int D>
 struct DqSmem {
   static constexpr uint32_t kT = 128 * D * 2;
-  static constexpr uint32_t offQ = 0, offDO = kT, offK = 2 * kT, offV = offK + kKStages * kT;
+  static constexpr uint32_t offK = 0, offV = offK + kKStages * kT;
   static constexpr uint32_t offBar = offV + kVStages * kT;
   static constexpr uint32_t offMisc = offBar + 24 * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
+  static_assert(DQ_NUM_BARS <= 24, "barrier slots");
 };
+
+// S = A B^T over K = D with A in TMEM (contiguous packed columns) and B K-major
+// in shared memory.  Issued warp-wide.
+template <int D>
+__device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+  if constexpr (D == 128)
+    mma_bf16_ts_kmaj_k128_warp<HALF_BYTES>(d_tmem, a_tmem, b, idesc, 0u);
+  else
+    mma_bf16_ts_kmaj_k64_warp(d_tmem, a_tmem, b, idesc, 0u);
+}
 
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end, int lo_min,
@@ -150,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + SM::offQ, sDO = s_base + SM::offDO, sK = s_base + SM::offK, sV = s_base + SM::offV;
+  const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
@@ -181,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hkv = h / g.G;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(DQ_QD_FULL), 1);
+    mbar_init(bar(DQ_QD_FULL), 8);  // the element-wise warps, once Q and dO sit in TMEM
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(bar(DQ_K_FULL + i), 1);
       mbar_init(bar(DQ_K_EMPTY + i), 1);
@@ -190,10 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(DQ_V_FULL + i), 1);
       mbar_init(bar(DQ_V_EMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(DQ_S_FULL + i), 1);
-      mbar_init(bar(DQ_S_EMPTY + i), 8);
-    }
+    mbar_init(bar(DQ_S_FULL), 1);
+    mbar_init(bar(DQ_S_EMPTY), 8);
     mbar_init(bar(DQ_DP_FULL), 1);
     mbar_init(bar(DQ_DS_FULL), 8);
     mbar_init(bar(DQ_DONE), 1);
@@ -209,19 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM: S double-buffered (columns 0 and 384), dP (then dS, packed bf16) at 128, dQ at 256.
-  const uint32_t tdP = tmem + 128, tdQ = tmem + 256;
-  auto tS = [&](int b) { return tmem + (b ? 384u : 0u); };
+  // TMEM: S at 0, dP (then dS, packed bf16) at 128, dQ at 256, and the A
+  // operands Q at 384 and dO at 448 (D/2 packed columns each).
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tQ = tmem + 384, tdO = tmem + 448;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(DQ_QD_FULL), 2 * SM::kT);
-      const int qrow = q_row0 + it.q0;
-      (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows, status);
-      for (int hh = 0; hh < NH; ++hh) {
-        tma_load_2d(sQ + hh * HALF_BYTES, &tm_q, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
-        tma_load_2d(sDO + hh * HALF_BYTES, &tm_do, bar(DQ_QD_FULL), h * D + hh * 64, qrow);
-      }
       int nk = 0, nv = 0;
       for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
@@ -241,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       });
       if (*abort_flag) {
         // Wait for this CTA's own copies: the last loads of each stage.
-        mbar_wait(bar(DQ_QD_FULL), 0, nullptr, status);
         for (int i = max(0, nk - kKStages); i < nk; ++i)
           mbar_wait(bar(DQ_K_FULL + i % kKStages), (i / kKStages) & 1, nullptr, status);
         for (int i = max(0, nv - kVStages); i < nv; ++i)
@@ -254,14 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, D, 1);
-      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024);
       constexpr uint64_t kStep = SM::kT >> 4;  // one stage in descriptor units
-      // Issue order for key tile n: S_n (into S buffer n & 1), dQ_{n-1},
-      // dP_n.  dS stays in TMEM over the dP columns it came from and is the
-      // A operand of dQ; dP_n overwrites those columns only after dQ_{n-1},
-      // issued before it by this thread, has read them.
+      // Issue order for key tile n: S_n, dQ_{n-1}, dP_n.  S has one TMEM
+      // buffer: S_n is issued once the element-wise warps have read S_{n-1}
+      // (they finish that while dQ_{n-2} and dP_{n-1} run).  dS stays in TMEM
+      // over the dP columns it came from and is the A operand of dQ; dP_n
+      // overwrites those columns only after dQ_{n-1}, issued before it by
+      // this thread, has read them.
       auto issue_dq = [&](int m) {  // dQ += dS_m K_m
         mma_bf16_ts_k128_halves_warp(tdQ, tdP, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
                                 m > 0 ? 1u : 0u);
@@ -271,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp_all(mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status))) {
         for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) {
           if (warp_all(*abort_flag != 0)) return;
-          const int ks = n % kKStages, vs = n % kVStages, sb = n & 1;
+          const int ks = n % kKStages, vs = n % kVStages;
           if (!warp_all(mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status))) return;
-          // S buffer sb: the element-wise warps have read S_{n-2} from it.
-          if (n >= 2 && !warp_all(mbar_wait(bar(DQ_S_EMPTY + sb), ((n >> 1) & 1) ^ 1, abort_flag, status))) return;
+          // The element-wise warps have read S_{n-1}.
+          if (n >= 1 && !warp_all(mbar_wait(bar(DQ_S_EMPTY), (n - 1) & 1, abort_flag, status))) return;
           tc_fence_after();
-          mma_qk<D>(tS(sb), dQ0, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
-          mma_commit_warp(bar(DQ_S_FULL + sb));
+          mma_tk<D>(tS, tQ, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
+          mma_commit_warp(bar(DQ_S_FULL));
           if (n > 0) {
             if (!warp_all(mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status))) return;
             tc_fence_after();
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!warp_all(mbar_wait(bar(DQ_V_FULL + vs), (n / kVStages) & 1, abort_flag, status))) return;
           tc_fence_after();
-          mma_qk<D>(tdP, dDO0, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s);
+          mma_tk<D>(tdP, tdO, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s);
           mma_commit_warp(bar(DQ_DP_FULL));
           mma_commit_warp(bar(DQ_V_EMPTY + vs));
           ++n;
@@ -312,12 +318,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = (row_valid && ld_ok) ? args.lse[lrow] * kLog2e : INFINITY;
     const float dlt = (row_valid && ld_ok) ? args.delta[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
+    {
+      // This thread's half of its Q and dO rows into TMEM (lane = row; the
+      // bf16 pairs of a row in memory order are the packed columns).  Rows
+      // past the tile's end are zero.
+      constexpr int W = D / 4;  // 32-bit words per half row
+      const size_t grow = static_cast<size_t>(q_row0 + it.q0 + row) * Hq + h;
+      const bool in = row_valid && CP_IN_BOUNDS(q_row0 + it.q0 + row < rows, status);
+      const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q) + grow * D) + half * (W / 4);
+      const uint4* dsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.dO) + grow * D) + half * (W / 4);
+      uint32_t qw[W], dw[W];
+#pragma unroll
+      for (int i = 0; i < W / 4; ++i) {
+        const uint4 x = in ? qsrc[i] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 y = in ? dsrc[i] : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * i] = x.x, qw[4 * i + 1] = x.y, qw[4 * i + 2] = x.z, qw[4 * i + 3] = x.w;
+        dw[4 * i] = y.x, dw[4 * i + 1] = y.y, dw[4 * i + 2] = y.z, dw[4 * i + 3] = y.w;
+      }
+      if constexpr (D == 128) {
+        tmem_st32(tQ + lane_off + half * W, qw);
+        tmem_st32(tdO + lane_off + half * W, dw);
+      } else {
+        tmem_st16(tQ + lane_off + half * W, qw);
+        tmem_st16(tdO + lane_off + half * W, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQ_QD_FULL));
+    }
     int n = 0;
     bool ok = true;
     for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int kpos0, int klen) {
       if (!ok) return;
-      const int sb = n & 1;
-      ok = warp_all(mbar_wait(bar(DQ_S_FULL + sb), (n >> 1) & 1, abort_flag, status));
+      ok = warp_all(mbar_wait(bar(DQ_S_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
       const bool full = (klen == BN) && (kpos0 + BN - 1 <= qpos0) && (lo_max <= kpos0);
@@ -328,32 +362,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pp[BN / 4];
       const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
       uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
-      tmem_ld32(tS(sb) + lane_off + 64 * half, sr2[0]);
-      tmem_ld32(tS(sb) + lane_off + 64 * half + 32, sr2[1]);
+      tmem_ld32(tS + lane_off + 64 * half, sr2[0]);
+      tmem_ld32(tS + lane_off + 64 * half + 32, sr2[1]);
       tmem_wait_ld();
       reg_fence(sr2[0]);
       reg_fence(sr2[1]);
+      // Two instantiations: tiles wholly inside the window take the loop with
+      // no mask at all (a mask test folded into every element costs more
+      // than the rest of the loop).
+      auto phase_a = [&](auto masked) {
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c4 = 2 * half + cc;
-        const uint32_t* sr = sr2[cc];
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c4 = 2 * half + cc;
+          const uint32_t* sr = sr2[cc];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = c4 * 32 + e;
-          const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, nlse2);
-          float y0, y1;
-          split_f32x2(y, y0, y1);
-          float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
-          if (!full) {
-            if (col < c_lo || col > c_hi) x0 = 0.f;
-            if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+          for (int e = 0; e < 32; e += 2) {
+            const int col = c4 * 32 + e;
+            const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, nlse2);
+            float y0, y1;
+            split_f32x2(y, y0, y1);
+            float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
+            if constexpr (decltype(masked)::value) {
+              if (col < c_lo || col > c_hi) x0 = 0.f;
+              if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+            }
+            pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
           }
-          pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
         }
-      }
+      };
+      if (full)
+        phase_a(std::false_type{});
+      else
+        phase_a(std::true_type{});
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(DQ_S_EMPTY + sb));
+      if (lane == 0) mbar_arrive(bar(DQ_S_EMPTY));
       // Phase B: dS = P * (dP - D), packed to bf16 pairs over the dP columns
       // this warp has read (32-column chunk cc of this half -> columns
       // 64*half + 16*cc ..): the A operand of dQ.
@@ -742,27 +785,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(sr2[0]);
       reg_fence(sr2[1]);
+      // Two instantiations, as in the dQ kernel: no mask code on whole tiles.
+      auto phase_a = [&](auto masked) {
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c4 = 2 * half + cc;
-        const uint32_t* sr = sr2[cc];
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c4 = 2 * half + cc;
+          const uint32_t* sr = sr2[cc];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = c4 * 32 + e;
-          const float2 nl = ld_shared_f32x2(aLse + 4 * col);
-          const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
-                                    make_f32x2(nl.x, nl.y));
-          float y0, y1;
-          split_f32x2(y, y0, y1);
-          float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
-          if (!full) {
-            if (col < c_lo || col > c_hi) x0 = 0.f;
-            if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+          for (int e = 0; e < 32; e += 2) {
+            const int col = c4 * 32 + e;
+            const float2 nl = ld_shared_f32x2(aLse + 4 * col);
+            const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
+                                      make_f32x2(nl.x, nl.y));
+            float y0, y1;
+            split_f32x2(y, y0, y1);
+            float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
+            if constexpr (decltype(masked)::value) {
+              if (col < c_lo || col > c_hi) x0 = 0.f;
+              if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
+            }
+            pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
           }
-          pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
+          tmem_st16(tSt + lane_off + 64 * half + 16 * cc, *reinterpret_cast<const uint32_t(*)[16]>(pp + cc * 16));
         }
-        tmem_st16(tSt + lane_off + 64 * half + 16 * cc, *reinterpret_cast<const uint32_t(*)[16]>(pp + cc * 16));
-      }
+      };
+      if (full)
+        phase_a(std::false_type{});
+      else
+        phase_a(std::true_type{});
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

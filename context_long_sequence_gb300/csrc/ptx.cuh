@@ -234,6 +234,46 @@ __device__ __forceinline__ void mma_bf16_ts_k128_halves_warp(uint32_t d_tmem, ui
       : "memory");
 }
 
+// D (+)= A[tmem] * B^T with A (M=128 rows x K) in TMEM as contiguous packed
+// columns (row i in lane i, K-elements 2j, 2j+1 in column a + j, the even
+// one in the lower half): K-step kk reads columns a + 8kk..a + 8kk + 7.  B is
+// K-major in shared memory, 128-byte swizzled, its two 64-column halves HALF
+// bytes apart (the layout of mma_bf16_ss_k128_warp's B).  Eight MMAs, K = 128.
+template <uint32_t HALF>
+__device__ __forceinline__ void mma_bf16_ts_kmaj_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                           uint32_t idesc, uint32_t accumulate) {
+  constexpr uint64_t h = HALF >> 4;
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, %5;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, %6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, %7;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, %8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(h), "n"(h + 2), "n"(h + 4), "n"(h + 6)
+      : "memory");
+}
+
+// Same, K = 64 (four K=16 steps within one 64-column half of B).
+__device__ __forceinline__ void mma_bf16_ts_kmaj_k64_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all prior tcgen05 ops of the issuing
 // thread finish; executed by one elected lane of a converged warp.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {

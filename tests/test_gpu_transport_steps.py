@@ -106,12 +106,14 @@ def test_transport_forward_and_backward_on_one_gpu(cpa, case):
     O, LSE = gh.from_slots(plan, o_seq, lse_seq, idx)
     O_ref, LSE_ref = oracle.attention(inp["q"], inp["k"], inp["v"], offsets=docs)
     gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name + " transport fwd", bf16_out=True)
-    # Beside the single-launch forward: the same result within bf16 rounding.
+    # Beside the single-launch forward (fused merge): the two round P to bf16
+    # against different running maxima, so they agree within the workload
+    # bounds, not bit for bit; LSE is not rounded to bf16.
     o_f = torch.empty_like(q)
     lse_f = torch.empty(plan.P, Hq, plan.n, dtype=torch.float32, device="cuda")
     cpa.cp_attn_fwd(plan, q, k, v, o_f, lse_f, cpa.alloc_workspace(plan))
     diff = (o_seq.float() - o_f.float()).abs()
-    assert (diff <= 2.0 ** -7 * o_f.float().abs() + 1e-3).all(), float(diff.max())
+    assert float(diff.max()) <= gh.O_MAX_ABS and float(diff.mean()) <= gh.O_MEAN_ABS, float(diff.max())
     assert float((lse_seq - lse_f).abs().max()) <= 1e-5
 
     # Backward from the single-launch forward's O and LSE.
