@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c_hi = min(my_pos - kpos0, klen - 1);
       // Phase A: P = exp2(S * scale*log2e - LSE*log2e), masked, as packed bf16
       // (this warp's half of the row: 32-column chunks c4 = 2*half, 2*half+1).
-      uint32_t pp[BN / 4];
+      float pf[BN / 2];  // P of this half of the row, fp32 (dS is formed from it)
       const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
       uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
       tmem_ld32(tS + lane_off + 64 * half, sr2[0]);
@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (col < c_lo || col > c_hi) x0 = 0.f;
               if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
             }
-            pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
+            pf[cc * 32 + e] = x0;
+            pf[cc * 32 + e + 1] = x1;
           }
         }
       };
@@ -415,11 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t dsp[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const uint32_t pk = pp[cc * 16 + e / 2];
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(-dlt, -dlt));
           float s0, s1;
-          split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)), dd), s0, s1);
+          split_f32x2(mul_f32x2(make_f32x2(pf[cc * 32 + e], pf[cc * 32 + e + 1]), dd), s0, s1);
           dsp[e / 2] = pack_bf16x2(s0, s1);
         }
         tmem_st16(tdP + lane_off + 64 * half + 16 * cc, dsp);
@@ -476,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- dK, dV (key-tile outer)
 
 enum DkvBar { KV_FULL = 0, KV_Q_FULL = 1, KV_Q_EMPTY = 4, KV_DO_FULL = 7, KV_DO_EMPTY = 9, KV_S_FULL = 11,
-              KV_DP_FULL = 12, KV_P_FULL = 13, KV_DS_FULL = 14, KV_ACC_DONE = 15, KV_DRAIN = 16, KV_NUM_BARS = 17 };
+              KV_DP_FULL = 12, KV_P_FULL = 13, KV_DS_FULL = 14, KV_ACC_DONE = 15, KV_DRAIN = 16,
+              KV_LD_FULL = 17,   // +buffer: the LSE/D of a query tile are staged (4 writer warps)
+              KV_LD_EMPTY = 19,  // +buffer: every element-wise warp has read them (8 warps)
+              KV_NUM_BARS = 21 };
 
 constexpr int kQStages = 3;   // Q tiles in flight (Q is last read by dK, the last product of a tile)
 constexpr int kDOStages = 2;  // dO tiles in flight (dO is last read by dV)
@@ -486,10 +489,17 @@ struct DkvSmem {
   static constexpr uint32_t kT = 128 * D * 2;
   static constexpr uint32_t offK = 0, offV = kT, offQ = 2 * kT, offDO = offQ + kQStages * kT;
   static constexpr uint32_t offBar = offDO + kDOStages * kT;
-  static constexpr uint32_t offLD = offBar + 24 * 8;   // 128 -LSE*log2(e) + 128 -D floats
-  static constexpr uint32_t offMisc = offLD + 2 * 128 * 4;
+  static constexpr uint32_t offLD = offBar + 24 * 8;   // 2 buffers x (128 -LSE*log2(e) + 128 -D floats)
+  static constexpr uint32_t offMisc = offLD + 2 * 2 * 128 * 4;
   static constexpr uint32_t kUsed = offMisc + 16;
-  static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
+  // Up to 1 KB of slack aligns the tiles to the 128-byte swizzle's 1 KB
+  // atoms, but no more than the per-CTA limit is requested: the dynamic base
+  // is 1 KB-aligned in practice, and the kernel checks that the aligned
+  // layout fits (an error status otherwise, before anything is touched).
+  static constexpr uint32_t kMaxDyn = 227 * 1024;
+  static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024
+                                     : (kUsed + 1024 < kMaxDyn ? kUsed + 1024 : kMaxDyn);
+  static_assert(kUsed <= kMaxDyn, "dkv shared-memory layout");
 };
 
 // Every query tile (of every ring rank, in ring order from the owner) and
@@ -574,12 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (static_cast<uint32_t>(smem - smem_raw) + SM::kUsed > SM::kBytes) {
+    if (threadIdx.x == 0) record_status(args.status, CP_ERR_DEVICE_BOUNDS);
+    return;
+  }
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV, sQ = s_base + SM::offQ, sDO = s_base + SM::offDO;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
-  float* sLse = reinterpret_cast<float*>(smem + SM::offLD);  // -LSE * log2(e) per query column
-  float* sDel = sLse + 128;                                  // -D per query column
-  const uint32_t aLse = smem_u32(sLse), aDel = smem_u32(sDel);  // the same, as shared-window addresses
+  // Two buffers b of [128 -LSE * log2(e)][128 -D] per query column.
+  float* sLD = reinterpret_cast<float*>(smem + SM::offLD);
+  const uint32_t aLD = smem_u32(sLD);  // the same, as a shared-window address
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
 
@@ -622,6 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(KV_DS_FULL), 8);
     mbar_init(bar(KV_ACC_DONE), 1);
     mbar_init(bar(KV_DRAIN), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(KV_LD_FULL + i), 4);
+      mbar_init(bar(KV_LD_EMPTY + i), 8);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -766,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if (have) prefetch(cur);
-    auto process = [&](int qpos0, int qlen) {
+    auto process = [&](int qpos0, int qlen, uint32_t aLse, uint32_t aDel) {
       if (!ok) return;
       ok = warp_all(mbar_wait(bar(KV_S_FULL), n & 1, abort_flag, status));
       if (!ok) return;
@@ -777,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Phase A: P^T = exp2(S^T * scale*log2e - LSE*log2e), masked, packed to
       // bf16 pairs and written back over the S^T columns this warp has read
       // (32-column chunk cc of this half -> columns 64*half + 16*cc ..).
-      uint32_t pp[BM / 4];
+      float pf[BM / 2];  // P^T of this half of the row, fp32 (dS^T is formed from it)
       const f32x2 nsl2 = make_f32x2(sl2, sl2);
       uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
       tmem_ld32(tSt + lane_off + 64 * half, sr2[0]);
@@ -791,10 +809,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 2; ++cc) {
           const int c4 = 2 * half + cc;
           const uint32_t* sr = sr2[cc];
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int col = c4 * 32 + e;
-            const float2 nl = ld_shared_f32x2(aLse + 4 * col);
+            const float2 nl = ld_shared_f32x2(aLse + 4 * col);  // -LSE * log2(e) of query columns col, col+1
             const f32x2 y = fma_f32x2(make_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
                                       make_f32x2(nl.x, nl.y));
             float y0, y1;
@@ -804,9 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (col < c_lo || col > c_hi) x0 = 0.f;
               if (col + 1 < c_lo || col + 1 > c_hi) x1 = 0.f;
             }
-            pp[cc * 16 + e / 2] = pack_bf16x2(x0, x1);
+            pk[e / 2] = pack_bf16x2(x0, x1);
+            pf[cc * 32 + e] = x0;
+            pf[cc * 32 + e + 1] = x1;
           }
-          tmem_st16(tSt + lane_off + 64 * half + 16 * cc, *reinterpret_cast<const uint32_t(*)[16]>(pp + cc * 16));
+          tmem_st16(tSt + lane_off + 64 * half + 16 * cc, pk);
         }
       };
       if (full)
@@ -836,12 +857,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = c4 * 32 + e;
-          const uint32_t pk = pp[cc * 16 + e / 2];
-          const float2 nd = ld_shared_f32x2(aDel + 4 * col);
+          const float2 nd = ld_shared_f32x2(aDel + 4 * col);  // -D of query columns col, col+1
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(nd.x, nd.y));
           float s0, s1;
-          split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)), dd), s0, s1);
+          split_f32x2(mul_f32x2(make_f32x2(pf[cc * 32 + e], pf[cc * 32 + e + 1]), dd), s0, s1);
           dsp[e / 2] = pack_bf16x2(s0, s1);
         }
         tmem_st16(tdPt + lane_off + 64 * half + 16 * cc, dsp);
@@ -852,19 +872,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(KV_DS_FULL));
       ++n;
     };
-    while (have) {
-      // Every element-wise warp walks the same tiles and reaches both
-      // barriers on every tile, also after an abort, so they stay balanced.
-      named_bar_sync(1, 256);  // everyone finished reading the previous tile's values
+    // Staging of LSE and D through two shared buffers: warps 2-5 (etid <
+    // 128) write query tile n's values into buffer n & 1 once every warp has
+    // read that buffer's previous contents (tile n - 2), then arrive on its
+    // "full" barrier; every warp reads it after that barrier and arrives on
+    // its "empty" barrier when done.  No warp waits for all others at every
+    // tile, and every wait is bounded.
+    int ld = 0;  // query tiles staged
+    while (have && ok) {
+      const int b = ld & 1;
+      float* sL = sLD + b * 256;
       if (etid < BM) {
+        if (ld >= 2 && !(ok = warp_all(mbar_wait(bar(KV_LD_EMPTY + b), ((ld >> 1) - 1) & 1, abort_flag, status))))
+          break;
         const bool in = etid < pf_len;
-        sLse[etid] = in ? -pf_lse * kLog2e : -INFINITY;
-        sDel[etid] = in ? -pf_del : 0.f;
+        sL[etid] = in ? -pf_lse * kLog2e : -INFINITY;
+        sL[128 + etid] = in ? -pf_del : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KV_LD_FULL + b));
       }
-      named_bar_sync(1, 256);
       const bool have_next = walk.next(nxt);
       if (have_next) prefetch(nxt);
-      process(cur.qpos0, cur.qlen);
+      if (!(ok = warp_all(mbar_wait(bar(KV_LD_FULL + b), (ld >> 1) & 1, abort_flag, status)))) break;
+      const uint32_t aL = aLD + b * 1024;
+      process(cur.qpos0, cur.qlen, aL, aL + 512);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KV_LD_EMPTY + b));
+      ++ld;
       cur = nxt;
       have = have_next;
     }
