@@ -42,6 +42,7 @@ CP_TOKEN_MAJOR = 0
 CP_HEAD_MAJOR = 1
 CP_OP_FWD = 0
 CP_OP_BWD = 1
+CP_OP_BWD_RANK_STATS = 2
 
 
 CP_RESHARD_MAX_JOBS = 8
@@ -107,8 +108,8 @@ def _L():
     lib.cp_attn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.cp_attn_bwd.argtypes = [_vp] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp]
     lib.cp_attn_fwd_step.argtypes = [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]
-    lib.cp_attn_bwd_delta.argtypes = [_vp, _vp, _vp, _vp, _vp]
-    lib.cp_attn_bwd_step.argtypes = [_vp, _i, _i] + [_vp] * 9 + [_vp]
+    lib.cp_attn_bwd_delta.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
+    lib.cp_attn_bwd_step.argtypes = [_vp, _i, _i] + [_vp] * 8 + [_vp]
     lib.cp_merge_lse.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
     lib.cp_get_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
     lib.cp_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), _vp]
@@ -286,16 +287,16 @@ def cp_attn_fwd_step(plan: Plan, rank, step, q_rank, k_chunk, v_chunk, o_part, l
                                  _ptr(o_part), _ptr(lse_part), _stream(stream)), "cp_attn_fwd_step")
 
 
-def cp_attn_bwd_delta(plan: Plan, o_rank, do_rank, delta_rank, stream=None):
-    _check(_L().cp_attn_bwd_delta(plan.handle, _ptr(o_rank), _ptr(do_rank), _ptr(delta_rank), _stream(stream)),
-           "cp_attn_bwd_delta")
+def cp_attn_bwd_delta(plan: Plan, o_rank, do_rank, lse_rank, stats_rank, stream=None):
+    _check(_L().cp_attn_bwd_delta(plan.handle, _ptr(o_rank), _ptr(do_rank), _ptr(lse_rank), _ptr(stats_rank),
+                                  _stream(stream)), "cp_attn_bwd_delta")
 
 
-def cp_attn_bwd_step(plan: Plan, rank, step, q_rank, do_rank, lse_rank, delta_rank, k_chunk, v_chunk, dq_rank,
-                     dk_chunk, dv_chunk, stream=None):
-    _check(_L().cp_attn_bwd_step(plan.handle, int(rank), int(step), _ptr(q_rank), _ptr(do_rank), _ptr(lse_rank),
-                                 _ptr(delta_rank), _ptr(k_chunk), _ptr(v_chunk), _ptr(dq_rank), _ptr(dk_chunk),
-                                 _ptr(dv_chunk), _stream(stream)), "cp_attn_bwd_step")
+def cp_attn_bwd_step(plan: Plan, rank, step, q_rank, do_rank, stats_rank, k_chunk, v_chunk, dq_rank, dk_chunk,
+                     dv_chunk, stream=None):
+    _check(_L().cp_attn_bwd_step(plan.handle, int(rank), int(step), _ptr(q_rank), _ptr(do_rank), _ptr(stats_rank),
+                                 _ptr(k_chunk), _ptr(v_chunk), _ptr(dq_rank), _ptr(dk_chunk), _ptr(dv_chunk),
+                                 _stream(stream)), "cp_attn_bwd_step")
 
 
 def cp_merge_lse(n_parts, rows, H, d, o_parts, lse_parts, o_out, lse_out, stream=None):

@@ -77,16 +77,25 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(float x) { return x; }
 
+// One warp per (row, head): D = rowsum(dO * O); writes -D and -LSE * log2(e)
+// into the chunk-padded statistics layout (ld_index), then fills the padding
+// slots with 0 and -inf.  rows = attention ranks x T (T in rank-local mode).
 template <int D, typename OT>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dO,
-                                                        float* __restrict__ delta, long long rows, int H, int T,
-                                                        int32_t* status) {
+                                                        const float* __restrict__ lse, float* __restrict__ nlse,
+                                                        float* __restrict__ nd, const AttnGeom g, int chunk_pad,
+                                                        long long rows, int32_t* status) {
   constexpr int E = D / 32;  // elements per lane
+  const int H = g.Hq_loc, T = g.T;
   const int lane = threadIdx.x & 31;
   const long long total = rows * H;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long wi = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < total; wi += nwarps) {
+  const long long ranks = rows / T;
+  [[maybe_unused]] const long long tp = static_cast<long long>(g.nchunks) * chunk_pad;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long nwarps = nthreads >> 5;
+  const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (long long wi = gtid >> 5; wi < total; wi += nwarps) {
     const long long row = wi / H;
     const int h = static_cast<int>(wi - row * H);
     const OT* po = o + wi * D + lane * E;
@@ -98,8 +107,24 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       const long long r = row / T, t = row - r * T;
-      const long long di = (r * H + h) * T + t;
-      if (CP_IN_BOUNDS(di >= 0 && di < total, status)) delta[di] = acc;
+      const long long li = (r * H + h) * T + t;
+      const size_t di = ld_index(g, chunk_pad, static_cast<int>(r), h, static_cast<int>(t));
+      if (CP_IN_BOUNDS(li >= 0 && li < total && di < static_cast<size_t>(ranks * H * tp), status)) {
+        const float l = lse[li];
+        nlse[di] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+        nd[di] = -acc;
+      }
+    }
+  }
+  // Padding: slots [chunk, chunk_pad) of every chunk.
+  const int padw = chunk_pad - g.chunk;
+  const long long npad = ranks * H * g.nchunks * padw;
+  for (long long i = gtid; i < npad; i += nthreads) {
+    const long long c = i / padw;  // (rank, head, chunk)
+    const long long idx = c * chunk_pad + g.chunk + (i - c * padw);
+    if (CP_IN_BOUNDS(idx < ranks * H * tp, status)) {
+      nlse[idx] = -INFINITY;
+      nd[idx] = 0.f;
     }
   }
 }
@@ -313,10 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = row < it.len;
     const int my_pos = row_valid ? qpos0 + row : -1;
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
-    const size_t lrow = (static_cast<size_t>(rank_local ? 0 : a) * Hq + h) * g.T + it.q0 + row;
-    const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rows) * Hq, status);
-    const float lse2 = (row_valid && ld_ok) ? args.lse[lrow] * kLog2e : INFINITY;
-    const float dlt = (row_valid && ld_ok) ? args.delta[lrow] : 0.f;
+    // -LSE*log2(e) and -D of this row, prepared by the delta pass.
+    const size_t lrow = ld_index(g, args.chunk_pad, rank_local ? 0 : a, h, row_valid ? it.q0 + row : 0);
+    const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rows / g.T) * Hq * g.nchunks * args.chunk_pad,
+                                                  status);
+    const float nl2 = (row_valid && ld_ok) ? args.nlse[lrow] : -INFINITY;
+    const float ndl = (row_valid && ld_ok) ? args.nd[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
     {
       // This thread's half of its Q and dO rows into TMEM (lane = row; the
@@ -360,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Phase A: P = exp2(S * scale*log2e - LSE*log2e), masked, as packed bf16
       // (this warp's half of the row: 32-column chunks c4 = 2*half, 2*half+1).
       float pf[BN / 2];  // P of this half of the row, fp32 (dS is formed from it)
-      const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(-lse2, -lse2);
+      const f32x2 nsl2 = make_f32x2(sl2, sl2), nlse2 = make_f32x2(nl2, nl2);
       uint32_t sr2[2][32];  // both chunks of this half: one TMEM round trip
       tmem_ld32(tS + lane_off + 64 * half, sr2[0]);
       tmem_ld32(tS + lane_off + 64 * half + 32, sr2[1]);
@@ -417,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
-                                     make_f32x2(-dlt, -dlt));
+                                     make_f32x2(ndl, ndl));
           float s0, s1;
           split_f32x2(mul_f32x2(make_f32x2(pf[cc * 32 + e], pf[cc * 32 + e + 1]), dd), s0, s1);
           dsp[e / 2] = pack_bf16x2(s0, s1);
@@ -490,7 +517,8 @@ struct DkvSmem {
   static constexpr uint32_t offK = 0, offV = kT, offQ = 2 * kT, offDO = offQ + kQStages * kT;
   static constexpr uint32_t offBar = offDO + kDOStages * kT;
   static constexpr uint32_t offLD = offBar + 24 * 8;   // 2 buffers x (128 -LSE*log2(e) + 128 -D floats)
-  static constexpr uint32_t offMisc = offLD + 2 * 2 * 128 * 4;
+  static constexpr uint32_t offMeta = offLD + 2 * 2 * 128 * 4;  // 2 x {first position, length} of the query tile
+  static constexpr uint32_t offMisc = offMeta + 2 * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   // Up to 1 KB of slack aligns the tiles to the 128-byte swizzle's 1 KB
   // atoms, but no more than the per-CTA limit is requested: the dynamic base
@@ -524,57 +552,6 @@ __device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int 
   }
 }
 
-// The same walk as for_each_q_tile, one tile at a time, so a caller can look
-// one tile ahead.
-struct QTile {
-  int rr, qslot0, qpos0, qlen, h;
-};
-
-struct QTileWalk {
-  const AttnGeom& g;
-  int src, s_end, kpos0, hi_max, jh;
-  int s, ch = 0, t = 0, t1 = -1, hh = 0, rr = 0, cslot0 = 0, cpos0 = 0;
-  bool in_chunk = false;
-  __device__ QTileWalk(const AttnGeom& g_, int src_, int s_begin_, int s_end_, int kpos0_, int hi_max_, int jh_)
-      : g(g_), src(src_), s_end(s_end_), kpos0(kpos0_), hi_max(hi_max_), jh(jh_), s(s_begin_) {}
-  __device__ bool next(QTile& q) {
-    for (;;) {
-      if (in_chunk) {
-        if (hh < g.G) {
-          q.rr = rr;
-          q.qslot0 = cslot0 + t * BM;
-          q.qpos0 = cpos0 + t * BM;
-          q.qlen = min(BM, g.chunk - t * BM);
-          q.h = jh * g.G + hh;
-          ++hh;
-          return true;
-        }
-        hh = 0;
-        if (++t <= t1) continue;
-        in_chunk = false;
-        ++ch;
-      }
-      if (ch >= g.nchunks) {
-        ch = 0;
-        ++s;
-      }
-      if (s >= s_end) return false;
-      rr = (src + s) % g.R;
-      cslot0 = ch * g.chunk;
-      cpos0 = slot_pos(g, rr, cslot0);
-      const int lo = max(cpos0, kpos0);
-      const int hi = min(cpos0 + g.chunk - 1, hi_max);
-      if (lo > hi) {
-        ++ch;
-        continue;
-      }
-      t = (lo - cpos0) / BM;
-      t1 = (hi - cpos0) / BM;
-      in_chunk = true;
-    }
-  }
-};
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -591,9 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV, sQ = s_base + SM::offQ, sDO = s_base + SM::offDO;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
-  // Two buffers b of [128 -LSE * log2(e)][128 -D] per query column.
-  float* sLD = reinterpret_cast<float*>(smem + SM::offLD);
-  const uint32_t aLD = smem_u32(sLD);  // the same, as a shared-window address
+  // Two buffers b of [128 -LSE * log2(e)][128 -D] per query column, and the
+  // first position and length of the query tile each holds.
+  const uint32_t aLD = s_base + SM::offLD;
+  volatile int* sMeta = reinterpret_cast<volatile int*>(smem + SM::offMeta);  // [2][2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
 
@@ -637,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(KV_ACC_DONE), 1);
     mbar_init(bar(KV_DRAIN), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(KV_LD_FULL + i), 4);
+      mbar_init(bar(KV_LD_FULL + i), 1);
       mbar_init(bar(KV_LD_EMPTY + i), 8);
     }
     *abort_flag = 0;
@@ -663,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
       }
-      int nq = 0, ndo = 0;  // Q and dO loads issued
-      for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int rr, int qslot0, int, int, int h) {
+      int nq = 0, ndo = 0, nld = 0;  // Q, dO and statistics loads issued
+      [[maybe_unused]] const size_t ld_total = static_cast<size_t>(rows / g.T) * Hq * g.nchunks * args.chunk_pad;
+      for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int rr, int qslot0, int qpos0, int qlen, int h) {
         if (*abort_flag) return;
         const int qs = nq % kQStages, ds = ndo % kDOStages;
         const int qrow = (rank_local ? 0 : (rr * g.U + u) * g.T) + qslot0;
@@ -679,8 +658,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < NH; ++hh)
           tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_DO_FULL + ds), h * D + hh * 64, qrow);
         ++ndo;
+        // The tile's -LSE*log2(e) and -D (128 each, chunk-padded so the copy
+        // starts on a 512-byte boundary) and its position and length, for
+        // the element-wise warps; the stage is reused once all 8 of them
+        // have finished the tile two before.
+        const int ls = nld & 1;
+        if (nld >= 2 && !mbar_wait(bar(KV_LD_EMPTY + ls), ((nld >> 1) - 1) & 1, abort_flag, status)) return;
+        const size_t li = ld_index(g, args.chunk_pad, rank_local ? 0 : rr * g.U + u, h, qslot0);
+        (void)CP_IN_BOUNDS(li + 128 <= ld_total, status);
+        sMeta[2 * ls] = qpos0;
+        sMeta[2 * ls + 1] = qlen;
+        mbar_arrive_expect_tx(bar(KV_LD_FULL + ls), 1024);
+        bulk_load(aLD + ls * 1024, args.nlse + li, 512, bar(KV_LD_FULL + ls));
+        bulk_load(aLD + ls * 1024 + 512, args.nd + li, 512, bar(KV_LD_FULL + ls));
+        ++nld;
       });
+      if (!*abort_flag) {
+        // End of the walk: a stage with length 0 tells the element-wise warps.
+        const int ls = nld & 1;
+        if (nld < 2 || mbar_wait(bar(KV_LD_EMPTY + ls), ((nld >> 1) - 1) & 1, abort_flag, status)) {
+          sMeta[2 * ls + 1] = 0;
+          mbar_arrive(bar(KV_LD_FULL + ls));
+        }
+      }
       if (*abort_flag) {
+        for (int i = max(0, nld - 2); i < nld; ++i)
+          mbar_wait(bar(KV_LD_FULL + (i & 1)), (i >> 1) & 1, nullptr, status);
         // Wait for this CTA's own copies before it exits (a stage is reused
         // only after its previous load landed, so the last loads of each
         // stage are the only ones that can still be in flight).
@@ -759,7 +762,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const int half = (warp - 2) >> 2;  // warps 2-5: query columns 0-63; warps 6-9: 64-127
     const int row = wq * 32 + lane;     // key row of the tile
-    const int etid = threadIdx.x - 64;  // 0..255 across the element-wise warps
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const bool key_valid = row < it.len;
     const int kpos = kpos0 + row;
@@ -767,23 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = g.scale * kLog2e;
     int n = 0;
     bool ok = true;
-    // LSE and D of the next query tile are loaded (into registers) while the
-    // current one is processed, then staged in shared memory for all warps.
-    QTileWalk walk(g, src, s_begin, s_end, kpos0, hi_max, jh);
-    QTile cur, nxt;
-    bool have = walk.next(cur);
-    float pf_lse = 0.f, pf_del = 0.f;
-    int pf_len = 0;
-    auto prefetch = [&](const QTile& q) {
-      pf_len = q.qlen;
-      if (etid < q.qlen) {
-        const size_t li = (static_cast<size_t>(rank_local ? 0 : q.rr * g.U + u) * Hq + q.h) * g.T + q.qslot0 + etid;
-        if (!CP_IN_BOUNDS(li < static_cast<size_t>(rows) * Hq, status)) return;
-        pf_lse = args.lse[li];
-        pf_del = args.delta[li];
-      }
-    };
-    if (have) prefetch(cur);
     auto process = [&](int qpos0, int qlen, uint32_t aLse, uint32_t aDel) {
       if (!ok) return;
       ok = warp_all(mbar_wait(bar(KV_S_FULL), n & 1, abort_flag, status));
@@ -872,35 +857,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(KV_DS_FULL));
       ++n;
     };
-    // Staging of LSE and D through two shared buffers: warps 2-5 (etid <
-    // 128) write query tile n's values into buffer n & 1 once every warp has
-    // read that buffer's previous contents (tile n - 2), then arrive on its
-    // "full" barrier; every warp reads it after that barrier and arrives on
-    // its "empty" barrier when done.  No warp waits for all others at every
-    // tile, and every wait is bounded.
-    int ld = 0;  // query tiles staged
-    while (have && ok) {
-      const int b = ld & 1;
-      float* sL = sLD + b * 256;
-      if (etid < BM) {
-        if (ld >= 2 && !(ok = warp_all(mbar_wait(bar(KV_LD_EMPTY + b), ((ld >> 1) - 1) & 1, abort_flag, status))))
-          break;
-        const bool in = etid < pf_len;
-        sL[etid] = in ? -pf_lse * kLog2e : -INFINITY;
-        sL[128 + etid] = in ? -pf_del : 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KV_LD_FULL + b));
-      }
-      const bool have_next = walk.next(nxt);
-      if (have_next) prefetch(nxt);
-      if (!(ok = warp_all(mbar_wait(bar(KV_LD_FULL + b), (ld >> 1) & 1, abort_flag, status)))) break;
-      const uint32_t aL = aLD + b * 1024;
-      process(cur.qpos0, cur.qlen, aL, aL + 512);
+    // Query tiles arrive from the producer warp: buffer n & 1 holds the
+    // tile's -LSE*log2(e), -D, first position and length (length 0 ends the
+    // walk).  Each warp hands the buffer back once it has finished the tile.
+    while (ok) {
+      const int ls = n & 1;
+      if (!(ok = warp_all(mbar_wait(bar(KV_LD_FULL + ls), (n >> 1) & 1, abort_flag, status)))) break;
+      const int qpos0 = sMeta[2 * ls], qlen = sMeta[2 * ls + 1];
+      if (qlen == 0) break;
+      const uint32_t aL = aLD + ls * 1024;
+      process(qpos0, qlen, aL, aL + 512);
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KV_LD_EMPTY + b));
-      ++ld;
-      cur = nxt;
-      have = have_next;
+      if (lane == 0) mbar_arrive(bar(KV_LD_EMPTY + ls));
     }
     if (ok && n > 0) {
       ok = warp_all(mbar_wait(bar(KV_ACC_DONE), 0, abort_flag, status));
@@ -987,12 +955,12 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     if (grid > sms * 16LL) grid = sms * 16LL;
     if (grid > 0 && a.o_fp32)
       bwd_delta_kernel<D, float><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-          static_cast<const float*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
-          static_cast<long long>(rows), g.Hq_loc, g.T, a.status);
+          static_cast<const float*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.nlse, a.nd, g,
+          a.chunk_pad, static_cast<long long>(rows), a.status);
     else if (grid > 0)
       bwd_delta_kernel<D, __nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.delta,
-          static_cast<long long>(rows), g.Hq_loc, g.T, a.status);
+          static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.nlse, a.nd, g,
+          a.chunk_pad, static_cast<long long>(rows), a.status);
   }
   const long long grid_kv = static_cast<long long>(a.n_items_kv) * g.Hkv_loc;
   const long long grid_q = static_cast<long long>(a.n_items_q) * g.Hq_loc;

@@ -311,11 +311,20 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
 }
 
 struct BwdWorkspace {
-  size_t delta, qh, kh, vh, oh, doh, lseh, dqh, dkh, dvh, total;
+  size_t nlse, nd, qh, kh, vh, oh, doh, lseh, dqh, dkh, dvh, total;
 };
 
-// delta = rowsum(dO * O) always; with U > 1 also the head-sharded copies of
-// the inputs and gradients.
+// Query-tile-aligned length of one chunk in the backward's row statistics.
+int chunk_pad_of(const cp_plan* p) { return (p->chunk + kTile - 1) / kTile * kTile; }
+
+// Floats of one attention rank's statistics array (-LSE*log2e or -D):
+// Hq/U heads x nchunks x chunk_pad slots.
+size_t rank_ld_floats(const cp_plan* p) {
+  return static_cast<size_t>(p->desc.Hq / p->desc.ulysses_degree) * p->nchunks * chunk_pad_of(p);
+}
+
+// The row statistics (-LSE*log2e and -D, chunk-padded) always; with U > 1
+// also the head-sharded copies of the inputs and gradients.
 BwdWorkspace bwd_workspace(const cp_plan* p) {
   const cp_plan_desc_t& d = p->desc;
   const size_t L = d.L;
@@ -326,7 +335,8 @@ BwdWorkspace bwd_workspace(const cp_plan* p) {
     off += align256(bytes);
     return at;
   };
-  w.delta = take(L * d.Hq * 4);
+  w.nlse = take(static_cast<size_t>(p->P) * rank_ld_floats(p) * 4);
+  w.nd = take(static_cast<size_t>(p->P) * rank_ld_floats(p) * 4);
   if (d.ulysses_degree > 1) {
     w.qh = take(L * d.Hq * d.d * 2);
     w.kh = take(L * d.Hkv * d.d * 2);
@@ -507,6 +517,8 @@ int cp_workspace_size(const cp_plan_t* p, int op, size_t* bytes) {
     *bytes = fwd_workspace(p).total;
   else if (op == CP_OP_BWD)
     *bytes = bwd_workspace(p).total;
+  else if (op == CP_OP_BWD_RANK_STATS)
+    *bytes = 2 * rank_ld_floats(p) * 4;
   else
     return CP_ERR_INVALID_ARG;
   return CP_OK;
@@ -723,7 +735,9 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.nlse = reinterpret_cast<float*>(ws + w.nlse);
+  a.nd = reinterpret_cast<float*>(ws + w.nd);
+  a.chunk_pad = chunk_pad_of(p);
   a.items_q = p->d_items_q;
   a.n_items_q = p->n_items_q;
   a.items_kv = p->d_items_kv;
@@ -801,10 +815,11 @@ int cp_attn_fwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank,
   return cpattn::launch_attn_fwd(a, stream);
 }
 
-int cp_attn_bwd_delta(const cp_plan_t* p, const void* o_rank, const void* do_rank, float* delta_rank,
-                      cudaStream_t stream) {
-  if (!p || !o_rank || !do_rank || !delta_rank) return CP_ERR_INVALID_ARG;
-  if (!aligned16(o_rank) || !aligned16(do_rank) || !aligned16(delta_rank)) return CP_ERR_ALIGNMENT;
+int cp_attn_bwd_delta(const cp_plan_t* p, const void* o_rank, const void* do_rank, const float* lse_rank,
+                      float* stats_rank, cudaStream_t stream) {
+  if (!p || !o_rank || !do_rank || !lse_rank || !stats_rank) return CP_ERR_INVALID_ARG;
+  if (!aligned16(o_rank) || !aligned16(do_rank) || !aligned16(lse_rank) || !aligned16(stats_rank))
+    return CP_ERR_ALIGNMENT;
   int rc = check_device(p);
   if (rc != CP_OK) return rc;
   cpattn::BwdArgs a{};
@@ -812,8 +827,11 @@ int cp_attn_bwd_delta(const cp_plan_t* p, const void* o_rank, const void* do_ran
   a.g.kv_global = 0;
   a.o = o_rank;
   a.dO = do_rank;
+  a.lse = lse_rank;
   a.o_fp32 = p->desc.out_fp32;
-  a.delta = delta_rank;
+  a.nlse = stats_rank;
+  a.nd = stats_rank + rank_ld_floats(p);
+  a.chunk_pad = chunk_pad_of(p);
   // The launcher also builds the four tensor maps: point them at valid rows.
   a.q = a.k = a.v = do_rank;
   a.d = p->desc.d;
@@ -826,14 +844,12 @@ int cp_attn_bwd_delta(const cp_plan_t* p, const void* o_rank, const void* do_ran
 }
 
 int cp_attn_bwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank, const void* do_rank,
-                     const float* lse_rank, const float* delta_rank, const void* k_chunk, const void* v_chunk,
-                     float* dq_rank, float* dk_chunk, float* dv_chunk, cudaStream_t stream) {
-  if (!p || !q_rank || !do_rank || !lse_rank || !delta_rank || !k_chunk || !v_chunk || !dq_rank || !dk_chunk ||
-      !dv_chunk)
+                     const float* stats_rank, const void* k_chunk, const void* v_chunk, float* dq_rank,
+                     float* dk_chunk, float* dv_chunk, cudaStream_t stream) {
+  if (!p || !q_rank || !do_rank || !stats_rank || !k_chunk || !v_chunk || !dq_rank || !dk_chunk || !dv_chunk)
     return CP_ERR_INVALID_ARG;
-  if (!aligned16(q_rank) || !aligned16(do_rank) || !aligned16(lse_rank) || !aligned16(delta_rank) ||
-      !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(dq_rank) || !aligned16(dk_chunk) ||
-      !aligned16(dv_chunk))
+  if (!aligned16(q_rank) || !aligned16(do_rank) || !aligned16(stats_rank) || !aligned16(k_chunk) ||
+      !aligned16(v_chunk) || !aligned16(dq_rank) || !aligned16(dk_chunk) || !aligned16(dv_chunk))
     return CP_ERR_ALIGNMENT;
   const int R = p->desc.ring_degree, U = p->desc.ulysses_degree;
   if (rank < 0 || rank >= p->P || step < 0 || step >= R) return CP_ERR_INVALID_ARG;
@@ -847,8 +863,9 @@ int cp_attn_bwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank,
   a.g.kv_global = 0;
   a.q = q_rank;
   a.dO = do_rank;
-  a.lse = lse_rank;
-  a.delta = const_cast<float*>(delta_rank);  // read only: phases exclude the delta kernel
+  a.nlse = const_cast<float*>(stats_rank);  // read only: phases exclude the delta kernel
+  a.nd = const_cast<float*>(stats_rank) + rank_ld_floats(p);
+  a.chunk_pad = chunk_pad_of(p);
   a.k = k_chunk;
   a.v = v_chunk;
   a.o = do_rank;  // not read (the delta phase is excluded)

@@ -81,7 +81,14 @@ struct BwdArgs {
   const void* o;  const float* lse;  const void* dO;
   int o_fp32;     // o is fp32 instead of bf16
   float* dq;  float* dk;  float* dv;
-  float* delta;   // [R*U][Hq_loc][T] workspace: rowsum(dO * O)
+  // Row statistics the delta pass prepares for the gradient kernels, per
+  // (attention rank, query head, slot) in the chunk-padded layout
+  // [R*U][Hq_loc][nchunks][chunk_pad] (ld_index below): every 128-slot query
+  // tile starts on a 512-byte boundary, so it can be fetched with one bulk
+  // copy; padding slots hold -inf and 0.
+  float* nlse;    // -LSE * log2(e)   (-inf for a row with no visible key)
+  float* nd;      // -D = -rowsum(dO * O)
+  int chunk_pad;  // chunk rounded up to a multiple of 128
   const WorkItem* items_q;
   int n_items_q;
   const WorkItem* items_kv;
@@ -103,6 +110,14 @@ struct BwdArgs {
 };
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+
+// Index of slot t of attention rank a (0 in rank-local buffers), query head h
+// in the chunk-padded statistics layout of BwdArgs::nlse / nd.
+__host__ __device__ inline size_t ld_index(const AttnGeom& g, int chunk_pad, int a, int h, int t) {
+  const int ch = t / g.chunk;
+  return (static_cast<size_t>(a) * g.Hq_loc + h) * (static_cast<size_t>(g.nchunks) * chunk_pad) +
+         static_cast<size_t>(ch) * chunk_pad + (t - ch * g.chunk);
+}
 
 // All-gather of K or V in the emulation: out[slot_pos(r, t)] = in[r*T + t],
 // rows of row_bytes (a multiple of 16).

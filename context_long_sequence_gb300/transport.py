@@ -209,7 +209,7 @@ def ring_backward(comm, kernels, place: RingPlacement, q, kv, o, lse, do, dq_out
     returns, per local ring rank, its own chunk's (dK, dV), each
     [U][T][Hkv/U][d] fp32."""
     R, U, Rl = place.R, place.U, place.Rl
-    delta = [[kernels.delta(o[i][u], do[i][u]) for u in range(U)] for i in range(Rl)]
+    stats = [[kernels.delta(o[i][u], do[i][u], lse[i][u]) for u in range(U)] for i in range(Rl)]
     hold = [tuple(c) for c in kv]
     spare = tuple(kernels.empty_like(t) for t in kv[0])
     ghold = [tuple(kernels.grad_buffer(t) for t in kv[0]) for _ in range(Rl)]
@@ -220,7 +220,7 @@ def ring_backward(comm, kernels, place: RingPlacement, q, kv, o, lse, do, dq_out
         for i in range(Rl):
             for u in range(U):
                 a = (place.r0 + i) * U + u
-                kernels.bwd_step(a, s, q[i][u], do[i][u], lse[i][u], delta[i][u], hold[i][0][u], hold[i][1][u],
+                kernels.bwd_step(a, s, q[i][u], do[i][u], stats[i][u], hold[i][0][u], hold[i][1][u],
                                  dq_out[i][u], ghold[i][0][u], ghold[i][1][u])
         if handles is not None:
             _finish(comm, place, handles, s)
@@ -262,12 +262,13 @@ class CudaRingKernels:
         R, T, Hl, d = o_parts.shape
         self.cpa.cp_merge_lse(R, T, Hl, d, o_parts, lse_parts, o_out, lse_out, stream=self.stream)
 
-    def delta(self, o_a, do_a):
-        T, Hl, _ = do_a.shape
-        out = torch.empty(Hl, T, dtype=torch.float32, device=do_a.device)
-        self.cpa.cp_attn_bwd_delta(self.plan, o_a, do_a, out, stream=self.stream)
+    def delta(self, o_a, do_a, lse_a):
+        """The rank's row statistics (-LSE*log2e, -D) for its backward steps."""
+        n = self.plan.workspace_size(self.cpa.CP_OP_BWD_RANK_STATS) // 4
+        out = torch.empty(n, dtype=torch.float32, device=do_a.device)
+        self.cpa.cp_attn_bwd_delta(self.plan, o_a, do_a, lse_a, out, stream=self.stream)
         return out
 
-    def bwd_step(self, a, s, q_a, do_a, lse_a, delta_a, k_c, v_c, dq_a, dk_c, dv_c):
-        self.cpa.cp_attn_bwd_step(self.plan, a, s, q_a, do_a, lse_a, delta_a, k_c, v_c, dq_a, dk_c, dv_c,
+    def bwd_step(self, a, s, q_a, do_a, stats_a, k_c, v_c, dq_a, dk_c, dv_c):
+        self.cpa.cp_attn_bwd_step(self.plan, a, s, q_a, do_a, stats_a, k_c, v_c, dq_a, dk_c, dv_c,
                                   stream=self.stream)

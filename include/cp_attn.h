@@ -98,6 +98,7 @@ extern "C" {
 /* Operations for cp_workspace_size(). */
 #define CP_OP_FWD 0
 #define CP_OP_BWD 1
+#define CP_OP_BWD_RANK_STATS 2  /* one attention rank's stats_rank buffer (cp_attn_bwd_delta) */
 
 /* Plan description (host struct; copied by cp_plan_create). */
 typedef struct {
@@ -256,7 +257,7 @@ int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void 
  * rank's own buffers and a visiting chunk held in separate buffers (the
  * layout each process keeps per rank):
  *   q_rank, do_rank [T][Hq/U][d] bf16; o_rank the same (fp32 if out_fp32);
- *   lse_rank, delta_rank [Hq/U][T] fp32;  T = L/R slots of ring rank r
+ *   lse_rank [Hq/U][T] fp32;  T = L/R slots of ring rank r
  *   k_chunk, v_chunk [T][Hkv/U][d] bf16: the slots of attention rank
  *   a_src = ((r - s) mod R)*U + u, the chunk that visits rank a at step s.
  * With U == 1 these are plain sequence shards; with U > 1 they are the
@@ -273,25 +274,31 @@ int cp_attn_fwd_step(const cp_plan_t *plan, int rank, int step, const void *q_ra
                      const void *k_chunk, const void *v_chunk, float *o_part, float *lse_part,
                      cudaStream_t stream);
 
-/* D = rowsum(dO * O) of one rank's rows (the backward's first pass):
- * delta_rank [Hq/U][T] fp32 out. */
+/* The backward's first pass over one rank's rows: D = rowsum(dO * O), and
+ * the row statistics the gradient steps read, written to stats_rank
+ * (cp_workspace_size(plan, CP_OP_BWD_RANK_STATS, ...) bytes):
+ *   stats_rank[0][h][slot'] = -LSE * log2(e),  stats_rank[1][h][slot'] = -D
+ * for the Hq/U heads of the rank, where slot' pads every position chunk of
+ * the rank to a multiple of 128 slots (padding: -inf and 0) so that each
+ * 128-slot query tile starts on a 512-byte boundary.  lse_rank [Hq/U][T]. */
 int cp_attn_bwd_delta(const cp_plan_t *plan, const void *o_rank, const void *do_rank,
-                      float *delta_rank, cudaStream_t stream);
+                      const float *lse_rank, float *stats_rank, cudaStream_t stream);
 
 /* Backward contributions of ring step s (fp32):
  *   dq_rank [T][Hq/U][d]: rank a's dQ, from the visiting chunk's keys;
  *   dk_chunk, dv_chunk [T][Hkv/U][d]: the visiting chunk's dK, dV, from
  *   rank a's queries (the buffers travel with the chunk).
+ * stats_rank is rank a's buffer from cp_attn_bwd_delta.
  * Step 0 (every chunk at its owner) writes all three, zeros where nothing
  * is visible; steps s > 0 add to them.  After the R steps of every rank,
- * rank a's dQ equals its
- * rows of cp_attn_bwd's dq and each chunk's dk/dv equal its owner's rows of
- * cp_attn_bwd's dk/dv (the same products; the fp32 sums are taken per ring
- * step, so the results agree within fp32 rounding, not bit for bit). */
+ * rank a's dQ equals its rows of cp_attn_bwd's dq and each chunk's dk/dv
+ * equal its owner's rows of cp_attn_bwd's dk/dv (the same products; the
+ * fp32 sums are taken per ring step, so the results agree within fp32
+ * rounding, not bit for bit). */
 int cp_attn_bwd_step(const cp_plan_t *plan, int rank, int step, const void *q_rank,
-                     const void *do_rank, const float *lse_rank, const float *delta_rank,
-                     const void *k_chunk, const void *v_chunk, float *dq_rank, float *dk_chunk,
-                     float *dv_chunk, cudaStream_t stream);
+                     const void *do_rank, const float *stats_rank, const void *k_chunk,
+                     const void *v_chunk, float *dq_rank, float *dk_chunk, float *dv_chunk,
+                     cudaStream_t stream);
 
 /* Merge n_parts normalised attention partials over disjoint key sets
  * ([MTX] "Split heads or rotate KV": partial computation and merge):

@@ -148,11 +148,17 @@ def test_workspace_sizes(cpa):
     p = cpa.Plan(16384, 32, 8, 128, ulysses_degree=4)
     L = 16384
     assert p.workspace_size(cpa.CP_OP_FWD) == al(L * 32 * 256) * 2 + al(L * 8 * 256) * 2 + al(L * 32 * 4)
-    # delta, then head-sharded q, k, v, o, dO (bf16), LSE, dq, dk, dv (fp32).
-    assert p.workspace_size(cpa.CP_OP_BWD) == (al(L * 32 * 4) + al(L * 32 * 256) * 3 + al(L * 8 * 256) * 2
+    # Row statistics (-LSE*log2e, -D; chunks already multiples of 128), then
+    # head-sharded q, k, v, o, dO (bf16), LSE, dq, dk, dv (fp32).
+    assert p.workspace_size(cpa.CP_OP_BWD) == (al(L * 32 * 4) * 2 + al(L * 32 * 256) * 3 + al(L * 8 * 256) * 2
                                               + al(L * 32 * 4) + al(L * 32 * 512) + al(L * 8 * 512) * 2)
+    assert p.workspace_size(cpa.CP_OP_BWD_RANK_STATS) == 2 * 8 * 16384 * 4  # T = L/R = 16384 slots, 8 heads
     p = cpa.Plan(16384, 32, 8, 128, ring_degree=4)
-    assert p.workspace_size(cpa.CP_OP_BWD) == al(L * 32 * 4)
+    assert p.workspace_size(cpa.CP_OP_BWD) == al(L * 32 * 4) * 2
+    # Ragged chunks pad to 128 slots: T = 500, two chunks of 250 -> 2 x 256.
+    p = cpa.Plan(1000, 4, 2, 64, ring_degree=2, layout=1)
+    assert p.workspace_size(cpa.CP_OP_BWD_RANK_STATS) == 2 * 4 * 512 * 4
+    assert p.workspace_size(cpa.CP_OP_BWD) == al(2 * 4 * 512 * 4) * 2
     p = cpa.Plan(1024, 4, 4, 64, ring_degree=4, emit_partials=True)
     assert p.workspace_size(cpa.CP_OP_FWD) == al(4 * 1024 * 4 * 64 * 4) + al(4 * 1024 * 4 * 4)
     p = cpa.Plan(1024, 4, 4, 64, ring_degree=4)

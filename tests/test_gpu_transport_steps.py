@@ -155,7 +155,7 @@ def test_step_entries_reject_bad_arguments(cpa):
             cpa.cp_attn_fwd_step(plan, rank, step, z, z, z, f, f)
         assert e.value.code == cpa.CP_ERR_INVALID_ARG
         with pytest.raises(cpa.CPError) as e:
-            cpa.cp_attn_bwd_step(plan, rank, step, z, z, f, f, z, z, f, f, f)
+            cpa.cp_attn_bwd_step(plan, rank, step, z, z, f, z, z, f, f, f)
         assert e.value.code == cpa.CP_ERR_INVALID_ARG
     ag = cpa.Plan(1024, 4, 2, 128, ring_degree=4, layout=1, kv_exchange=cpa.CP_KV_ALLGATHER)
     with pytest.raises(cpa.CPError) as e:

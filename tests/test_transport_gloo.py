@@ -63,10 +63,11 @@ class OracleKernels:
         o_out.copy_(torch.from_numpy(o))
         lse_out.copy_(torch.from_numpy(lse))
 
-    def delta(self, o_a, do_a):
-        return o_a  # the oracle's step forms D = rowsum(dO * O) from O itself
+    def delta(self, o_a, do_a, lse_a):
+        return o_a, lse_a  # the oracle's step forms D = rowsum(dO * O) from O itself
 
-    def bwd_step(self, a, s, q_a, do_a, lse_a, o_a, k_c, v_c, dq_a, dk_c, dv_c):
+    def bwd_step(self, a, s, q_a, do_a, stats, k_c, v_c, dq_a, dk_c, dv_c):
+        o_a, lse_a = stats
         r = a // self.U
         src = (r - s) % self.R
         pq, pk, pv = self.orc.attention_bwd_partial(q_a.numpy(), do_a.numpy(), o_a.numpy(), lse_a.numpy(),
