@@ -91,10 +91,19 @@ struct FwdSmem {
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
 };
 
-// Visit, in ring order, every 128-key tile that may hold a visible key for
-// query positions <= qpos_last whose documents start at or after lo_min.
+// Visit every 128-key tile that may hold a visible key for query positions
+// <= qpos_last whose documents start at or after lo_min.
 // f(kv_row, kpos0, klen): first row of the tile in the [R*U*T] row space,
 // the tile's first position, and its number of valid keys.
+//
+// One ring step (emit-partials, rank-local): the chunk of rank (r - s) mod R.
+// All ring steps in one launch: the visiting chunks are walked in position
+// order rather than ring order.  Every chunk is resident, so the order is
+// free; the merge is exact, so it changes only the fp32 rounding order.  In
+// position order all the long query blocks running at once sweep the same
+// key tiles together and share them in L2; in ring order each starts from
+// its own rank's chunk, and a tile's many readers come too far apart in time
+// for L2 to keep it (at 256K tokens, 180x the compulsory DRAM reads).
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end,
                                                  int lo_min, int qpos_last, F&& f) {
@@ -102,6 +111,21 @@ __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u
     // All-gathered K/V: row = position; one pass in position order.
     const int t1 = qpos_last / BN;
     for (int t = lo_min / BN; t <= t1; ++t) f(t * BN, t * BN, min(BN, g.L - t * BN));
+    return;
+  }
+  if (s_begin == 0 && s_end == g.R && g.R > 1) {
+    const int c = g.chunk;
+    const int j1 = qpos_last / c;
+    for (int j = lo_min / c; j <= j1; ++j) {
+      int src, cslot0;
+      chunk_owner(g, j, src, cslot0);
+      const int cpos0 = j * c;
+      const int lo = max(cpos0, lo_min);
+      const int hi = min(cpos0 + c - 1, qpos_last);
+      const int t1 = (hi - cpos0) / BN;
+      for (int t = (lo - cpos0) / BN; t <= t1; ++t)
+        f((src * g.U + u) * g.T + cslot0 + t * BN, cpos0 + t * BN, min(BN, c - t * BN));
+    }
     return;
   }
   const int nchunks = g.nchunks;
@@ -174,8 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttnGeom& g = args.g;
   int32_t* status = args.status;
-  const int item_idx = blockIdx.x / g.Hq_loc;
-  const int h = blockIdx.x % g.Hq_loc;
+  int item_idx, h;
+  if (args.stream_major) {
+    const int per_stream = args.n_items_u * g.G;
+    const int sidx = blockIdx.x / per_stream;  // K/V stream (u, KV head)
+    const int rem = blockIdx.x - sidx * per_stream;
+    const int su = sidx / g.Hkv_loc;
+    item_idx = su * args.n_items_u + rem / g.G;
+    h = (sidx - su * g.Hkv_loc) * g.G + rem % g.G;
+  } else {
+    item_idx = blockIdx.x / g.Hq_loc;
+    h = blockIdx.x % g.Hq_loc;
+  }
   if (!CP_IN_BOUNDS(item_idx < args.n_items, status)) return;
   WorkItem it = args.items[item_idx];
   const bool rank_local = args.rank_local != 0;  // one ring step; Q and K/V are local buffers

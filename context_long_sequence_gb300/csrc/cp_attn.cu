@@ -48,10 +48,14 @@ struct cp_plan {
   int device;
   std::vector<int32_t> chunk_pos;  // balanced layout: [R][nchunks] first position of each chunk
   int32_t* d_chunk_pos;          // device copy, or null
+  std::vector<int32_t> chunk_own;  // balanced layout: position chunk -> r * nchunks + k
+  int32_t* d_chunk_own;          // device copy, or null
   int32_t* d_doc_start;          // [L] or null
   int32_t* d_doc_end;            // [L] or null
   WorkItem* d_items_fused;       // forward: 256-row query blocks, all ring steps
   int n_items_fused;
+  WorkItem* d_items_byu;         // the same grouped by Ulysses member (stream-major launch order), or null
+  int n_items_u;                 // items per member
   WorkItem* d_items_q;           // backward dQ: 128-row query tiles
   int n_items_q;
   WorkItem* d_items_steps;       // emit-partials: one item per (256-row query block, ring step)
@@ -112,6 +116,7 @@ AttnGeom geom(const cp_plan* p, bool on_host = false) {
   g.chunk = p->chunk;
   g.nchunks = p->nchunks;
   g.chunk_pos = p->chunk_pos.empty() ? nullptr : (on_host ? p->chunk_pos.data() : p->d_chunk_pos);
+  g.chunk_owner = p->chunk_own.empty() ? nullptr : (on_host ? p->chunk_own.data() : p->d_chunk_own);
   g.kv_global = d.kv_exchange == CP_KV_ALLGATHER ? 1 : 0;
   g.scale = p->scale;
   g.doc_start = p->d_doc_start;
@@ -138,6 +143,20 @@ int visited_tiles(const cp_plan* p, const AttnGeom& g, int r, int q0, int len, i
     }
   }
   return count;
+}
+
+// The forward over every rank and ring step in one launch: the items
+// grouped by Ulysses member, launched stream-major (see FwdArgs), when the
+// grouping exists; else the plain longest-first list.
+void set_fused_items(const cp_plan* p, cpattn::FwdArgs& a) {
+  if (p->d_items_byu) {
+    a.items = p->d_items_byu;
+    a.stream_major = 1;
+    a.n_items_u = p->n_items_u;
+  } else {
+    a.items = p->d_items_fused;
+  }
+  a.n_items = p->n_items_fused;
 }
 
 // Query blocks of `rows` slots, ordered by descending work (longest first
@@ -204,6 +223,8 @@ void balanced_chunk_table(cp_plan* p) {
     std::sort(held[r].begin(), held[r].end());
     for (int k = 0; k < m; ++k) p->chunk_pos[static_cast<size_t>(r) * m + k] = held[r][k] * c;
   }
+  p->chunk_own.assign(static_cast<size_t>(C), 0);
+  for (int e = 0; e < C; ++e) p->chunk_own[p->chunk_pos[e] / c] = e;
 }
 
 int doc_end_host(const cp_plan* p, int pos) {
@@ -407,12 +428,13 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->nchunks = nchunks;
   p->chunk = T / p->nchunks;
   if (d.layout == CP_LAYOUT_BALANCED) balanced_chunk_table(p);
-  p->d_chunk_pos = nullptr;
+  p->d_chunk_pos = p->d_chunk_own = nullptr;
   p->scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
   p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = p->d_items_rank = nullptr;
-  p->d_items_q_rank = p->d_items_kv_rank = nullptr;
+  p->d_items_q_rank = p->d_items_kv_rank = p->d_items_byu = nullptr;
+  p->n_items_u = 0;
   p->n_items_fused = p->n_items_q = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
@@ -442,11 +464,28 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       if (rc == CP_OK) rc = upload(de, &p->d_doc_end);
     }
     if (rc == CP_OK) rc = upload(p->chunk_pos, &p->d_chunk_pos);
+    if (rc == CP_OK) rc = upload(p->chunk_own, &p->d_chunk_own);
     std::vector<WorkItem> fused = build_items(p, false, 2 * kTile);
     p->n_items_fused = static_cast<int>(fused.size());
     if (rc == CP_OK) rc = upload(fused, &p->d_items_fused);
     // The same items grouped by rank, each group keeping the longest-first order.
     if (rc == CP_OK) rc = upload(group_by_rank(fused, p->P, &p->rank_item_off), &p->d_items_rank);
+    // And grouped by Ulysses member u = a % U (longest first within each),
+    // when every member has the same number of items.
+    if (rc == CP_OK) {
+      std::vector<WorkItem> byu;
+      std::vector<int> cnt(U, 0);
+      for (int uu = 0; uu < U; ++uu)
+        for (const WorkItem& it : fused)
+          if (it.a % U == uu) {
+            byu.push_back(it);
+            ++cnt[uu];
+          }
+      if (std::count(cnt.begin(), cnt.end(), cnt[0]) == U) {
+        p->n_items_u = cnt[0];
+        rc = upload(byu, &p->d_items_byu);
+      }
+    }
     if (rc == CP_OK) {
       std::vector<WorkItem> qt = build_items(p, false, kTile);
       p->n_items_q = static_cast<int>(qt.size());
@@ -467,8 +506,10 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     if (rc != CP_OK) {
       cudaFree(p->d_items_q_rank);
       cudaFree(p->d_items_kv_rank);
+      cudaFree(p->d_items_byu);
       cudaFree(p->d_items_rank);
       cudaFree(p->d_chunk_pos);
+      cudaFree(p->d_chunk_own);
       cudaFree(p->d_doc_start);
       cudaFree(p->d_doc_end);
       cudaFree(p->d_items_fused);
@@ -489,8 +530,10 @@ void cp_plan_destroy(cp_plan_t* p) {
   if (p->on_device) {
     cudaFree(p->d_items_q_rank);
     cudaFree(p->d_items_kv_rank);
+    cudaFree(p->d_items_byu);
     cudaFree(p->d_items_rank);
     cudaFree(p->d_chunk_pos);
+    cudaFree(p->d_chunk_own);
     cudaFree(p->d_doc_start);
     cudaFree(p->d_doc_end);
     cudaFree(p->d_items_fused);
@@ -625,8 +668,7 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
       a.k = ws + w.kall;
       a.v = ws + w.vall;
     }
-    a.items = p->d_items_fused;
-    a.n_items = p->n_items_fused;
+    set_fused_items(p, a);
     NvtxRange phase("attention");
     return cpattn::launch_attn_fwd(a, stream);
   }
@@ -651,8 +693,7 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.v = vh;
   a.o = oh;
   a.lse = lseh;
-  a.items = p->d_items_fused;
-  a.n_items = p->n_items_fused;
+  set_fused_items(p, a);
   {
     NvtxRange phase("attention");
     if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
@@ -680,8 +721,7 @@ int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const vo
   a.v = v;
   a.o = o;
   a.lse = lse;
-  a.items = p->d_items_fused;
-  a.n_items = p->n_items_fused;
+  set_fused_items(p, a);
   NvtxRange call("cp_attn_fwd_local");
   return cpattn::launch_attn_fwd(a, stream);
 }

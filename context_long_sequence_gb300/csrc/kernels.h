@@ -25,6 +25,8 @@ struct AttnGeom {
   int nchunks;             // chunks per ring rank: 1 (contiguous), 2 (zigzag), m (balanced)
   const int32_t* chunk_pos;  // balanced: [R][nchunks] first position of each chunk (host or
                              // device copy, matching where slot_pos runs); else null
+  const int32_t* chunk_owner;  // balanced: [R*nchunks] position chunk j -> r*nchunks + k, the
+                               // rank r and local chunk k holding it (inverse of chunk_pos); else null
   int kv_global;           // 1: K/V rows are in global position order (all-gathered), U == 1
   float scale;             // softmax scale
   const int32_t* doc_start;  // [L] start of the document holding each position, or null
@@ -38,6 +40,23 @@ __host__ __device__ inline int slot_pos(const AttnGeom& g, int r, int t) {
   if (g.layout == 1) return t < c ? r * c + t : (2 * g.R - 1 - r) * c + (t - c);
   const int j = t / c;
   return g.chunk_pos[r * g.nchunks + j] + (t - j * c);
+}
+
+// Ring rank and first slot of the position chunk j (positions [j*chunk,
+// (j+1)*chunk)): every layout cuts the sequence into chunks of g.chunk.
+__host__ __device__ inline void chunk_owner(const AttnGeom& g, int j, int& src, int& cslot0) {
+  if (g.layout == 0) {
+    src = j;
+    cslot0 = 0;
+  } else if (g.layout == 1) {
+    const bool first = j < g.R;
+    src = first ? j : 2 * g.R - 1 - j;
+    cslot0 = first ? 0 : g.chunk;
+  } else {
+    const int e = g.chunk_owner[j];
+    src = e / g.nchunks;
+    cslot0 = (e - src * g.nchunks) * g.chunk;
+  }
 }
 
 struct FwdArgs {
@@ -62,6 +81,13 @@ struct FwdArgs {
   // partial.  0 (the zero-initialised default): all ranks, as above.
   int rank_local;
   int step;
+  // Launch order.  0: block b = item b / Hq_loc, head b % Hq_loc.  1 (with
+  // `items` grouped by Ulysses member u, n_items_u each): blocks run one K/V
+  // stream (u, KV head) after another, and within a stream the items in
+  // list order with the G query heads of the KV head adjacent, so the CTAs
+  // resident at once read the same K/V tiles.
+  int stream_major;
+  int n_items_u;
 };
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
