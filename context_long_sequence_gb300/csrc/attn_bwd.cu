@@ -161,9 +161,29 @@ __device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint64_
     mma_bf16_ts_kmaj_k64_warp(d_tmem, a_tmem, b, idesc, 0u);
 }
 
+// Key tiles a query tile of ring rank r walks: one ring step (the chunk of
+// rank (r - s) mod R), or, for every ring step in one launch, the chunks in
+// position order (the order is free and the fp32 sums are exact up to
+// rounding; in position order the CTAs resident at once read the same key
+// tiles and share them in L2, as in the forward kernel).
 template <typename F>
 __device__ __forceinline__ void for_each_kv_tile(const AttnGeom& g, int r, int u, int s_begin, int s_end, int lo_min,
                                                  int qpos_last, F&& f) {
+  if (s_begin == 0 && s_end == g.R && g.R > 1) {
+    const int c = g.chunk;
+    const int j1 = qpos_last / c;
+    for (int j = lo_min / c; j <= j1; ++j) {
+      int src, cslot0;
+      chunk_owner(g, j, src, cslot0);
+      const int cpos0 = j * c;
+      const int lo = max(cpos0, lo_min);
+      const int hi = min(cpos0 + c - 1, qpos_last);
+      const int t1 = (hi - cpos0) / BN;
+      for (int t = (lo - cpos0) / BN; t <= t1; ++t)
+        f((src * g.U + u) * g.T + cslot0 + t * BN, cpos0 + t * BN, min(BN, c - t * BN));
+    }
+    return;
+  }
   const int nchunks = g.nchunks;
   for (int s = s_begin; s < s_end; ++s) {
     const int src = (r - s + g.R) % g.R;
@@ -199,15 +219,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnGeom& g = args.g;
   int32_t* status = args.status;
   const int Hq = g.Hq_loc;
-  if (!CP_IN_BOUNDS(static_cast<int>(blockIdx.x / Hq) < args.n_items_q, status)) return;
-  const WorkItem it = args.items_q[blockIdx.x / Hq];
+  // Launch order: item-major (heads fastest), or stream-major (one K/V
+  // stream (u, KV head) after another, the G query heads of the KV head
+  // adjacent, so the CTAs resident at once read the same K/V tiles).
+  int item_idx, h;
+  if (args.stream_major) {
+    const int per_stream = args.n_items_q_u * g.G;
+    const int sidx = blockIdx.x / per_stream;
+    const int rem = blockIdx.x - sidx * per_stream;
+    const int su = sidx / g.Hkv_loc;
+    item_idx = su * args.n_items_q_u + rem / g.G;
+    h = (sidx - su * g.Hkv_loc) * g.G + rem % g.G;
+  } else {
+    item_idx = blockIdx.x / Hq;
+    h = blockIdx.x % Hq;
+  }
+  if (!CP_IN_BOUNDS(item_idx < args.n_items_q, status)) return;
+  const WorkItem it = args.items_q[item_idx];
   // A query tile lies inside its attention rank's slots.
   if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
                         it.q0 + it.len <= g.T, status))
     return;
   const bool rank_local = args.rank_local != 0;
   [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dQ
-  const int h = blockIdx.x % Hq;
   const int a = it.a, r = a / g.U, u = a % g.U;  // rank a = ring rank r, Ulysses member u
   const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
   // Rank-local mode: the rank's rows start at 0, and so do the visiting chunk's.
@@ -535,6 +569,24 @@ struct DkvSmem {
 template <typename F>
 __device__ __forceinline__ void for_each_q_tile(const AttnGeom& g, int src, int s_begin, int s_end, int kpos0,
                                                 int hi_max, int jh, F&& f) {
+  if (s_begin == 0 && s_end == g.R && g.R > 1) {
+    // Every ring step in one launch: query chunks in position order (see
+    // for_each_kv_tile).
+    const int c = g.chunk;
+    const int j1 = hi_max / c;
+    for (int j = kpos0 / c; j <= j1; ++j) {
+      int rr, cslot0;
+      chunk_owner(g, j, rr, cslot0);
+      const int cpos0 = j * c;
+      const int lo = max(cpos0, kpos0);
+      const int hi = min(cpos0 + c - 1, hi_max);
+      const int t1 = (hi - cpos0) / BM;
+      for (int t = (lo - cpos0) / BM; t <= t1; ++t)
+        for (int hh = 0; hh < g.G; ++hh)
+          f(rr, cslot0 + t * BM, cpos0 + t * BM, min(BM, c - t * BM), jh * g.G + hh);
+    }
+    return;
+  }
   const int nchunks = g.nchunks;
   for (int s = s_begin; s < s_end; ++s) {
     const int rr = (src + s) % g.R;
@@ -579,15 +631,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnGeom& g = args.g;
   int32_t* status = args.status;
   const int Hkv = g.Hkv_loc, Hq = g.Hq_loc;
-  if (!CP_IN_BOUNDS(static_cast<int>(blockIdx.x / Hkv) < args.n_items_kv, status)) return;
-  const WorkItem it = args.items_kv[blockIdx.x / Hkv];
+  // Launch order: item-major (KV heads fastest), or stream-major (one
+  // (u, KV head) after another, so the CTAs resident at once read the same
+  // query tiles of that KV head's query heads).
+  int item_idx, jh;
+  if (args.stream_major) {
+    const int sidx = blockIdx.x / args.n_items_kv_u;
+    const int su = sidx / Hkv;
+    item_idx = su * args.n_items_kv_u + (blockIdx.x - sidx * args.n_items_kv_u);
+    jh = sidx - su * Hkv;
+  } else {
+    item_idx = blockIdx.x / Hkv;
+    jh = blockIdx.x % Hkv;
+  }
+  if (!CP_IN_BOUNDS(item_idx < args.n_items_kv, status)) return;
+  const WorkItem it = args.items_kv[item_idx];
   // A key tile lies inside its attention rank's slots.
   if (!CP_IN_BOUNDS(it.a >= 0 && it.a < g.R * g.U && it.q0 >= 0 && it.len > 0 && it.len <= BM &&
                         it.q0 + it.len <= g.T, status))
     return;
   const bool rank_local = args.rank_local != 0;
   [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dK, dV
-  const int jh = blockIdx.x % Hkv;
   const int a = it.a, src = a / g.U, u = a % g.U;  // key tile of rank a = ring rank src, member u
   const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
   // Rank-local mode: the chunk's rows start at 0, and so do the holder's.

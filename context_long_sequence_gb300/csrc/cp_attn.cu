@@ -56,6 +56,10 @@ struct cp_plan {
   int n_items_fused;
   WorkItem* d_items_byu;         // the same grouped by Ulysses member (stream-major launch order), or null
   int n_items_u;                 // items per member
+  WorkItem* d_items_q_byu;       // backward query tiles grouped by Ulysses member, or null
+  int n_items_q_u;
+  WorkItem* d_items_kv_byu;      // backward key tiles grouped by Ulysses member, or null
+  int n_items_kv_u;
   WorkItem* d_items_q;           // backward dQ: 128-row query tiles
   int n_items_q;
   WorkItem* d_items_steps;       // emit-partials: one item per (256-row query block, ring step)
@@ -157,6 +161,22 @@ void set_fused_items(const cp_plan* p, cpattn::FwdArgs& a) {
     a.items = p->d_items_fused;
   }
   a.n_items = p->n_items_fused;
+}
+
+// `items` (longest first) grouped by Ulysses member u = a % U, keeping the
+// order within each group; empty when the members' counts differ.
+std::vector<WorkItem> group_by_member(const std::vector<WorkItem>& items, int U, int* per_member) {
+  std::vector<WorkItem> out;
+  std::vector<int> cnt(U, 0);
+  for (int uu = 0; uu < U; ++uu)
+    for (const WorkItem& it : items)
+      if (it.a % U == uu) {
+        out.push_back(it);
+        ++cnt[uu];
+      }
+  *per_member = cnt[0];
+  if (std::count(cnt.begin(), cnt.end(), cnt[0]) != U) out.clear();
+  return out;
 }
 
 // Query blocks of `rows` slots, ordered by descending work (longest first
@@ -433,8 +453,8 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
   p->on_device = false;
   p->d_doc_start = p->d_doc_end = nullptr;
   p->d_items_fused = p->d_items_q = p->d_items_steps = p->d_items_kv = p->d_items_rank = nullptr;
-  p->d_items_q_rank = p->d_items_kv_rank = p->d_items_byu = nullptr;
-  p->n_items_u = 0;
+  p->d_items_q_rank = p->d_items_kv_rank = p->d_items_byu = p->d_items_q_byu = p->d_items_kv_byu = nullptr;
+  p->n_items_u = p->n_items_q_u = p->n_items_kv_u = 0;
   p->n_items_fused = p->n_items_q = p->n_items_steps = p->n_items_kv = 0;
 
   // Device tables, when a CUDA device is present (host-only use -- index
@@ -472,25 +492,13 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
     if (rc == CP_OK) rc = upload(group_by_rank(fused, p->P, &p->rank_item_off), &p->d_items_rank);
     // And grouped by Ulysses member u = a % U (longest first within each),
     // when every member has the same number of items.
-    if (rc == CP_OK) {
-      std::vector<WorkItem> byu;
-      std::vector<int> cnt(U, 0);
-      for (int uu = 0; uu < U; ++uu)
-        for (const WorkItem& it : fused)
-          if (it.a % U == uu) {
-            byu.push_back(it);
-            ++cnt[uu];
-          }
-      if (std::count(cnt.begin(), cnt.end(), cnt[0]) == U) {
-        p->n_items_u = cnt[0];
-        rc = upload(byu, &p->d_items_byu);
-      }
-    }
+    if (rc == CP_OK) rc = upload(group_by_member(fused, U, &p->n_items_u), &p->d_items_byu);
     if (rc == CP_OK) {
       std::vector<WorkItem> qt = build_items(p, false, kTile);
       p->n_items_q = static_cast<int>(qt.size());
       rc = upload(qt, &p->d_items_q);
       if (rc == CP_OK) rc = upload(group_by_rank(qt, p->P, &p->q_rank_off), &p->d_items_q_rank);
+      if (rc == CP_OK) rc = upload(group_by_member(qt, U, &p->n_items_q_u), &p->d_items_q_byu);
     }
     if (rc == CP_OK && d.emit_partials) {
       std::vector<WorkItem> steps = build_items(p, true, 2 * kTile);
@@ -502,11 +510,14 @@ int cp_plan_create(const cp_plan_desc_t* desc, cp_plan_t** out) {
       p->n_items_kv = static_cast<int>(kv.size());
       rc = upload(kv, &p->d_items_kv);
       if (rc == CP_OK) rc = upload(group_by_rank(kv, p->P, &p->kv_rank_off), &p->d_items_kv_rank);
+      if (rc == CP_OK) rc = upload(group_by_member(kv, U, &p->n_items_kv_u), &p->d_items_kv_byu);
     }
     if (rc != CP_OK) {
       cudaFree(p->d_items_q_rank);
       cudaFree(p->d_items_kv_rank);
       cudaFree(p->d_items_byu);
+      cudaFree(p->d_items_q_byu);
+      cudaFree(p->d_items_kv_byu);
       cudaFree(p->d_items_rank);
       cudaFree(p->d_chunk_pos);
       cudaFree(p->d_chunk_own);
@@ -531,6 +542,8 @@ void cp_plan_destroy(cp_plan_t* p) {
     cudaFree(p->d_items_q_rank);
     cudaFree(p->d_items_kv_rank);
     cudaFree(p->d_items_byu);
+    cudaFree(p->d_items_q_byu);
+    cudaFree(p->d_items_kv_byu);
     cudaFree(p->d_items_rank);
     cudaFree(p->d_chunk_pos);
     cudaFree(p->d_chunk_own);
@@ -782,6 +795,13 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   a.n_items_q = p->n_items_q;
   a.items_kv = p->d_items_kv;
   a.n_items_kv = p->n_items_kv;
+  if (p->d_items_q_byu && p->d_items_kv_byu) {  // stream-major launch order (see BwdArgs)
+    a.items_q = p->d_items_q_byu;
+    a.items_kv = p->d_items_kv_byu;
+    a.stream_major = 1;
+    a.n_items_q_u = p->n_items_q_u;
+    a.n_items_kv_u = p->n_items_kv_u;
+  }
   a.d = p->desc.d;
   a.status = status_ptr();
   if (!a.status) return CP_ERR_CUDA;

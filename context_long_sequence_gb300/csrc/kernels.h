@@ -133,6 +133,10 @@ struct BwdArgs {
   int step;
   int accumulate;  // 1: dq, dk, dv += this call's contribution (else overwritten)
   int phases;      // bit 0: delta, bit 1: dkv, bit 2: dq; 0 means all three
+  // Launch order as FwdArgs::stream_major, with items_q and items_kv grouped
+  // by Ulysses member (n_items_q_u and n_items_kv_u each).
+  int stream_major;
+  int n_items_q_u, n_items_kv_u;
 };
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
