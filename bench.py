@@ -210,6 +210,8 @@ def profiled_traffic(workload: str):
     if rec.get("kernel_source_sha") != kernel_source_hash():
         return None, "kernel changed since the committed capture"
     entry = rec.get("per_launch_bytes", {}).get(workload)
+    if entry is None:
+        return None, None
     if isinstance(entry, dict):
         return entry.get("bytes"), entry.get("how")
     return entry, rec.get("source")
