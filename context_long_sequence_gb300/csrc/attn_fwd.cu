@@ -403,17 +403,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) return;
       tc_fence_after();
       const bool full = w.full(kpos0, klen);
+      uint32_t sr[BN];
+      float* x = reinterpret_cast<float*>(sr);
+      auto col32 = [&](int c) -> uint32_t(&)[32] { return *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]); };
+      // P = exp2(S*scale*log2e - mb) of 32 columns -> 16 packed bf16 pairs,
+      // row sum into rs2.  Pairs of columns go through packed fp32x2 fma/add
+      // (half the issue slots of scalar code); exp2 stays per element on the
+      // MUFU pipe.
+      const f32x2 sl2x2 = make_f32x2(sl2, sl2);
+      auto exp32 = [&](int c, float mb, f32x2 (&rs2)[4], uint32_t (&pk)[16]) {
+        const f32x2 nmbx2 = make_f32x2(-mb, -mb);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float a0, a1;
+          split_f32x2(fma_f32x2(make_f32x2(x[c * 32 + e], x[c * 32 + e + 1]), sl2x2, nmbx2), a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          rs2[(e >> 1) & 3] = add_f32x2(rs2[(e >> 1) & 3], make_f32x2(p0, p1));
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+        }
+      };
+      auto sum4 = [](const f32x2 (&rs2)[4]) {
+        float lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_f32x2(rs2[i], lo[i], hi[i]);
+        return ((lo[0] + hi[0]) + (lo[1] + hi[1])) + ((lo[2] + hi[2]) + (lo[3] + hi[3]));
+      };
+      auto signal = [&](int b) {
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(b + t));
+      };
+      // Wholly visible tile, running max already set: keys 0-63 are
+      // exponentiated against the running max m without first taking their
+      // max; their row sum bounds every one of them, and the max of keys
+      // 64-127 (computed while those exponentials run) bounds the rest.  If
+      // every P stays below 2^16 the tile keeps m, and no max stands between
+      // the scores and the first exponential.  Otherwise the warp reloads S
+      // and takes the exact path below.  O and l grow by at most 2^16 per
+      // key relative to m, far inside fp32 range, and the final
+      // normalisation uses the same m, so the result is exact.
+      if (full && warp_all(m != -INFINITY)) {
+        tmem_ld32(tSt, col32(0));
+        tmem_ld32(tSt + 32, col32(1));
+        tmem_wait_ld();
+        reg_fence(col32(0));
+        reg_fence(col32(1));
+        tmem_ld32(tSt + 64, col32(2));   // in flight while keys 0-63 are exponentiated
+        tmem_ld32(tSt + 96, col32(3));
+        f32x2 rs2[4] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
+        uint32_t pk0[16], pk1[16];
+        exp32(0, m, rs2, pk0);
+        exp32(1, m, rs2, pk1);
+        tmem_wait_ld();
+        reg_fence(col32(2));
+        reg_fence(col32(3));
+        float m4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m4[i] = fmaxf(x[64 + i], x[68 + i]);
+#pragma unroll
+        for (int e = 72; e < BN; e += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[e + i], x[e + 4 + i]);
+        const float mx_hi = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float s_lo = sum4(rs2);
+        if (warp_all(s_lo < 65536.f && mx_hi * sl2 < m + 16.f)) {
+          tmem_st16(tSt, pk0);
+          tmem_st16(tSt + 16, pk1);
+          signal(BAR_P_HALF);
+          f32x2 rh[4] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
+          exp32(2, m, rh, pk0);
+          tmem_st16(tSt + 32, pk0);
+          exp32(3, m, rh, pk1);
+          tmem_st16(tSt + 48, pk1);
+          signal(BAR_P_FULL);
+          l += s_lo + sum4(rh);
+          ++k;
+          return;
+        }
+      }
+      // Exact path: masked tiles, the first tile of a row, and wholly visible
+      // tiles whose scores outgrew the running max.
       const int c_lo = my_lo - kpos0;
       const int c_hi = min(my_pos - kpos0, klen - 1);
       // S row -> registers: four 32-column loads in flight, one wait.
-      uint32_t sr[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tSt + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tSt + c * 32, col32(c));
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      float* x = reinterpret_cast<float*>(sr);
+      for (int c = 0; c < BN / 32; ++c) reg_fence(col32(c));
       if (!full) {
 #pragma unroll
         for (int e = 0; e < BN; ++e)
@@ -435,23 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       const float mb = (m == -INFINITY) ? 0.f : m;
-      // P = exp2(S*scale*log2e - m) -> packed bf16 into the first 64 columns
-      // of S (already read into registers).
-      // Pairs of columns go through packed fp32x2 fma/add (half the issue
-      // slots of scalar code); exp2 stays per element on the MUFU pipe.
-      const f32x2 sl2x2 = make_f32x2(sl2, sl2), nmbx2 = make_f32x2(-mb, -mb);
+      // P is written packed into the first 64 columns of S (already read
+      // into registers).
       f32x2 rs2[4] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
       auto exp_chunk = [&](int c) {
         uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float a0, a1;
-          split_f32x2(fma_f32x2(make_f32x2(x[c * 32 + e], x[c * 32 + e + 1]), sl2x2, nmbx2), a0, a1);
-          const float p0 = ex2_approx(a0);
-          const float p1 = ex2_approx(a1);
-          rs2[(e >> 1) & 3] = add_f32x2(rs2[(e >> 1) & 3], make_f32x2(p0, p1));
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-        }
+        exp32(c, mb, rs2, pk);
         tmem_st16(tSt + c * 16, pk);
       };
       exp_chunk(0);
@@ -470,20 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tOt + c * 32, ov);
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_HALF + t));
+      signal(BAR_P_HALF);
       exp_chunk(2);
       exp_chunk(3);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
-      float rs_lo[4], rs_hi[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) split_f32x2(rs2[i], rs_lo[i], rs_hi[i]);
-      l = l * alpha + (((rs_lo[0] + rs_hi[0]) + (rs_lo[1] + rs_hi[1])) + ((rs_lo[2] + rs_hi[2]) + (rs_lo[3] + rs_hi[3])));
+      signal(BAR_P_FULL);
+      l = l * alpha + sum4(rs2);
       ++k;
     });
     if (ok && k > 0) {

@@ -60,6 +60,40 @@ def test_fwd_matches_oracle(cpa, case, out_fp32):
     gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name, bf16_out=not out_fp32)
 
 
+JUMP_CASES = [
+    # name, L, R, layout, docs, spike keys (position, size) or None for a ramp
+    ("spikes_zigzag_R2", 2048, 2, 1, None, [(200, 6.0), (330, 12.0), (777, 18.0), (1500, 24.0)]),
+    ("spikes_docs_R1", 1536, 1, 0, [0, 700, 1536], [(100, 8.0), (420, 16.0), (900, 8.0), (1190, 20.0)]),
+    ("ramp_R1", 1536, 1, 0, None, None),
+]
+
+
+@pytest.mark.parametrize("case", JUMP_CASES, ids=[c[0] for c in JUMP_CASES])
+def test_fwd_running_max_jumps(cpa, case):
+    """Scores far above the running max inside wholly visible key tiles, in
+    their first or their second 64 keys (spikes), and scores that climb
+    steadily along the sequence (ramp).  Every query and key shares a
+    component mu, and chosen keys carry a multiple of it, so their score
+    exceeds the rest by about 4 log2 units per unit of size."""
+    import gpu_harness as gh
+    name, L, R, layout, docs, spikes = case
+    Hq, Hkv, d = 4, 2, 128
+    inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(name.encode()) % 1000)
+    mu = torch.full((d,), 0.5)
+    size = torch.zeros(L)
+    if spikes is None:
+        size = torch.arange(L, dtype=torch.float32) * (12.0 / L)
+    else:
+        for pos, a in spikes:
+            size[pos] = a
+    q = (inp["q"].float() + mu).bfloat16()
+    k = (inp["k"].float() + size[:, None, None] * mu).bfloat16()
+    plan = cpa.Plan(L, Hq, Hkv, d, ring_degree=R, layout=layout, doc_offsets=docs)
+    O, LSE = gh.fwd(plan, q, k, inp["v"])
+    O_ref, LSE_ref = oracle.attention(q, k, inp["v"], offsets=docs)
+    gh.assert_close(O.numpy(), LSE.numpy(), O_ref, LSE_ref, name, bf16_out=True)
+
+
 BALANCED_CASES = [
     # name, L, Hq, Hkv, d, U, R, chunks_per_rank, docs, emit_partials
     ("balanced_docs_m3", 1536, 8, 2, 128, 1, 2, 3, [0, 200, 1100, 1536], False),
