@@ -181,7 +181,8 @@ __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdArgs args) {
   using SM = FwdSmem<D>;
   constexpr int NH = D / 64;  // 64-column halves of a head row
   extern __shared__ uint8_t smem_raw[];
@@ -556,6 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = has ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
       const bool partial = args.o_part != nullptr;
       const int q_slot = it.q0 + t * BM + row;
+      // bf16 O of a warp whose 32 rows are all valid goes through shared
+      // memory (this query tile's Q buffer, free once every MMA completed)
+      // in the 128-byte-swizzled layout of the O map, then out with two TMA
+      // stores of 32 rows x 64 columns: whole 128-byte lines instead of one
+      // 16-byte piece of 32 different rows per store instruction.
+      const bool o_tma = !partial && !args.o_fp32 && warp_all(row_valid);
+      const uint32_t o_sm = sQ + t * SM::kQ + row * 128;
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         if (k > 0) {
@@ -574,6 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* dst = args.o_part + (part_row * g.Hq_loc + h) * D + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        } else if (o_tma) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            const int cc = c * 32 + e;                    // first column of this 16-byte piece
+            const int piece = (cc & 63) >> 3;              // 16-byte piece within the 128-byte line
+            st_shared_v4(o_sm + (cc >> 6) * HALF_BYTES + ((piece ^ (row & 7)) << 4), pack_bf16x2(o[e], o[e + 1]),
+                         pack_bf16x2(o[e + 2], o[e + 3]), pack_bf16x2(o[e + 4], o[e + 5]),
+                         pack_bf16x2(o[e + 6], o[e + 7]));
+          }
         } else if (args.o_fp32) {
           float* dst = reinterpret_cast<float*>(args.o) + (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
 #pragma unroll
@@ -587,6 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
                            pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
         }
+      }
+      if (o_tma) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = a * g.T + it.q0 + t * BM + wq * 32;
+          if (CP_IN_BOUNDS(y >= 0 && y + 32 <= q_rows, status)) {
+            for (int hh = 0; hh < NH; ++hh)
+              tma_store_2d(&tm_o, sQ + t * SM::kQ + hh * HALF_BYTES + wq * 32 * 128, h * D + hh * 64, y);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+        }
+        __syncwarp();
       }
       if (row_valid && CP_IN_BOUNDS(q_slot < g.T, status)) {
         if (partial && rank_local)
@@ -614,11 +645,19 @@ int launch_d(const FwdArgs& a, cudaStream_t stream) {
   // that rank's T rows and the visiting chunk's T rows.
   const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T) : static_cast<uint64_t>(g.R) * g.U * g.T;
   const uint64_t kv_rows = a.rank_local ? rows : g.kv_global ? static_cast<uint64_t>(g.L) : rows;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
       !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows) ||
       !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows))
     return CP_ERR_CUDA;
+  // bf16 O: the map of the TMA stores (32-row boxes), same shape as Q's.
+  // Partial and fp32 outputs are written with plain stores; the map then
+  // just repeats Q's.
+  if (!a.o_part && !a.o_fp32) {
+    if (!make_tile_map(&mo, a.o, static_cast<uint64_t>(g.Hq_loc) * D, rows, 32)) return CP_ERR_CUDA;
+  } else {
+    mo = mq;
+  }
   const uint32_t smem = FwdSmem<D>::kBytes;
   static bool attr_set = false;
   if (!attr_set) {
@@ -629,7 +668,7 @@ int launch_d(const FwdArgs& a, cudaStream_t stream) {
   const long long grid = static_cast<long long>(a.n_items) * g.Hq_loc;
   if (grid <= 0) return CP_OK;
   if (grid > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
-  attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mq, mk, mv, a);
+  attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mq, mk, mv, mo, a);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 

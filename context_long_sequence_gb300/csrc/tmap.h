@@ -23,13 +23,14 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D bf16 map over a [rows][cols] row-major matrix: box 64 columns (128
-// bytes) x 128 rows, 128-byte swizzle, zero fill outside the matrix.
-inline bool make_tile_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// bytes) x box_rows rows (128 unless stated), 128-byte swizzle, zero fill
+// outside the matrix.
+inline bool make_tile_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
