@@ -74,7 +74,8 @@ enum Bar {
   BAR_P_FULL = 3 + kTileBars + kSlots,     // +query tile
   BAR_DRAIN = 5 + kTileBars + kSlots,      // every MMA of the CTA completed
   BAR_P_HALF = 6 + kTileBars + kSlots,     // +query tile: P of keys 0-63 written
-  NUM_BARS = 8 + kTileBars + kSlots
+  BAR_O0 = 8 + kTileBars + kSlots,         // every MMA of query tile 0 completed
+  NUM_BARS = 9 + kTileBars + kSlots
 };
 
 template <int D>
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int blk_qp_last = win0.qp0 + it.len - 1;
 
   if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
     mbar_init(bar(BAR_Q), 1);
     for (int i = 0; i < kTileBars; ++i) mbar_init(bar(BAR_T_FULL + i), 1);
     for (int i = 0; i < kSlots; ++i) mbar_init(bar(BAR_KV_EMPTY + i), 1);
@@ -247,13 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_P_HALF + i), 4);
     }
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_O0), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
+    // The query tiles' loads go out before the TMEM allocation and the
+    // block-wide barrier, whose latency they then overlap.
+    mbar_arrive_expect_tx(bar(BAR_Q), 2 * SM::kQ);
+    const int qrow = q_row0 + it.q0;
+    for (int t = 0; t < 2; ++t) {
+      (void)CP_IN_BOUNDS(t * BM >= it.len || (qrow + t * BM >= 0 && qrow + t * BM < q_rows), status);
+      for (int hh = 0; hh < NH; ++hh)
+        tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -269,13 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(BAR_Q), 2 * SM::kQ);
-      const int qrow = q_row0 + it.q0;
-      for (int t = 0; t < 2; ++t) {
-        (void)CP_IN_BOUNDS(t * BM >= it.len || (qrow + t * BM >= 0 && qrow + t * BM < q_rows), status);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
-      }
       // Key tile nt: K into slot of load 2nt, V into slot of load 2nt+1, both
       // completing one tile barrier, so the issuer waits once per tile.  The
       // two slots were last used by V of tile nt-3 and K of tile nt-2, so the
@@ -377,8 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (v1) pend_sl = vslot;
           ++j;
         });
-        if (ok && pend_sl >= 0 && !warp_all(*abort_flag != 0)) issue_pv(1, pend_sl, true);
       }
+      // Query tile 0 has no MMA left: its epilogue overlaps the last softmax
+      // and PV of tile 1.
+      mma_commit_warp(bar(BAR_O0));
+      if (ok && pend_sl >= 0 && !warp_all(*abort_flag != 0)) issue_pv(1, pend_sl, true);
       // Every MMA issued so far completes before TMEM and shared memory are released.
       mma_commit_warp(bar(BAR_DRAIN));
       mbar_wait(bar(BAR_DRAIN), 0, nullptr, status);
@@ -547,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
     });
     if (ok && k > 0) {
-      // All MMAs of the CTA, the last PV_t among them, have completed.
-      ok = warp_all(mbar_wait(bar(BAR_DRAIN), 0, abort_flag, status));
+      // Every MMA of this query tile, its last PV_t among them, has completed.
+      ok = warp_all(mbar_wait(bar(t ? BAR_DRAIN : BAR_O0), 0, abort_flag, status));
       if (ok) tc_fence_after();
     }
     if (ok) {
@@ -564,13 +569,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16-byte piece of 32 different rows per store instruction.
       const bool o_tma = !partial && !args.o_fp32 && warp_all(row_valid);
       const uint32_t o_sm = sQ + t * SM::kQ + row * 128;
+      uint32_t oall[D];  // the row of O: every 32-column load in flight, one wait
+      if (k > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tOt + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&oall[c * 32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&oall[c * 32]));
+      }
+#pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        if (k > 0) {
-          tmem_ld32(tOt + c * 32, ov);
-          tmem_wait_ld();
-          reg_fence(ov);
-        }
+        const uint32_t* ov = &oall[c * 32];
         if (!row_valid) continue;
         if (!CP_IN_BOUNDS(q_slot < g.T && (!partial || r * g.R + s_begin < g.R * g.R), status)) continue;
         float o[32];
