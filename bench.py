@@ -9,7 +9,7 @@ N(0,1) tensors resident in HBM; L2 is flushed (a 256 MiB write) before every
 timed step and the flush is outside the step's CUDA-event bracket.
 
 The default workload is the largest one that fits one GPU: USP (Ulysses 4 x
-ring 8, zigzag) over L = 1,048,576 tokens.  After it, the other four
+ring 8, zigzag) over L = 1,048,576 tokens.  Before it, the other four
 workloads are measured in the same run (``per_config``): the 1K-token
 emit-partials ring, the 16K Ulysses forward, the 64K zigzag ring forward
 with its backward, and the 128K packed-document ring.
@@ -449,6 +449,22 @@ def main():
     if (world > 1 or args.transport) and transport_eligible(w, args, world):
         return run_transport(args, w, offsets, flops_fwd, flops_step, warmup, world, rank, dev, dist)
 
+    # The other workloads first, each on its own buffers (freed afterwards):
+    # their short launches then start from the thermal state a run of their
+    # own would see, not from the end of the main workload's minutes at the
+    # power cap.
+    per_config = {}
+    if not args.no_per_config and not args.L and rank == 0:
+        flush0 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        timer0 = Timer(torch, dev, torch.cuda.current_stream(dev), flush0)
+        peaks0, peak_src0 = load_peaks()
+        for ow in workloads.WORKLOADS:
+            if ow.name == w.name:
+                continue
+            per_config[ow.name] = measure_other_workload(cpa, torch, ow, dev, timer0, peaks0, peak_src0)
+        del flush0, timer0
+        torch.cuda.empty_cache()
+
     plan = make_plan(cpa, w, offsets, args.chunks_per_rank, args.kv_exchange)
     # Independent replica per GPU (the emulated ranks all live on one GPU):
     # each rank draws its own sequence.
@@ -683,17 +699,10 @@ def main():
             meta["input_sha256"] = sha256_tensors(cpu)
             meta["input_sha256_of"] = "global-order bf16 tensors as drawn (before sharding), raw bytes"
 
-    # Free the main workload before the others are measured.
     del q, k, v, o, lse, ws, g_inputs, set0
     if w.backward:
         del do, dq, dk, dv, ws_bwd
     torch.cuda.empty_cache()
-    per_config = {}
-    if not args.no_per_config and not args.L and rank == 0:
-        for ow in workloads.WORKLOADS:
-            if ow.name == w.name:
-                continue
-            per_config[ow.name] = measure_other_workload(cpa, torch, ow, dev, timer, peaks, peak_src)
 
     result = None
     if rank == 0:
