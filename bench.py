@@ -449,10 +449,10 @@ def main():
     if (world > 1 or args.transport) and transport_eligible(w, args, world):
         return run_transport(args, w, offsets, flops_fwd, flops_step, warmup, world, rank, dev, dist)
 
-    # The other workloads first, each on its own buffers (freed afterwards):
-    # their short launches then start from the thermal state a run of their
-    # own would see, not from the end of the main workload's minutes at the
-    # power cap.
+    # The other workloads first, each on its own buffers, freed before the
+    # default workload's inputs are drawn.  Each is timed over up to 50
+    # back-to-back launches (about half a second of work), long enough for
+    # the power cap to act on the larger ones.
     per_config = {}
     if not args.no_per_config and not args.L and rank == 0:
         flush0 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
