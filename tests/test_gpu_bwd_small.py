@@ -37,6 +37,9 @@ CASES = [
     ("ulysses_U4_gqa_d128", 1024, 8, 4, 128, 4, 1, 0, None, 1.0),
     ("usp_U2xR2_zigzag_docs_d64", 1536, 8, 2, 64, 2, 2, 1, [0, 500, 520, 1536], 1.0),
     ("usp_U2xR3_ragged_d128", 1440, 4, 2, 128, 2, 3, 0, [0, 711, 1440], 0.5),
+    # Eight query heads per KV head (the whole group on one Ulysses member).
+    ("gqa8_zigzag_docs_d128", 1536, 8, 1, 128, 1, 3, 1, [0, 900, 1536], 1.0),
+    ("gqa8_usp_U2xR2_d64", 1024, 16, 2, 64, 2, 2, 1, None, 1.0),
 ]
 
 

@@ -44,6 +44,8 @@ CASES = [
     ("single_ragged_tile", 72, 2, 1, 128, 1, 1, 0, None, False),
     ("partials_ragged_d128", 600, 4, 4, 128, 1, 3, 0, None, True),
     ("contig_ring_R5_docs", 1280, 4, 2, 64, 1, 5, 0, [0, 5, 6, 640, 1279, 1280], False),
+    ("gqa8_zigzag_docs_d128", 1536, 8, 1, 128, 1, 3, 1, [0, 900, 1536], False),
+    ("gqa8_usp_U2xR2_d64", 1024, 16, 2, 64, 2, 2, 1, None, False),
 ]
 
 
