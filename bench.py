@@ -360,7 +360,8 @@ def measure_other_workload(cpa, torch, w, dev, timer, peaks, peak_src):
            "fwd_frac": round(flops / fwd_ms / 1e9 / peak, 4), "peak": peak, "peak_source": plabel,
            "tokens_per_s": round(w.L / (fwd_ms * 1e-3), 1),
            "step": "emit-partials + merge" if w.emit_partials else
-                   ("reshard in, attention, reshard out" if w.ulysses > 1 else "attention (fused merge)")}
+                   ("attention; Ulysses exchanges in its loads and stores" if w.ulysses > 1
+                    else "attention (fused merge)")}
     if w.backward:
         do = g["do"][idx].contiguous()
         dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
@@ -626,15 +627,13 @@ def main():
         if args.kv_exchange == "allgather":  # the attention alone reads the gathered K/V (position order)
             kh, vh = g_inputs["k"], g_inputs["v"]
 
-    if U > 1:
-        # The attention alone reads the real head-sharded inputs (tensor-core
-        # power, and so the clock under the power cap, depends on the data).
-        cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh),
-                                         (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh),
-                                         (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, v, vh)],
-                                  stream=stream)
     reps = reps_for(mean_step_ms, 10)
-    attn_ms = timer(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
+    if U > 1:
+        # The forward is one launch (the Ulysses exchanges are the kernel's
+        # addressing): the attention alone is cp_attn_fwd itself.
+        attn_ms = timer(fwd, reps)
+    else:
+        attn_ms = timer(lambda: cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh, stream=stream), reps)
     kern["attn_fwd"] = {"ms": attn_ms, "tflops": flops_fwd / attn_ms / 1e9, "reps": reps}
     if U == 1 and not w.emit_partials:
         # Each ring rank's share alone (cp_attn_fwd_rank): the forward time of
@@ -708,11 +707,11 @@ def main():
     if rank == 0:
         ms_per_step = total_ms / args.steps
         value = aggregate_value(flops_step, world, ms_per_step)
-        # forward: attention, plus one batched reshard in (Q, K, V) and one out
-        # (O, LSE) when U > 1; merge with partials; two gathers with the
-        # all-gather exchange.  backward: delta, dkv, dq, plus one batched
-        # reshard in and one out when U > 1.
-        launches_per_step = ((3 if U > 1 else 1) + (1 if w.emit_partials else 0)
+        # forward: attention (with U > 1 the Ulysses exchanges are its
+        # addressing); merge with partials; two gathers with the all-gather
+        # exchange.  backward: delta, dkv, dq, plus one batched reshard in and
+        # one out when U > 1.
+        launches_per_step = (1 + (1 if w.emit_partials else 0)
                              + (2 if args.kv_exchange == "allgather" else 0)
                              + ((3 + (2 if U > 1 else 0)) if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12

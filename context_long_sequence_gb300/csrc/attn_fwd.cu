@@ -226,10 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Rank-local mode: Q row a*T + t is row t of the rank's buffer, and K/V
   // row a_src*T + t of the visiting chunk (a_src = ((r - step) mod R)*U + u)
   // is row t of the chunk buffer.
-  const int q_row0 = rank_local ? 0 : a * g.T;
+  // Sequence-sharded tensors (seq_io): ring rank r's slots are rows r*T ..
+  // r*T + T-1 and member u's heads a column range of the full head count.
+  const bool seq_io = args.seq_io != 0;
+  const int q_row0 = rank_local ? 0 : (seq_io ? r : a) * g.T;
   const int kv_sub = rank_local ? (((r - s_begin + g.R) % g.R) * g.U + u) * g.T : 0;
-  [[maybe_unused]] const int q_rows = rank_local ? g.T : g.R * g.U * g.T;       // rows of Q
-  [[maybe_unused]] const int kv_rows = rank_local ? g.T : g.kv_global ? g.L : g.R * g.U * g.T;  // rows of K/V
+  [[maybe_unused]] const int q_rows = rank_local ? g.T : (seq_io ? g.R : g.R * g.U) * g.T;  // rows of Q
+  [[maybe_unused]] const int kv_rows =
+      rank_local ? g.T : g.kv_global ? g.L : (seq_io ? g.R : g.R * g.U) * g.T;             // rows of K/V
+  // First column of this head in Q and O, and of its KV head in K and V.
+  auto qcol0 = [&]() { return (seq_io ? u * g.Hq_loc + h : h) * D; };
+  auto kvcol0 = [&]() { return (seq_io ? u * g.Hkv_loc + h / g.G : h / g.G) * D; };
   const int hkv = h / g.G;
 
   // The two query tiles' windows; the block walks the keys in [lo_min of
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       (void)CP_IN_BOUNDS(t * BM >= it.len || (qrow + t * BM >= 0 && qrow + t * BM < q_rows), status);
       for (int hh = 0; hh < NH; ++hh)
-        tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), h * D + hh * 64, qrow + t * BM);
+        tma_load_2d(sQ + t * SM::kQ + hh * HALF_BYTES, &tm_q, bar(BAR_Q), qcol0() + hh * 64, qrow + t * BM);
     }
   }
   if (warp == 1) {
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nt = 0;  // key tiles issued
       for_each_kv_tile(g, r, u, s_begin, s_end, blk_lo_min, blk_qp_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
-        const int kv_row = kv_row_all - kv_sub;
+        // kv_row_all = (src*U + u)*T + slot in the head-sharded row space.
+        const int kv_row = seq_io ? (kv_row_all / (g.T * g.U)) * g.T + kv_row_all % g.T : kv_row_all - kv_sub;
         const int slk = slot_of(n), slv = slot_of(n + 1);
         if (!mbar_wait(bar(BAR_KV_EMPTY + slk), parity_of(n) ^ 1, abort_flag, status)) return;
         if (!mbar_wait(bar(BAR_KV_EMPTY + slv), parity_of(n + 1) ^ 1, abort_flag, status)) return;
@@ -294,9 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(tb, 2 * SM::kKV);
         (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < kv_rows && hkv < g.Hkv_loc, status);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sKV + slk * SM::kKV + hh * HALF_BYTES, &tm_k, tb, hkv * D + hh * 64, kv_row);
+          tma_load_2d(sKV + slk * SM::kKV + hh * HALF_BYTES, &tm_k, tb, kvcol0() + hh * 64, kv_row);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sKV + slv * SM::kKV + hh * HALF_BYTES, &tm_v, tb, hkv * D + hh * 64, kv_row);
+          tma_load_2d(sKV + slv * SM::kKV + hh * HALF_BYTES, &tm_v, tb, kvcol0() + hh * 64, kv_row);
         n += 2;
         ++nt;
       });
@@ -562,6 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = has ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
       const bool partial = args.o_part != nullptr;
       const int q_slot = it.q0 + t * BM + row;
+      // This row's O (element offset) and LSE index in the output layout.
+      const int Hq_all = g.Hq_loc * g.U;
+      const size_t o_row_off =
+          seq_io ? (static_cast<size_t>(q_row0 + q_slot) * Hq_all + u * g.Hq_loc + h) * D
+                 : (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D;
+      const int n_mem = g.T / g.U;  // slots per attention rank (sequence-sharded LSE rows)
+      const size_t lse_idx =
+          seq_io ? (static_cast<size_t>(r * g.U + q_slot / n_mem) * Hq_all + u * g.Hq_loc + h) * n_mem + q_slot % n_mem
+                 : (static_cast<size_t>(a) * g.Hq_loc + h) * g.T + q_slot;
       // bf16 O of a warp whose 32 rows are all valid goes through shared
       // memory (this query tile's Q buffer, free once every MMA completed)
       // in the 128-byte-swizzled layout of the O map, then out with two TMA
@@ -601,12 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pack_bf16x2(o[e + 6], o[e + 7]));
           }
         } else if (args.o_fp32) {
-          float* dst = reinterpret_cast<float*>(args.o) + (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
+          float* dst = reinterpret_cast<float*>(args.o) + o_row_off + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         } else {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) +
-                               (static_cast<size_t>(a * g.T + q_slot) * g.Hq_loc + h) * D + c * 32;
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) + o_row_off + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 8)
             *reinterpret_cast<uint4*>(dst + e) =
@@ -618,10 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int y = a * g.T + it.q0 + t * BM + wq * 32;
+          const int y = q_row0 + it.q0 + t * BM + wq * 32;
           if (CP_IN_BOUNDS(y >= 0 && y + 32 <= q_rows, status)) {
             for (int hh = 0; hh < NH; ++hh)
-              tma_store_2d(&tm_o, sQ + t * SM::kQ + hh * HALF_BYTES + wq * 32 * 128, h * D + hh * 64, y);
+              tma_store_2d(&tm_o, sQ + t * SM::kQ + hh * HALF_BYTES + wq * 32 * 128, qcol0() + hh * 64, y);
             bulk_commit();
             bulk_wait_read_all();
           }
@@ -634,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (partial)
           args.lse_part[(static_cast<size_t>(r * g.R + s_begin) * g.Hq_loc + h) * g.T + q_slot] = lse;
         else
-          args.lse[(static_cast<size_t>(a) * g.Hq_loc + h) * g.T + q_slot] = lse;
+          args.lse[lse_idx] = lse;
       }
     }
   }
@@ -652,18 +668,22 @@ int launch_d(const FwdArgs& a, cudaStream_t stream) {
   const AttnGeom& g = a.g;
   // Rows of Q and of K/V: every rank's slots, or (one ring step of one rank)
   // that rank's T rows and the visiting chunk's T rows.
-  const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T) : static_cast<uint64_t>(g.R) * g.U * g.T;
+  // With seq_io the maps span the sequence-sharded tensors: R*T rows of all
+  // heads.
+  const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T)
+                                     : static_cast<uint64_t>(g.R) * (a.seq_io ? 1 : g.U) * g.T;
   const uint64_t kv_rows = a.rank_local ? rows : g.kv_global ? static_cast<uint64_t>(g.L) : rows;
+  const uint64_t hq_cols = static_cast<uint64_t>(g.Hq_loc) * (a.seq_io ? g.U : 1) * D;
+  const uint64_t hkv_cols = static_cast<uint64_t>(g.Hkv_loc) * (a.seq_io ? g.U : 1) * D;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
-      !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows) ||
-      !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, kv_rows))
+  if (!make_tile_map(&mq, a.q, hq_cols, rows) || !make_tile_map(&mk, a.k, hkv_cols, kv_rows) ||
+      !make_tile_map(&mv, a.v, hkv_cols, kv_rows))
     return CP_ERR_CUDA;
   // bf16 O: the map of the TMA stores (32-row boxes), same shape as Q's.
   // Partial and fp32 outputs are written with plain stores; the map then
   // just repeats Q's.
   if (!a.o_part && !a.o_fp32) {
-    if (!make_tile_map(&mo, a.o, static_cast<uint64_t>(g.Hq_loc) * D, rows, 32)) return CP_ERR_CUDA;
+    if (!make_tile_map(&mo, a.o, hq_cols, rows, 32)) return CP_ERR_CUDA;
   } else {
     mo = mq;
   }

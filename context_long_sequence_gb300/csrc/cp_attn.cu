@@ -319,7 +319,7 @@ int check_device(const cp_plan* p) {
 }
 
 struct FwdWorkspace {
-  size_t qh, kh, vh, oh, lseh, opart, lsepart, kall, vall, total;
+  size_t opart, lsepart, kall, vall, total;
 };
 
 FwdWorkspace fwd_workspace(const cp_plan* p) {
@@ -332,13 +332,6 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
     off += align256(bytes);
     return at;
   };
-  if (d.ulysses_degree > 1) {
-    w.qh = take(L * d.Hq * d.d * 2);
-    w.kh = take(L * d.Hkv * d.d * 2);
-    w.vh = take(L * d.Hkv * d.d * 2);
-    w.oh = take(L * d.Hq * d.d * (d.out_fp32 ? 4 : 2));
-    w.lseh = take(L * d.Hq * 4);
-  }
   if (d.emit_partials) {
     w.opart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * d.d * 4);
     w.lsepart = take(static_cast<size_t>(d.ring_degree) * L * d.Hq * 4);
@@ -685,36 +678,23 @@ int cp_attn_fwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
     NvtxRange phase("attention");
     return cpattn::launch_attn_fwd(a, stream);
   }
-  // Ulysses / USP: reshard in, ring attention per head group, reshard out.
-  const int R = d.ring_degree, U = d.ulysses_degree;
-  void* qh = ws + w.qh;
-  void* kh = ws + w.kh;
-  void* vh = ws + w.vh;
-  void* oh = ws + w.oh;
-  float* lseh = reinterpret_cast<float*>(ws + w.lseh);
-  // The Ulysses exchanges of every ring group, all tensors of one exchange
-  // in one launch: Q, K, V before attention, O and LSE after it.
-  {
-    NvtxRange phase("reshard_in");
-    const cpattn::ReshardSpec in[3] = {{d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, qh},
-                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, kh},
-                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, vh}};
-    if ((rc = cpattn::launch_reshard_batch(R, U, p->n, in, 3, stream, a.status))) return rc;
-  }
-  a.q = qh;
-  a.k = kh;
-  a.v = vh;
-  a.o = oh;
-  a.lse = lseh;
+  // Ulysses / USP: with every rank in this GPU's memory, the two exchanges
+  // ([MTX] "Split heads or rotate KV": tokens to heads before attention,
+  // heads to tokens after it) are the kernel's addressing.  Ring rank r's U
+  // members hold its T ring-local slots in order, so member u's head-sharded
+  // rows are the sequence-sharded rows r*T + t restricted to its heads: the
+  // kernel reads Q, K, V and writes O and LSE in the API layout directly.
+  // ulysses_reshard is the same exchange as a copy, for callers that want
+  // the head-sharded tensors (cp_attn_fwd_local, the backward).
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.seq_io = 1;
   set_fused_items(p, a);
-  {
-    NvtxRange phase("attention");
-    if ((rc = cpattn::launch_attn_fwd(a, stream))) return rc;
-  }
-  NvtxRange phase("reshard_out");
-  const cpattn::ReshardSpec out[2] = {{d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, d.out_fp32 ? 4 : 2, oh, o},
-                                      {d.Hq, 1, CP_HEAD_TO_SEQ, CP_HEAD_MAJOR, 4, lseh, lse}};
-  return cpattn::launch_reshard_batch(R, U, p->n, out, 2, stream, a.status);
+  NvtxRange phase("attention");
+  return cpattn::launch_attn_fwd(a, stream);
 }
 
 int cp_attn_fwd_local(const cp_plan_t* p, const void* q, const void* k, const void* v, void* o, float* lse,

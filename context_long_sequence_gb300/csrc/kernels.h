@@ -88,6 +88,13 @@ struct FwdArgs {
   // resident at once read the same K/V tiles.
   int stream_major;
   int n_items_u;
+  // seq_io = 1 (fused mode, U > 1): q, k, v, o and lse are the
+  // sequence-sharded API tensors, [R*T][Hq][d], [R*T][Hkv][d] and
+  // [R*U][Hq][n] (n = T/U), instead of head-sharded copies.  Ring rank r's
+  // U members hold its T ring-local slots in order, so slot t of ring rank r
+  // is row r*T + t, and member u's heads are the column range [u*Hq_loc,
+  // (u+1)*Hq_loc): the Ulysses exchange becomes the kernel's addressing.
+  int seq_io;
 };
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -191,9 +191,13 @@ int ulysses_reshard_batch(const cp_plan_t *plan, int n_jobs, const cp_reshard_jo
  *   k,v[P][n][Hkv][d] bf16
  *   o  [P][n][Hq][d]  bf16 out (fp32 if the plan's out_fp32 is set)
  *   lse[P][Hq][n]     fp32 out (natural log; -inf for a row with no visible key)
- * With U > 1 the call reshards Q, K, V to head-sharded layout in the
- * workspace, runs ring attention per head group and reshards O and LSE back
- * ([MTX] "Split heads or rotate KV": the two exchanges around attention).
+ * With U > 1 each Ulysses member u attends with its heads over the whole
+ * ring group's sequence ([MTX] "Split heads or rotate KV": the two
+ * exchanges around attention).  Every rank is in this GPU's memory, so the
+ * exchanges are the kernel's addressing: member u of ring rank r reads rows
+ * r*T .. r*T+T-1 of q, k, v (its group's slots, T = L/R) at its own heads
+ * and writes o and lse in place; no head-sharded copy is made (the copy is
+ * ulysses_reshard, for cp_attn_fwd_local and the backward).
  * Per ring rank r and step s the visiting chunk comes from rank (r-s) mod R;
  * with CP_KV_ALLGATHER the call first gathers K and V of all ranks into
  * position order in the workspace, and every rank's queries then walk the

@@ -197,6 +197,41 @@ def test_fwd_allgather_rank_by_rank(cpa):
     assert cpa.cp_get_status() == 0
 
 
+@pytest.mark.parametrize("U,R,layout,docs,Hq,Hkv,d", [(4, 1, 0, None, 8, 4, 128), (2, 2, 1, [0, 777, 2048], 8, 4, 128),
+                                                      (2, 3, 0, [0, 100, 1536], 4, 2, 64)])
+def test_usp_forward_equals_exchanges_around_local(cpa, U, R, layout, docs, Hq, Hkv, d):
+    """cp_attn_fwd on a Ulysses/USP plan reads and writes the sequence-sharded
+    tensors in place; it must equal, bit for bit, the explicit exchanges
+    (ulysses_reshard) around the head-sharded attention (cp_attn_fwd_local),
+    whose arithmetic is the same."""
+    L = 2048 if R == 2 else 1536 if R == 3 else 1024
+    inp = _inputs(L, Hq, Hkv, d, seed=zlib.crc32(f"usp_io_{U}_{R}".encode()) % 1000)
+    plan = cpa.Plan(L, Hq, Hkv, d, ulysses_degree=U, ring_degree=R, layout=layout, doc_offsets=docs)
+    idx = torch.from_numpy(plan.index_map().astype(np.int64))
+    q, k, v = (inp[n][idx].contiguous().cuda() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(plan.P, Hq, plan.n, dtype=torch.float32, device="cuda")
+    cpa.cp_attn_fwd(plan, q, k, v, o, lse, cpa.alloc_workspace(plan))
+    T = L // R
+    qh = torch.empty(R, U, T, Hq // U, d, dtype=torch.bfloat16, device="cuda")
+    kh = torch.empty(R, U, T, Hkv // U, d, dtype=torch.bfloat16, device="cuda")
+    vh = torch.empty_like(kh)
+    cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, Hq, d, 2, q, qh),
+                                     (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, Hkv, d, 2, k, kh),
+                                     (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, Hkv, d, 2, v, vh)])
+    oh = torch.empty_like(qh)
+    lh = torch.empty(R, U, Hq // U, T, dtype=torch.float32, device="cuda")
+    cpa.cp_attn_fwd_local(plan, qh, kh, vh, oh, lh)
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+    cpa.ulysses_reshard_batch(plan, [(cpa.CP_HEAD_TO_SEQ, cpa.CP_TOKEN_MAJOR, Hq, d, 2, oh, o2),
+                                     (cpa.CP_HEAD_TO_SEQ, cpa.CP_HEAD_MAJOR, Hq, 1, 4, lh, lse2)])
+    torch.cuda.synchronize()
+    assert cpa.cp_get_status() == 0
+    assert torch.equal(o, o2)
+    assert torch.equal(lse, lse2)
+
+
 def test_fwd_deterministic(cpa):
     import gpu_harness as gh
     inp = _inputs(1536, 8, 2, 128, seed=7)
