@@ -648,8 +648,9 @@ def main():
                             "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"
                                        + (" and 2 batched Ulysses reshards (6 tensors in, 3 out)" if U > 1 else "")}
     if U > 1:
-        # The two exchanges as cp_attn_fwd issues them: one launch for Q, K, V
-        # and one for O and LSE.
+        # The two exchanges as copies (ulysses_reshard, the form the backward
+        # and cp_attn_fwd_local callers use; the forward step folds them into
+        # the attention's addressing): one launch for Q, K, V, one for O, LSE.
         def rin():
             cpa.ulysses_reshard_batch(plan, [(cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hq, w.d, 2, q, qh),
                                              (cpa.CP_SEQ_TO_HEAD, cpa.CP_TOKEN_MAJOR, w.Hkv, w.d, 2, k, kh),
