@@ -645,8 +645,7 @@ def main():
     if w.backward:
         bwd_ms = timer(bwd, reps)
         kern["attn_bwd"] = {"ms": bwd_ms, "tflops": flops_fwd * BWD_FLOP_RATIO / bwd_ms / 1e9,
-                            "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"
-                                       + (" and 2 batched Ulysses reshards (6 tensors in, 3 out)" if U > 1 else "")}
+                            "kernels": "bwd_delta, attn_bwd_dkv, attn_bwd_dq"}
     if U > 1:
         # The two exchanges as copies (ulysses_reshard, the form the backward
         # and cp_attn_fwd_local callers use; the forward step folds them into
@@ -710,11 +709,11 @@ def main():
         value = aggregate_value(flops_step, world, ms_per_step)
         # forward: attention (with U > 1 the Ulysses exchanges are its
         # addressing); merge with partials; two gathers with the all-gather
-        # exchange.  backward: delta, dkv, dq, plus one batched reshard in and
-        # one out when U > 1.
+        # exchange.  backward: delta, dkv, dq (the exchanges again in their
+        # addressing).
         launches_per_step = (1 + (1 if w.emit_partials else 0)
                              + (2 if args.kv_exchange == "allgather" else 0)
-                             + ((3 + (2 if U > 1 else 0)) if w.backward else 0))
+                             + (3 if w.backward else 0))
         achieved = flops_fwd / (attn_ms * 1e-3) / 1e12
         peak, plabel = tensor_peak(peaks, peak_src, attn_ms)
         traffic, traffic_how = (None, None) if args.L else profiled_traffic(w.name)

@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
                                                         const __nv_bfloat16* __restrict__ dO,
                                                         const float* __restrict__ lse, float* __restrict__ nlse,
                                                         float* __restrict__ nd, const AttnGeom g, int chunk_pad,
-                                                        long long rows, int32_t* status) {
+                                                        long long rows, int seq_io, int32_t* status) {
   constexpr int E = D / 32;  // elements per lane
   const int H = g.Hq_loc, T = g.T;
   const int lane = threadIdx.x & 31;
@@ -98,16 +98,24 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
   for (long long wi = gtid >> 5; wi < total; wi += nwarps) {
     const long long row = wi / H;
     const int h = static_cast<int>(wi - row * H);
-    const OT* po = o + wi * D + lane * E;
-    const __nv_bfloat16* pd = dO + wi * D + lane * E;
+    // Row `row` = slot t of attention rank a (head-sharded enumeration);
+    // with seq_io the same row and head of the sequence-sharded tensors.
+    const long long a_r = row / T, t_r = row - a_r * T;
+    const long long io =
+        seq_io ? ((a_r / g.U) * T + t_r) * (static_cast<long long>(H) * g.U) + (a_r % g.U) * H + h : wi;
+    const OT* po = o + io * D + lane * E;
+    const __nv_bfloat16* pd = dO + io * D + lane * E;
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) acc = fmaf(to_f32(po[e]), __bfloat162float(pd[e]), acc);
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-      const long long r = row / T, t = row - r * T;
-      const long long li = (r * H + h) * T + t;
+      const long long r = a_r, t = t_r;
+      const long long n_m = T / g.U;  // slots per attention rank
+      const long long li = seq_io ? (((r / g.U) * g.U + t / n_m) * (static_cast<long long>(H) * g.U) +
+                                     (r % g.U) * H + h) * n_m + t % n_m
+                                  : (r * H + h) * T + t;
       const size_t di = ld_index(g, chunk_pad, static_cast<int>(r), h, static_cast<int>(t));
       if (CP_IN_BOUNDS(li >= 0 && li < total && di < static_cast<size_t>(ranks * H * tp), status)) {
         const float l = lse[li];
@@ -241,11 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.q0 + it.len <= g.T, status))
     return;
   const bool rank_local = args.rank_local != 0;
-  [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dQ
+  const bool seq_io = args.seq_io != 0;
+  // rows of Q, dO, K, V, dQ (sequence-sharded: ring rank r's slots are rows r*T..)
+  [[maybe_unused]] const int rows = rank_local ? g.T : (seq_io ? g.R : g.R * g.U) * g.T;
   const int a = it.a, r = a / g.U, u = a % g.U;  // rank a = ring rank r, Ulysses member u
   const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
   // Rank-local mode: the rank's rows start at 0, and so do the visiting chunk's.
-  const int q_row0 = rank_local ? 0 : a * g.T;
+  const int q_row0 = rank_local ? 0 : (seq_io ? r : a) * g.T;
   const int kv_sub = rank_local ? (((r - s_begin + g.R) % g.R) * g.U + u) * g.T : 0;
   const int qpos0 = slot_pos(g, r, it.q0);
   const int qpos_last = qpos0 + it.len - 1;
@@ -290,18 +300,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk = 0, nv = 0;
       for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
-        const int kv_row = kv_row_all - kv_sub;
+        // kv_row_all = (src*U + u)*T + slot in the head-sharded row space.
+        const int kv_row = seq_io ? (kv_row_all / (g.T * g.U)) * g.T + kv_row_all % g.T : kv_row_all - kv_sub;
+        const int kv_col = (seq_io ? u * g.Hkv_loc + hkv : hkv) * D;
         const int ks = nk % kKStages, vs = nv % kVStages;
         if (!mbar_wait(bar(DQ_K_EMPTY + ks), ((nk / kKStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(DQ_K_FULL + ks), SM::kT);
         (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < rows && hkv < g.Hkv_loc, status);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + ks), hkv * D + hh * 64, kv_row);
+          tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + ks), kv_col + hh * 64, kv_row);
         ++nk;
         if (!mbar_wait(bar(DQ_V_EMPTY + vs), ((nv / kVStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(DQ_V_FULL + vs), SM::kT);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sV + vs * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_V_FULL + vs), hkv * D + hh * 64, kv_row);
+          tma_load_2d(sV + vs * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_V_FULL + vs), kv_col + hh * 64, kv_row);
         ++nv;
       });
       if (*abort_flag) {
@@ -374,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_lo = (row_valid && g.doc_start) ? g.doc_start[my_pos] : 0;
     // -LSE*log2(e) and -D of this row, prepared by the delta pass.
     const size_t lrow = ld_index(g, args.chunk_pad, rank_local ? 0 : a, h, row_valid ? it.q0 + row : 0);
-    const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rows / g.T) * Hq * g.nchunks * args.chunk_pad,
+    const bool ld_ok = !row_valid || CP_IN_BOUNDS(lrow < static_cast<size_t>(rank_local ? 1 : g.R * g.U) * Hq *
+                                                             g.nchunks * args.chunk_pad,
                                                   status);
     const float nl2 = (row_valid && ld_ok) ? args.nlse[lrow] : -INFINITY;
     const float ndl = (row_valid && ld_ok) ? args.nd[lrow] : 0.f;
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bf16 pairs of a row in memory order are the packed columns).  Rows
       // past the tile's end are zero.
       constexpr int W = D / 4;  // 32-bit words per half row
-      const size_t grow = static_cast<size_t>(q_row0 + it.q0 + row) * Hq + h;
+      const size_t grow = static_cast<size_t>(q_row0 + it.q0 + row) * (seq_io ? Hq * g.U : Hq) + (seq_io ? u * Hq + h : h);
       const bool in = row_valid && CP_IN_BOUNDS(q_row0 + it.q0 + row < rows, status);
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q) + grow * D) + half * (W / 4);
       const uint4* dsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.dO) + grow * D) + half * (W / 4);
@@ -497,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Accumulate mode adds to dQ (nothing to add when no key tile was seen).
     if (ok && !(args.accumulate && n == 0)) {
-      float* dst = args.dq + (static_cast<size_t>(q_row0 + it.q0 + row) * Hq + h) * D;
+      float* dst = args.dq + (static_cast<size_t>(q_row0 + it.q0 + row) * (seq_io ? Hq * g.U : Hq) +
+                              (seq_io ? u * Hq + h : h)) * D;
       const bool store_ok = !row_valid || CP_IN_BOUNDS(q_row0 + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32];
@@ -651,11 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.q0 + it.len <= g.T, status))
     return;
   const bool rank_local = args.rank_local != 0;
-  [[maybe_unused]] const int rows = rank_local ? g.T : g.R * g.U * g.T;  // rows of Q, dO, K, V, dK, dV
+  const bool seq_io = args.seq_io != 0;
+  // rows of Q, dO, K, V, dK, dV (sequence-sharded: ring rank r's slots are rows r*T..)
+  [[maybe_unused]] const int rows = rank_local ? g.T : (seq_io ? g.R : g.R * g.U) * g.T;
   const int a = it.a, src = a / g.U, u = a % g.U;  // key tile of rank a = ring rank src, member u
   const int s_begin = rank_local ? args.step : 0, s_end = rank_local ? args.step + 1 : g.R;
   // Rank-local mode: the chunk's rows start at 0, and so do the holder's.
-  const int k_row0 = rank_local ? 0 : a * g.T;
+  const int k_row0 = rank_local ? 0 : (seq_io ? src : a) * g.T;
   const int kpos0 = slot_pos(g, src, it.q0);
   const int kpos_last = kpos0 + it.len - 1;
   if (!CP_IN_BOUNDS(kpos0 >= 0 && kpos_last < g.L, status)) return;
@@ -702,25 +718,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int krow = k_row0 + it.q0;
       (void)CP_IN_BOUNDS(krow >= 0 && krow < rows, status);
       for (int hh = 0; hh < NH; ++hh) {
-        tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), jh * D + hh * 64, krow);
-        tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), jh * D + hh * 64, krow);
+        const int kv_col = (seq_io ? u * Hkv + jh : jh) * D;
+        tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), kv_col + hh * 64, krow);
+        tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), kv_col + hh * 64, krow);
       }
       int nq = 0, ndo = 0, nld = 0;  // Q, dO and statistics loads issued
-      [[maybe_unused]] const size_t ld_total = static_cast<size_t>(rows / g.T) * Hq * g.nchunks * args.chunk_pad;
+      // statistics of every attention rank (one in rank-local mode)
+      [[maybe_unused]] const size_t ld_total =
+          static_cast<size_t>(rank_local ? 1 : g.R * g.U) * Hq * g.nchunks * args.chunk_pad;
       for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int rr, int qslot0, int qpos0, int qlen, int h) {
         if (*abort_flag) return;
         const int qs = nq % kQStages, ds = ndo % kDOStages;
-        const int qrow = (rank_local ? 0 : (rr * g.U + u) * g.T) + qslot0;
+        const int qrow = (rank_local ? 0 : (seq_io ? rr : rr * g.U + u) * g.T) + qslot0;
+        const int q_col = (seq_io ? u * Hq + h : h) * D;
         if (!mbar_wait(bar(KV_Q_EMPTY + qs), ((nq / kQStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(KV_Q_FULL + qs), SM::kT);
         (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows && h < Hq, status);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_Q_FULL + qs), h * D + hh * 64, qrow);
+          tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_Q_FULL + qs), q_col + hh * 64, qrow);
         ++nq;
         if (!mbar_wait(bar(KV_DO_EMPTY + ds), ((ndo / kDOStages) & 1) ^ 1, abort_flag, status)) return;
         mbar_arrive_expect_tx(bar(KV_DO_FULL + ds), SM::kT);
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_DO_FULL + ds), h * D + hh * 64, qrow);
+          tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_DO_FULL + ds), q_col + hh * 64, qrow);
         ++ndo;
         // The tile's -LSE*log2(e) and -D (128 each, chunk-padded so the copy
         // starts on a 512-byte boundary) and its position and length, for
@@ -940,7 +960,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Accumulate mode adds to dK and dV (nothing to add when no query tile was seen).
     if (ok && !(args.accumulate && n == 0)) {
-      const size_t orow = (static_cast<size_t>(k_row0 + it.q0 + row) * Hkv + jh) * D;
+      const size_t orow = (static_cast<size_t>(k_row0 + it.q0 + row) * (seq_io ? Hkv * g.U : Hkv) +
+                           (seq_io ? u * Hkv + jh : jh)) * D;
       const bool store_ok = !key_valid || CP_IN_BOUNDS(k_row0 + it.q0 + row < rows, status);
       for (int c4 = half * (D / 64); c4 < (half + 1) * (D / 64); ++c4) {
         uint32_t v[32], k[32];
@@ -996,11 +1017,13 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   // and one chunk's T rows.
   const uint64_t rows = a.rank_local ? static_cast<uint64_t>(g.T) : static_cast<uint64_t>(g.R) * g.U * g.T;
   const int phases = a.phases ? a.phases : 7;
+  // With seq_io the maps span the sequence-sharded tensors: R*T rows of all heads.
+  const uint64_t map_rows = a.seq_io ? static_cast<uint64_t>(g.R) * g.T : rows;
+  const uint64_t wq = static_cast<uint64_t>(g.Hq_loc) * (a.seq_io ? g.U : 1) * D;
+  const uint64_t wkv = static_cast<uint64_t>(g.Hkv_loc) * (a.seq_io ? g.U : 1) * D;
   CUtensorMap mq, mdo, mk, mv;
-  if (!make_tile_map(&mq, a.q, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
-      !make_tile_map(&mdo, a.dO, static_cast<uint64_t>(g.Hq_loc) * D, rows) ||
-      !make_tile_map(&mk, a.k, static_cast<uint64_t>(g.Hkv_loc) * D, rows) ||
-      !make_tile_map(&mv, a.v, static_cast<uint64_t>(g.Hkv_loc) * D, rows))
+  if (!make_tile_map(&mq, a.q, wq, map_rows) || !make_tile_map(&mdo, a.dO, wq, map_rows) ||
+      !make_tile_map(&mk, a.k, wkv, map_rows) || !make_tile_map(&mv, a.v, wkv, map_rows))
     return CP_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1020,11 +1043,11 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     if (grid > 0 && a.o_fp32)
       bwd_delta_kernel<D, float><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
           static_cast<const float*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.nlse, a.nd, g,
-          a.chunk_pad, static_cast<long long>(rows), a.status);
+          a.chunk_pad, static_cast<long long>(rows), a.seq_io, a.status);
     else if (grid > 0)
       bwd_delta_kernel<D, __nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.nlse, a.nd, g,
-          a.chunk_pad, static_cast<long long>(rows), a.status);
+          a.chunk_pad, static_cast<long long>(rows), a.seq_io, a.status);
   }
   const long long grid_kv = static_cast<long long>(a.n_items_kv) * g.Hkv_loc;
   const long long grid_q = static_cast<long long>(a.n_items_q) * g.Hq_loc;

@@ -345,7 +345,7 @@ FwdWorkspace fwd_workspace(const cp_plan* p) {
 }
 
 struct BwdWorkspace {
-  size_t nlse, nd, qh, kh, vh, oh, doh, lseh, dqh, dkh, dvh, total;
+  size_t nlse, nd, total;
 };
 
 // Query-tile-aligned length of one chunk in the backward's row statistics.
@@ -357,11 +357,9 @@ size_t rank_ld_floats(const cp_plan* p) {
   return static_cast<size_t>(p->desc.Hq / p->desc.ulysses_degree) * p->nchunks * chunk_pad_of(p);
 }
 
-// The row statistics (-LSE*log2e and -D, chunk-padded) always; with U > 1
-// also the head-sharded copies of the inputs and gradients.
+// The row statistics (-LSE*log2e and -D, chunk-padded).  With U > 1 the
+// kernels address the sequence-sharded tensors directly: no copies.
 BwdWorkspace bwd_workspace(const cp_plan* p) {
-  const cp_plan_desc_t& d = p->desc;
-  const size_t L = d.L;
   BwdWorkspace w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -371,17 +369,6 @@ BwdWorkspace bwd_workspace(const cp_plan* p) {
   };
   w.nlse = take(static_cast<size_t>(p->P) * rank_ld_floats(p) * 4);
   w.nd = take(static_cast<size_t>(p->P) * rank_ld_floats(p) * 4);
-  if (d.ulysses_degree > 1) {
-    w.qh = take(L * d.Hq * d.d * 2);
-    w.kh = take(L * d.Hkv * d.d * 2);
-    w.vh = take(L * d.Hkv * d.d * 2);
-    w.oh = take(L * d.Hq * d.d * (d.out_fp32 ? 4 : 2));
-    w.doh = take(L * d.Hq * d.d * 2);
-    w.lseh = take(L * d.Hq * 4);
-    w.dqh = take(L * d.Hq * d.d * 4);
-    w.dkh = take(L * d.Hkv * d.d * 4);
-    w.dvh = take(L * d.Hkv * d.d * 4);
-  }
   w.total = off;
   return w;
 }
@@ -787,43 +774,14 @@ int cp_attn_bwd(const cp_plan_t* p, const void* q, const void* k, const void* v,
   if (!a.status) return CP_ERR_CUDA;
   const cp_plan_desc_t& d = p->desc;
   NvtxRange call("cp_attn_bwd");
-  if (d.ulysses_degree == 1) {
-    NvtxRange phase("attention_bwd");
-    return cpattn::launch_attn_bwd(a, stream);
-  }
-  // Ulysses / USP: the forward's exchanges run in reverse for the gradients.
-  // Inputs (q, k, v, o, dO, LSE) go to the head-sharded layout, the ring
-  // backward runs per head group, and dQ, dK, dV come back token-sharded.
-  const int R = d.ring_degree, U = d.ulysses_degree, n = p->n;
-  const int ob = d.out_fp32 ? 4 : 2;
-  {
-    NvtxRange phase("reshard_in");
-    const cpattn::ReshardSpec in[6] = {{d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, q, ws + w.qh},
-                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, k, ws + w.kh},
-                                       {d.Hkv, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, v, ws + w.vh},
-                                       {d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, ob, o, ws + w.oh},
-                                       {d.Hq, d.d, CP_SEQ_TO_HEAD, CP_TOKEN_MAJOR, 2, dO, ws + w.doh},
-                                       {d.Hq, 1, CP_SEQ_TO_HEAD, CP_HEAD_MAJOR, 4, lse, ws + w.lseh}};
-    if ((rc = cpattn::launch_reshard_batch(R, U, n, in, 6, stream, a.status))) return rc;
-  }
-  a.q = ws + w.qh;
-  a.k = ws + w.kh;
-  a.v = ws + w.vh;
-  a.o = ws + w.oh;
-  a.dO = ws + w.doh;
-  a.lse = reinterpret_cast<const float*>(ws + w.lseh);
-  a.dq = reinterpret_cast<float*>(ws + w.dqh);
-  a.dk = reinterpret_cast<float*>(ws + w.dkh);
-  a.dv = reinterpret_cast<float*>(ws + w.dvh);
-  {
-    NvtxRange phase("attention_bwd");
-    if ((rc = cpattn::launch_attn_bwd(a, stream))) return rc;
-  }
-  NvtxRange phase("reshard_out");
-  const cpattn::ReshardSpec out[3] = {{d.Hq, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dq, dq},
-                                      {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dk, dk},
-                                      {d.Hkv, d.d, CP_HEAD_TO_SEQ, CP_TOKEN_MAJOR, 4, a.dv, dv}};
-  return cpattn::launch_reshard_batch(R, U, n, out, 3, stream, a.status);
+  // Ulysses / USP: the forward's exchanges run in reverse for the gradients
+  // ([MTX] "Split heads or rotate KV").  As in the forward, with every rank
+  // in this GPU's memory they are the kernels' addressing: member u of ring
+  // rank r reads q, k, v, o, dO, LSE and writes dq, dk, dv at rows r*T.. and
+  // its own heads of the sequence-sharded tensors.
+  a.seq_io = d.ulysses_degree > 1 ? 1 : 0;
+  NvtxRange phase("attention_bwd");
+  return cpattn::launch_attn_bwd(a, stream);
 }
 
 int cp_attn_fwd_step(const cp_plan_t* p, int rank, int step, const void* q_rank, const void* k_chunk,

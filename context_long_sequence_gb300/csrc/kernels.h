@@ -144,6 +144,10 @@ struct BwdArgs {
   // by Ulysses member (n_items_q_u and n_items_kv_u each).
   int stream_major;
   int n_items_q_u, n_items_kv_u;
+  // seq_io = 1 (all ranks, U > 1): q, k, v, o, dO, lse, dq, dk and dv are
+  // the sequence-sharded API tensors, addressed as FwdArgs::seq_io describes
+  // (slot t of ring rank r is row r*T + t; member u's heads a column range).
+  int seq_io;
 };
 
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -197,7 +197,7 @@ int ulysses_reshard_batch(const cp_plan_t *plan, int n_jobs, const cp_reshard_jo
  * exchanges are the kernel's addressing: member u of ring rank r reads rows
  * r*T .. r*T+T-1 of q, k, v (its group's slots, T = L/R) at its own heads
  * and writes o and lse in place; no head-sharded copy is made (the copy is
- * ulysses_reshard, for cp_attn_fwd_local and the backward).
+ * ulysses_reshard, for cp_attn_fwd_local and the per-step entries).
  * Per ring rank r and step s the visiting chunk comes from rank (r-s) mod R;
  * with CP_KV_ALLGATHER the call first gathers K and V of all ranks into
  * position order in the workspace, and every rank's queries then walk the
@@ -242,12 +242,14 @@ int cp_attn_fwd_rank(const cp_plan_t *plan, int rank, const void *q, const void 
  * lse [P][Hq][n] fp32;
  * dq [P][n][Hq][d], dk, dv [P][n][Hkv][d] fp32 out (overwritten).
  * Gradients of a KV chunk land on the rank that owns the chunk.  With U > 1
- * (Ulysses, USP) the forward's exchanges run in reverse: q, k, v, o, dO and
- * LSE are resharded to head sharding ([MTX] "Split heads or rotate KV"),
- * the ring backward runs per head group, and dq, dk, dv are resharded back
- * to token sharding.  Deterministic: no atomics, fixed summation order.
- * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes (with U > 1 it holds
- * the head-sharded copies: about 2x the inputs and gradients). */
+ * (Ulysses, USP) the forward's exchanges run in reverse ([MTX] "Split heads
+ * or rotate KV"): each member runs the ring backward of its heads over the
+ * group's sequence.  As in cp_attn_fwd the exchanges are the kernels'
+ * addressing (rows r*T.. of ring rank r, the member's heads), so no
+ * head-sharded copy is made.  Deterministic: no atomics, fixed summation
+ * order.
+ * workspace: cp_workspace_size(plan, CP_OP_BWD) bytes: the per-row
+ * statistics (-LSE*log2e and -D), 8 bytes per row and query head. */
 int cp_attn_bwd(const cp_plan_t *plan, const void *q, const void *k, const void *v,
                 const void *o, const float *lse, const void *dO,
                 float *dq, float *dk, float *dv, void *workspace, size_t workspace_bytes,
