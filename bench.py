@@ -546,6 +546,9 @@ def main():
     if w.backward:
         set0.update(do=do, dq=dq, dk=dk, dv=dv)
     e2e_steps = reps_for(mean_step_ms, 10)
+    # The pipeline's first copy in and last copy out are not overlapped:
+    # at least six steps, so that they weigh as in a run of many.
+    e2e_pipe_steps = max(6, e2e_steps)
     e2e_ms = e2e_serial_ms = float("nan")
     h2d = sum(set0[n].numel() * set0[n].element_size() for n in in_names)
     d2h = sum(set0[n].numel() * set0[n].element_size() for n in out_names)
@@ -601,7 +604,7 @@ def main():
 
         pipelined(2)
         barrier()
-        e2e_ms = pipelined(e2e_steps) / e2e_steps
+        e2e_ms = pipelined(e2e_pipe_steps) / e2e_pipe_steps
         serial_step()
         barrier()
         ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -751,7 +754,7 @@ def main():
             result["e2e"] = {
                 "value": round(world * flops_step / (e2e_ms_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
-                "steps": e2e_steps,
+                "steps": e2e_pipe_steps, "serial_steps": e2e_steps,
                 "overlap": "2 device buffer sets; H2D and D2H of neighbouring steps overlap compute",
                 "serial_value": round(world * flops_step / (e2e_serial_ms_max * 1e-3) / 1e12, 3),
                 "serial_ms_per_step": round(e2e_serial_ms_max, 4)}
