@@ -27,9 +27,11 @@
 // nougat.kr "MaxText long-context training and KV parallelism", "Split heads
 // or rotate KV": the chunk's partial results travel with it).
 //
-// The kernels read the head-sharded layout of the Ulysses exchange (rank
-// a = r*U + u holds ring rank r's slots for head group u; U == 1 is plain
-// sequence sharding); the ring runs over r within each head group.
+// Attention rank a = r*U + u works on ring rank r's slots for head group u
+// (U == 1 is plain sequence sharding); the ring runs over r within each
+// head group.  The kernels read either the head-sharded layout of the
+// Ulysses exchange or, with seq_io, the sequence-sharded tensors themselves
+// (slot t of ring rank r is row r*T + t, group u a range of heads).
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
 // warps 2..9 element-wise: one TMEM lane = one row, warps 2-5 take the

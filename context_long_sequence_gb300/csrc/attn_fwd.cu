@@ -2,11 +2,12 @@
 //
 // One CTA computes a block of up to 256 query rows (two 128-row tiles, Q0
 // and Q1, of the same head and the same contiguous-position chunk) of one
-// attention rank.  It walks the KV chunks of the ring in ring order -- at
-// step s the chunk of ring rank (r - s) mod R ([MTX] nougat.kr "MaxText
-// long-context training and KV parallelism", section "Split heads or rotate
-// KV": P2P keeps token sharding and computes a partial with each visiting KV
-// chunk) -- and, per 128-key tile visible from either query tile:
+// attention rank.  It visits the KV chunks of the ring -- at step s the
+// chunk of ring rank (r - s) mod R ([MTX] nougat.kr "MaxText long-context
+// training and KV parallelism", section "Split heads or rotate KV": P2P
+// keeps token sharding and computes a partial with each visiting KV chunk),
+// in position order when one launch covers every step (for_each_kv_tile) --
+// and, per 128-key tile visible from either query tile:
 //
 //   S_t = Q_t K^T          tcgen05.mma, Q and K in shared memory (TMA,
 //                          128-byte swizzle), fp32 accumulator in TMEM
