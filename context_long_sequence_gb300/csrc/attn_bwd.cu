@@ -79,51 +79,76 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(float x) { return x; }
 
-// One warp per (row, head): D = rowsum(dO * O); writes -D and -LSE * log2(e)
-// into the chunk-padded statistics layout (ld_index), then fills the padding
-// slots with 0 and -inf.  rows = attention ranks x T (T in rank-local mode).
+// One warp per (attention rank, query head, 32 consecutive slots); lane i
+// takes slot t0 + i: D = rowsum(dO * O) over its row with 16-byte loads,
+// then -D and -LSE * log2(e) into the chunk-padded statistics layout
+// (ld_index).  Consecutive slots make the warp's LSE loads and statistics
+// stores whole 128-byte lines.  Then the padding slots get 0 and -inf.
+// rows = attention ranks x T (T in rank-local mode).
 template <int D, typename OT>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dO,
                                                         const float* __restrict__ lse, float* __restrict__ nlse,
                                                         float* __restrict__ nd, const AttnGeom g, int chunk_pad,
                                                         long long rows, int seq_io, int32_t* status) {
-  constexpr int E = D / 32;  // elements per lane
   const int H = g.Hq_loc, T = g.T;
   const int lane = threadIdx.x & 31;
-  const long long total = rows * H;
   const long long ranks = rows / T;
+  const int tblocks = (T + 31) / 32;
+  const long long total = ranks * H * tblocks;
   [[maybe_unused]] const long long tp = static_cast<long long>(g.nchunks) * chunk_pad;
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long nwarps = nthreads >> 5;
   const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long n_m = T / g.U;  // slots per attention rank (sequence-sharded LSE rows)
   for (long long wi = gtid >> 5; wi < total; wi += nwarps) {
-    const long long row = wi / H;
-    const int h = static_cast<int>(wi - row * H);
-    // Row `row` = slot t of attention rank a (head-sharded enumeration);
-    // with seq_io the same row and head of the sequence-sharded tensors.
-    const long long a_r = row / T, t_r = row - a_r * T;
-    const long long io =
-        seq_io ? ((a_r / g.U) * T + t_r) * (static_cast<long long>(H) * g.U) + (a_r % g.U) * H + h : wi;
-    const OT* po = o + io * D + lane * E;
-    const __nv_bfloat16* pd = dO + io * D + lane * E;
-    float acc = 0.f;
+    const long long ah = wi / tblocks;
+    const int t = static_cast<int>(wi - ah * tblocks) * 32 + lane;
+    const long long a_r = ah / H;
+    const int h = static_cast<int>(ah - a_r * H);
+    if (t >= T) continue;
+    // Slot t of attention rank a_r, head h: head-sharded row a_r*T + t, or
+    // with seq_io row (a_r/U)*T + t at head (a_r%U)*H + h of all H*U heads.
+    const long long io = seq_io ? ((a_r / g.U) * T + t) * (static_cast<long long>(H) * g.U) + (a_r % g.U) * H + h
+                                : (a_r * T + t) * H + h;
+    const uint4* pd = reinterpret_cast<const uint4*>(dO + io * D);
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc = fmaf(to_f32(po[e]), __bfloat162float(pd[e]), acc);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 dv = pd[c];
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+      float ov[8];
+      if constexpr (sizeof(OT) == 2) {
+        const uint4 x = reinterpret_cast<const uint4*>(o + io * D)[c];
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
-    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const long long r = a_r, t = t_r;
-      const long long n_m = T / g.U;  // slots per attention rank
-      const long long li = seq_io ? (((r / g.U) * g.U + t / n_m) * (static_cast<long long>(H) * g.U) +
-                                     (r % g.U) * H + h) * n_m + t % n_m
-                                  : (r * H + h) * T + t;
-      const size_t di = ld_index(g, chunk_pad, static_cast<int>(r), h, static_cast<int>(t));
-      if (CP_IN_BOUNDS(li >= 0 && li < total && di < static_cast<size_t>(ranks * H * tp), status)) {
-        const float l = lse[li];
-        nlse[di] = l == -INFINITY ? -INFINITY : -l * kLog2e;
-        nd[di] = -acc;
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(o2[i]);
+          ov[2 * i] = f.x;
+          ov[2 * i + 1] = f.y;
+        }
+      } else {
+        const float4 x0 = reinterpret_cast<const float4*>(o + io * D)[2 * c];
+        const float4 x1 = reinterpret_cast<const float4*>(o + io * D)[2 * c + 1];
+        ov[0] = x0.x, ov[1] = x0.y, ov[2] = x0.z, ov[3] = x0.w;
+        ov[4] = x1.x, ov[5] = x1.y, ov[6] = x1.z, ov[7] = x1.w;
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(d2[i]);
+        acc0 = fmaf(ov[2 * i], f.x, acc0);
+        acc1 = fmaf(ov[2 * i + 1], f.y, acc1);
+      }
+    }
+    const float acc = acc0 + acc1;
+    const long long li = seq_io ? (((a_r / g.U) * g.U + t / n_m) * (static_cast<long long>(H) * g.U) +
+                                   (a_r % g.U) * H + h) * n_m + t % n_m
+                                : (a_r * H + h) * T + t;
+    const size_t di = ld_index(g, chunk_pad, static_cast<int>(a_r), h, t);
+    if (CP_IN_BOUNDS(li >= 0 && li < ranks * H * T && di < static_cast<size_t>(ranks * H * tp), status)) {
+      const float l = lse[li];
+      nlse[di] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+      nd[di] = -acc;
     }
   }
   // Padding: slots [chunk, chunk_pad) of every chunk.
@@ -1039,7 +1064,7 @@ int launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (phases & 1) {
-    const long long warps = rows * g.Hq_loc;
+    const long long warps = static_cast<long long>(rows / g.T) * g.Hq_loc * ((g.T + 31) / 32);
     long long grid = (warps * 32 + 255) / 256;
     if (grid > sms * 16LL) grid = sms * 16LL;
     if (grid > 0 && a.o_fp32)
