@@ -167,19 +167,21 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const OT* __restrict__ o
 // ---------------------------------------------------------------- dQ (query-tile outer)
 
 constexpr int kKStages = 4;  // K tiles in flight (K is last read by dQ, issued a tile later)
-constexpr int kVStages = 3;  // V tiles in flight (V is read by dP only)
+constexpr int kVStages = 2;  // V tiles in flight (V is read by dP only)
 
-enum DqBar { DQ_QD_FULL = 0, DQ_K_FULL = 1, DQ_K_EMPTY = DQ_K_FULL + kKStages, DQ_V_FULL = DQ_K_EMPTY + kKStages,
-             DQ_V_EMPTY = DQ_V_FULL + kVStages, DQ_S_FULL = DQ_V_EMPTY + kVStages, DQ_S_EMPTY, DQ_DP_FULL,
-             DQ_DS_FULL, DQ_DONE, DQ_DRAIN, DQ_NUM_BARS };
+// One "full" barrier per key tile covers its K and V (indexed like K).
+enum DqBar { DQ_Q_FULL = 0, DQ_DO_FULL, DQ_KV_FULL, DQ_K_EMPTY = DQ_KV_FULL + kKStages,
+             DQ_V_EMPTY = DQ_K_EMPTY + kKStages, DQ_S_FULL = DQ_V_EMPTY + kVStages, DQ_DP_FULL, DQ_S_FREE,
+             DQ_DP_FREE, DQ_DS_FULL, DQ_DS_EMPTY, DQ_DONE, DQ_DRAIN, DQ_NUM_BARS };
 
-// Q and dO live in tensor memory (the A operands of S = Q K^T and dP = dO
-// V^T), so shared memory holds only the streamed K and V tiles.
+// Q lives in tensor memory (the A operand of S = Q K^T); dO sits in shared
+// memory beside the streamed K and V tiles (the A operand of dP = dO V^T),
+// which leaves tensor memory room for a dS buffer of its own.
 template <int D>
 struct DqSmem {
   static constexpr uint32_t kT = 128 * D * 2;
-  static constexpr uint32_t offK = 0, offV = offK + kKStages * kT;
-  static constexpr uint32_t offBar = offV + kVStages * kT;
+  static constexpr uint32_t offK = 0, offV = offK + kKStages * kT, offDO = offV + kVStages * kT;
+  static constexpr uint32_t offBar = offDO + kT;
   static constexpr uint32_t offMisc = offBar + 24 * 8;
   static constexpr uint32_t kUsed = offMisc + 16;
   static constexpr uint32_t kBytes = (kUsed + 1024 < 120 * 1024) ? 120 * 1024 : kUsed + 1024;
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV;
+  const uint32_t sK = s_base + SM::offK, sV = s_base + SM::offV, sDO = s_base + SM::offDO;
   auto bar = [&](int i) { return s_base + SM::offBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::offMisc + 4);
@@ -292,19 +294,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hkv = h / g.G;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(DQ_QD_FULL), 8);  // the element-wise warps, once Q and dO sit in TMEM
+    mbar_init(bar(DQ_Q_FULL), 8);  // the element-wise warps, once Q sits in TMEM
+    mbar_init(bar(DQ_DO_FULL), 1);
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(bar(DQ_K_FULL + i), 1);
+      mbar_init(bar(DQ_KV_FULL + i), 1);
       mbar_init(bar(DQ_K_EMPTY + i), 1);
     }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(bar(DQ_V_FULL + i), 1);
-      mbar_init(bar(DQ_V_EMPTY + i), 1);
-    }
+    for (int i = 0; i < kVStages; ++i) mbar_init(bar(DQ_V_EMPTY + i), 1);
     mbar_init(bar(DQ_S_FULL), 1);
-    mbar_init(bar(DQ_S_EMPTY), 8);
     mbar_init(bar(DQ_DP_FULL), 1);
+    mbar_init(bar(DQ_S_FREE), 8);
+    mbar_init(bar(DQ_DP_FREE), 8);
     mbar_init(bar(DQ_DS_FULL), 8);
+    mbar_init(bar(DQ_DS_EMPTY), 1);
     mbar_init(bar(DQ_DONE), 1);
     mbar_init(bar(DQ_DRAIN), 1);
     *abort_flag = 0;
@@ -318,37 +320,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM: S at 0, dP (then dS, packed bf16) at 128, dQ at 256, and the A
-  // operands Q at 384 and dO at 448 (D/2 packed columns each).
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tQ = tmem + 384, tdO = tmem + 448;
+  // TMEM: S at 0, dP at 128, dQ at 256, the A operand Q at 384 (D/2 packed
+  // columns) and dS (packed bf16, 64 columns) at 448.
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tQ = tmem + 384, tdS = tmem + 448;
 
   if (warp == 0) {
     if (lane == 0) {
-      int nk = 0, nv = 0;
+      // The tile's dO rows (rows past a ragged tile's end are other rows of
+      // the tensor or the map's zero fill: their P is 0, and so is their dS).
+      {
+        const int qrow = q_row0 + it.q0;
+        const int q_col = (seq_io ? u * Hq + h : h) * D;
+        mbar_arrive_expect_tx(bar(DQ_DO_FULL), SM::kT);
+        (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows, status);
+        for (int hh = 0; hh < NH; ++hh)
+          tma_load_2d(sDO + hh * HALF_BYTES, &tm_do, bar(DQ_DO_FULL), q_col + hh * 64, qrow);
+      }
+      int nk = 0;  // key tiles loaded
       for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int kv_row_all, int, int) {
         if (*abort_flag) return;
         // kv_row_all = (src*U + u)*T + slot in the head-sharded row space.
         const int kv_row = seq_io ? (kv_row_all / (g.T * g.U)) * g.T + kv_row_all % g.T : kv_row_all - kv_sub;
         const int kv_col = (seq_io ? u * g.Hkv_loc + hkv : hkv) * D;
-        const int ks = nk % kKStages, vs = nv % kVStages;
+        const int ks = nk % kKStages, vs = nk % kVStages;
         if (!mbar_wait(bar(DQ_K_EMPTY + ks), ((nk / kKStages) & 1) ^ 1, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(DQ_K_FULL + ks), SM::kT);
+        if (!mbar_wait(bar(DQ_V_EMPTY + vs), ((nk / kVStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(DQ_KV_FULL + ks), 2 * SM::kT);
         (void)CP_IN_BOUNDS(kv_row >= 0 && kv_row < rows && hkv < g.Hkv_loc, status);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_K_FULL + ks), kv_col + hh * 64, kv_row);
+        for (int hh = 0; hh < NH; ++hh) {
+          tma_load_2d(sK + ks * SM::kT + hh * HALF_BYTES, &tm_k, bar(DQ_KV_FULL + ks), kv_col + hh * 64, kv_row);
+          tma_load_2d(sV + vs * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_KV_FULL + ks), kv_col + hh * 64, kv_row);
+        }
         ++nk;
-        if (!mbar_wait(bar(DQ_V_EMPTY + vs), ((nv / kVStages) & 1) ^ 1, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(DQ_V_FULL + vs), SM::kT);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sV + vs * SM::kT + hh * HALF_BYTES, &tm_v, bar(DQ_V_FULL + vs), kv_col + hh * 64, kv_row);
-        ++nv;
       });
       if (*abort_flag) {
         // Wait for this CTA's own copies: the last loads of each stage.
+        mbar_wait(bar(DQ_DO_FULL), 0, nullptr, status);
         for (int i = max(0, nk - kKStages); i < nk; ++i)
-          mbar_wait(bar(DQ_K_FULL + i % kKStages), (i / kKStages) & 1, nullptr, status);
-        for (int i = max(0, nv - kVStages); i < nv; ++i)
-          mbar_wait(bar(DQ_V_FULL + i % kVStages), (i / kVStages) & 1, nullptr, status);
+          mbar_wait(bar(DQ_KV_FULL + i % kKStages), (i / kKStages) & 1, nullptr, status);
       }
     }
   } else if (warp == 1) {
@@ -358,47 +367,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_dq = idesc_bf16_f32(BM, D, 1);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dDO = smem_desc_sw128(sDO, 16, 1024);
       const uint64_t dKmn0 = smem_desc_sw128(sK, HALF_BYTES, 1024);
       constexpr uint64_t kStep = SM::kT >> 4;  // one stage in descriptor units
-      // Issue order for key tile n: S_n, dQ_{n-1}, dP_n.  S has one TMEM
-      // buffer: S_n is issued once the element-wise warps have read S_{n-1}
-      // (they finish that while dQ_{n-2} and dP_{n-1} run).  dS stays in TMEM
-      // over the dP columns it came from and is the A operand of dQ; dP_n
-      // overwrites those columns only after dQ_{n-1}, issued before it by
-      // this thread, has read them.
+      // Issue order for key tile n: S_n, dP_n, dQ_{n-1}.  S and dP have one
+      // TMEM buffer each, free once the element-wise warps have loaded S_{n-1}
+      // (resp. dP_{n-1}) into registers.  dS_{n-1} has a buffer of its own,
+      // written once dQ_{n-2} has read it, so the element-wise warps form
+      // dS_{n-1} while S_n and dP_n run.  The tensor pipe's queue holds only
+      // a couple of MMAs, so anything the issuer does between two MMA groups
+      // (a barrier check costs about 80 cycles even when the phase has
+      // completed) idles the pipe once it is longer than that: one check per
+      // group, two barriers checked at once before S_n, and a plain counted
+      // loop.
       auto issue_dq = [&](int m) {  // dQ += dS_m K_m
-        mma_bf16_ts_k128_halves_warp(tdQ, tdP, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
-                                m > 0 ? 1u : 0u);
+        mma_bf16_ts_k128_warp(tdQ, tdS, dKmn0 + static_cast<uint64_t>(m % kKStages) * kStep, idesc_dq,
+                              m > 0 ? 1u : 0u);
         mma_commit_warp(bar(DQ_K_EMPTY + m % kKStages));
+        mma_commit_warp(bar(DQ_DS_EMPTY));
       };
-      int n = 0;
-      if (warp_all(mbar_wait(bar(DQ_QD_FULL), 0, abort_flag, status))) {
-        for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) {
-          if (warp_all(*abort_flag != 0)) return;
-          const int ks = n % kKStages, vs = n % kVStages;
-          if (!warp_all(mbar_wait(bar(DQ_K_FULL + ks), (n / kKStages) & 1, abort_flag, status))) return;
-          // The element-wise warps have read S_{n-1}.
-          if (n >= 1 && !warp_all(mbar_wait(bar(DQ_S_EMPTY), (n - 1) & 1, abort_flag, status))) return;
-          tc_fence_after();
-          mma_tk<D>(tS, tQ, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
-          mma_commit_warp(bar(DQ_S_FULL));
-          if (n > 0) {
-            if (!warp_all(mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status))) return;
-            tc_fence_after();
-            issue_dq(n - 1);
-          }
-          if (!warp_all(mbar_wait(bar(DQ_V_FULL + vs), (n / kVStages) & 1, abort_flag, status))) return;
-          tc_fence_after();
-          mma_tk<D>(tdP, tdO, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s);
-          mma_commit_warp(bar(DQ_DP_FULL));
-          mma_commit_warp(bar(DQ_V_EMPTY + vs));
-          ++n;
-        });
-        if (n > 0 && !warp_all(*abort_flag != 0) && warp_all(mbar_wait(bar(DQ_DS_FULL), (n - 1) & 1, abort_flag, status))) {
+      int ntiles = 0;
+      for_each_kv_tile(g, r, u, s_begin, s_end, lo_min, qpos_last, [&](int, int, int) { ++ntiles; });
+      bool ok = warp_all(mbar_wait(bar(DQ_Q_FULL), 0, abort_flag, status)) &&
+                warp_all(mbar_wait(bar(DQ_DO_FULL), 0, abort_flag, status));
+      for (int n = 0; ok && n < ntiles; ++n) {
+        const int ks = n % kKStages, vs = n % kVStages;
+        const uint32_t kv_par = (n / kKStages) & 1, prev = (n - 1) & 1;
+        // K_n and V_n landed; S_{n-1} is in registers.
+        if (!warp_all(n >= 1 ? mbar_try_wait2(bar(DQ_KV_FULL + ks), kv_par, bar(DQ_S_FREE), prev)
+                             : mbar_try_wait(bar(DQ_KV_FULL + ks), kv_par)))
+          ok = warp_all(mbar_wait(bar(DQ_KV_FULL + ks), kv_par, abort_flag, status)) &&
+               (n < 1 || warp_all(mbar_wait(bar(DQ_S_FREE), prev, abort_flag, status)));
+        if (!ok) break;
+        tc_fence_after();
+        mma_tk<D>(tS, tQ, dK0 + static_cast<uint64_t>(ks) * kStep, idesc_s);
+        mma_commit_warp(bar(DQ_S_FULL));
+        // dP_{n-1} is in registers.
+        if (n >= 1 && !(ok = warp_all(mbar_wait(bar(DQ_DP_FREE), prev, abort_flag, status)))) break;
+        tc_fence_after();
+        if constexpr (D == 128)
+          mma_bf16_ss_k128_warp<HALF_BYTES>(tdP, dDO, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s, 0u);
+        else
+          mma_bf16_ss_k64_warp(tdP, dDO, dV0 + static_cast<uint64_t>(vs) * kStep, idesc_s, 0u);
+        mma_commit_warp(bar(DQ_DP_FULL));
+        mma_commit_warp(bar(DQ_V_EMPTY + vs));
+        if (n >= 1) {
+          if (!(ok = warp_all(mbar_wait(bar(DQ_DS_FULL), prev, abort_flag, status)))) break;
           tc_fence_after();
           issue_dq(n - 1);
-          mma_commit_warp(bar(DQ_DONE));
         }
+      }
+      if (ok && ntiles > 0 && warp_all(mbar_wait(bar(DQ_DS_FULL), (ntiles - 1) & 1, abort_flag, status))) {
+        tc_fence_after();
+        issue_dq(ntiles - 1);
+        mma_commit_warp(bar(DQ_DONE));
       }
       mma_commit_warp(bar(DQ_DRAIN));
       mbar_wait(bar(DQ_DRAIN), 0, nullptr, status);
@@ -420,33 +442,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float ndl = (row_valid && ld_ok) ? args.nd[lrow] : 0.f;
     const float sl2 = g.scale * kLog2e;
     {
-      // This thread's half of its Q and dO rows into TMEM (lane = row; the
-      // bf16 pairs of a row in memory order are the packed columns).  Rows
-      // past the tile's end are zero.
+      // This thread's half of its Q row into TMEM (lane = row; the bf16
+      // pairs of a row in memory order are the packed columns).  Rows past
+      // the tile's end are zero.
       constexpr int W = D / 4;  // 32-bit words per half row
       const size_t grow = static_cast<size_t>(q_row0 + it.q0 + row) * (seq_io ? Hq * g.U : Hq) + (seq_io ? u * Hq + h : h);
       const bool in = row_valid && CP_IN_BOUNDS(q_row0 + it.q0 + row < rows, status);
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q) + grow * D) + half * (W / 4);
-      const uint4* dsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.dO) + grow * D) + half * (W / 4);
-      uint32_t qw[W], dw[W];
+      uint32_t qw[W];
 #pragma unroll
       for (int i = 0; i < W / 4; ++i) {
         const uint4 x = in ? qsrc[i] : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 y = in ? dsrc[i] : make_uint4(0u, 0u, 0u, 0u);
         qw[4 * i] = x.x, qw[4 * i + 1] = x.y, qw[4 * i + 2] = x.z, qw[4 * i + 3] = x.w;
-        dw[4 * i] = y.x, dw[4 * i + 1] = y.y, dw[4 * i + 2] = y.z, dw[4 * i + 3] = y.w;
       }
-      if constexpr (D == 128) {
+      if constexpr (D == 128)
         tmem_st32(tQ + lane_off + half * W, qw);
-        tmem_st32(tdO + lane_off + half * W, dw);
-      } else {
+      else
         tmem_st16(tQ + lane_off + half * W, qw);
-        tmem_st16(tdO + lane_off + half * W, dw);
-      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(DQ_QD_FULL));
+      if (lane == 0) mbar_arrive(bar(DQ_Q_FULL));
     }
     int n = 0;
     bool ok = true;
@@ -468,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(sr2[0]);
       reg_fence(sr2[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQ_S_FREE));
       // Two instantiations: tiles wholly inside the window take the loop with
       // no mask at all (a mask test folded into every element costs more
       // than the rest of the loop).
@@ -496,12 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         phase_a(std::false_type{});
       else
         phase_a(std::true_type{});
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(DQ_S_EMPTY));
-      // Phase B: dS = P * (dP - D), packed to bf16 pairs over the dP columns
-      // this warp has read (32-column chunk cc of this half -> columns
-      // 64*half + 16*cc ..): the A operand of dQ.
+      // Phase B: dS = P * (dP - D), packed to bf16 pairs in the dS buffer
+      // (keys 64*half + 32*cc.. -> columns 32*half + 16*cc..): the A operand
+      // of dQ.  The dP columns are released as soon as they are in
+      // registers; dS is stored once dQ_{n-1} has read the buffer.
       ok = warp_all(mbar_wait(bar(DQ_DP_FULL), n & 1, abort_flag, status));
       if (!ok) return;
       tc_fence_after();
@@ -511,20 +528,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(pr2[0]);
       reg_fence(pr2[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQ_DP_FREE));
+      uint32_t dsp[2][16];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t* pr = pr2[cc];
-        uint32_t dsp[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const f32x2 dd = add_f32x2(make_f32x2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
                                      make_f32x2(ndl, ndl));
           float s0, s1;
           split_f32x2(mul_f32x2(make_f32x2(pf[cc * 32 + e], pf[cc * 32 + e + 1]), dd), s0, s1);
-          dsp[e / 2] = pack_bf16x2(s0, s1);
+          dsp[cc][e / 2] = pack_bf16x2(s0, s1);
         }
-        tmem_st16(tdP + lane_off + 64 * half + 16 * cc, dsp);
       }
+      if (n >= 1) {
+        ok = warp_all(mbar_wait(bar(DQ_DS_EMPTY), (n - 1) & 1, abort_flag, status));
+        if (!ok) return;
+        tc_fence_after();
+      }
+      tmem_st16(tdS + lane_off + 32 * half, dsp[0]);
+      tmem_st16(tdS + lane_off + 32 * half + 16, dsp[1]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -577,11 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dK, dV (key-tile outer)
 
-enum DkvBar { KV_FULL = 0, KV_Q_FULL = 1, KV_Q_EMPTY = 4, KV_DO_FULL = 7, KV_DO_EMPTY = 9, KV_S_FULL = 11,
-              KV_DP_FULL = 12, KV_P_FULL = 13, KV_DS_FULL = 14, KV_ACC_DONE = 15, KV_DRAIN = 16,
-              KV_LD_FULL = 17,   // +buffer: the LSE/D of a query tile are staged (4 writer warps)
-              KV_LD_EMPTY = 19,  // +buffer: every element-wise warp has read them (8 warps)
-              KV_NUM_BARS = 21 };
+// One "full" barrier per query tile covers its Q and dO (indexed like Q).
+enum DkvBar { KV_FULL = 0, KV_QD_FULL = 1, KV_Q_EMPTY = 4, KV_DO_EMPTY = 7, KV_S_FULL = 9,
+              KV_DP_FULL = 10, KV_P_FULL = 11, KV_DS_FULL = 12, KV_ACC_DONE = 13, KV_DRAIN = 14,
+              KV_LD_FULL = 15,   // +buffer: the LSE/D of a query tile are staged (4 writer warps)
+              KV_LD_EMPTY = 17,  // +buffer: every element-wise warp has read them (8 warps)
+              KV_NUM_BARS = 19 };
 
 constexpr int kQStages = 3;   // Q tiles in flight (Q is last read by dK, the last product of a tile)
 constexpr int kDOStages = 2;  // dO tiles in flight (dO is last read by dV)
@@ -708,13 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(KV_FULL), 1);
     for (int i = 0; i < kQStages; ++i) {
-      mbar_init(bar(KV_Q_FULL + i), 1);
+      mbar_init(bar(KV_QD_FULL + i), 1);
       mbar_init(bar(KV_Q_EMPTY + i), 1);
     }
-    for (int i = 0; i < kDOStages; ++i) {
-      mbar_init(bar(KV_DO_FULL + i), 1);
-      mbar_init(bar(KV_DO_EMPTY + i), 1);
-    }
+    for (int i = 0; i < kDOStages; ++i) mbar_init(bar(KV_DO_EMPTY + i), 1);
     mbar_init(bar(KV_S_FULL), 1);
     mbar_init(bar(KV_DP_FULL), 1);
     mbar_init(bar(KV_P_FULL), 8);
@@ -749,26 +773,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sK + hh * HALF_BYTES, &tm_k, bar(KV_FULL), kv_col + hh * 64, krow);
         tma_load_2d(sV + hh * HALF_BYTES, &tm_v, bar(KV_FULL), kv_col + hh * 64, krow);
       }
-      int nq = 0, ndo = 0, nld = 0;  // Q, dO and statistics loads issued
+      int nq = 0, nld = 0;  // query tiles (Q and dO) and statistics loads issued
       // statistics of every attention rank (one in rank-local mode)
       [[maybe_unused]] const size_t ld_total =
           static_cast<size_t>(rank_local ? 1 : g.R * g.U) * Hq * g.nchunks * args.chunk_pad;
       for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int rr, int qslot0, int qpos0, int qlen, int h) {
         if (*abort_flag) return;
-        const int qs = nq % kQStages, ds = ndo % kDOStages;
+        const int qs = nq % kQStages, ds = nq % kDOStages;
         const int qrow = (rank_local ? 0 : (seq_io ? rr : rr * g.U + u) * g.T) + qslot0;
         const int q_col = (seq_io ? u * Hq + h : h) * D;
         if (!mbar_wait(bar(KV_Q_EMPTY + qs), ((nq / kQStages) & 1) ^ 1, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(KV_Q_FULL + qs), SM::kT);
+        if (!mbar_wait(bar(KV_DO_EMPTY + ds), ((nq / kDOStages) & 1) ^ 1, abort_flag, status)) return;
+        mbar_arrive_expect_tx(bar(KV_QD_FULL + qs), 2 * SM::kT);
         (void)CP_IN_BOUNDS(qrow >= 0 && qrow < rows && h < Hq, status);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_Q_FULL + qs), q_col + hh * 64, qrow);
+        for (int hh = 0; hh < NH; ++hh) {
+          tma_load_2d(sQ + qs * SM::kT + hh * HALF_BYTES, &tm_q, bar(KV_QD_FULL + qs), q_col + hh * 64, qrow);
+          tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_QD_FULL + qs), q_col + hh * 64, qrow);
+        }
         ++nq;
-        if (!mbar_wait(bar(KV_DO_EMPTY + ds), ((ndo / kDOStages) & 1) ^ 1, abort_flag, status)) return;
-        mbar_arrive_expect_tx(bar(KV_DO_FULL + ds), SM::kT);
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_2d(sDO + ds * SM::kT + hh * HALF_BYTES, &tm_do, bar(KV_DO_FULL + ds), q_col + hh * 64, qrow);
-        ++ndo;
         // The tile's -LSE*log2(e) and -D (128 each, chunk-padded so the copy
         // starts on a 512-byte boundary) and its position and length, for
         // the element-wise warps; the stage is reused once all 8 of them
@@ -800,9 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage are the only ones that can still be in flight).
         mbar_wait(bar(KV_FULL), 0, nullptr, status);
         for (int i = max(0, nq - kQStages); i < nq; ++i)
-          mbar_wait(bar(KV_Q_FULL + i % kQStages), (i / kQStages) & 1, nullptr, status);
-        for (int i = max(0, ndo - kDOStages); i < ndo; ++i)
-          mbar_wait(bar(KV_DO_FULL + i % kDOStages), (i / kDOStages) & 1, nullptr, status);
+          mbar_wait(bar(KV_QD_FULL + i % kQStages), (i / kQStages) & 1, nullptr, status);
       }
     }
   } else if (warp == 1) {
@@ -819,7 +839,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dS^T stay in TMEM, where the element-wise warps wrote them over the
       // S^T and dP^T they came from, and are the A operands of dV and dK;
       // S_n (dP_n) overwrites those columns only after dV_{n-1} (dK_{n-1}),
-      // issued before it by this thread, has read them.
+      // issued before it by this thread, has read them.  Two checks per tile
+      // (P_{n-1} written with Q_n and dO_n landed; dS_{n-1} written) and a
+      // plain counted loop: each check between two MMA groups idles the
+      // tensor pipe for about as long as it takes.
       auto issue_dv = [&](int m) {  // dV += P^T_m dO_m
         mma_bf16_ts_k128_halves_warp(tdV, tSt, dDOmn0 + static_cast<uint64_t>(m % kDOStages) * kStep, idesc_acc,
                                 m > 0 ? 1u : 0u);
@@ -830,40 +853,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 m > 0 ? 1u : 0u);
         mma_commit_warp(bar(KV_Q_EMPTY + m % kQStages));
       };
-      int n = 0;
-      if (warp_all(mbar_wait(bar(KV_FULL), 0, abort_flag, status))) {
-        for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int, int, int, int, int) {
-          if (warp_all(*abort_flag != 0)) return;
-          if (n > 0) {
-            if (!warp_all(mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status))) return;
-            tc_fence_after();
-            issue_dv(n - 1);
-          }
-          const int qs = n % kQStages, ds = n % kDOStages;
-          if (!warp_all(mbar_wait(bar(KV_Q_FULL + qs), (n / kQStages) & 1, abort_flag, status))) return;
+      int ntiles = 0;
+      for_each_q_tile(g, src, s_begin, s_end, kpos0, hi_max, jh, [&](int, int, int, int, int) { ++ntiles; });
+      bool ok = warp_all(mbar_wait(bar(KV_FULL), 0, abort_flag, status));
+      for (int n = 0; ok && n < ntiles; ++n) {
+        const int qs = n % kQStages, ds = n % kDOStages;
+        const uint32_t q_par = (n / kQStages) & 1, prev = (n - 1) & 1;
+        if (!warp_all(n >= 1 ? mbar_try_wait2(bar(KV_P_FULL), prev, bar(KV_QD_FULL + qs), q_par)
+                             : mbar_try_wait(bar(KV_QD_FULL + qs), q_par)))
+          ok = (n < 1 || warp_all(mbar_wait(bar(KV_P_FULL), prev, abort_flag, status))) &&
+               warp_all(mbar_wait(bar(KV_QD_FULL + qs), q_par, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        if (n > 0) issue_dv(n - 1);
+        mma_qk<D>(tSt, dK0, dQ0 + static_cast<uint64_t>(qs) * kStep, idesc_s);
+        mma_commit_warp(bar(KV_S_FULL));
+        if (n > 0) {
+          if (!(ok = warp_all(mbar_wait(bar(KV_DS_FULL), prev, abort_flag, status)))) break;
           tc_fence_after();
-          mma_qk<D>(tSt, dK0, dQ0 + static_cast<uint64_t>(qs) * kStep, idesc_s);
-          mma_commit_warp(bar(KV_S_FULL));
-          if (n > 0) {
-            if (!warp_all(mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status))) return;
-            tc_fence_after();
-            issue_dk(n - 1);
-          }
-          if (!warp_all(mbar_wait(bar(KV_DO_FULL + ds), (n / kDOStages) & 1, abort_flag, status))) return;
+          issue_dk(n - 1);
+        }
+        mma_qk<D>(tdPt, dV0, dDO0 + static_cast<uint64_t>(ds) * kStep, idesc_s);
+        mma_commit_warp(bar(KV_DP_FULL));
+      }
+      // dV and dK of the last query tile.
+      if (ok && ntiles > 0 && warp_all(mbar_wait(bar(KV_P_FULL), (ntiles - 1) & 1, abort_flag, status))) {
+        tc_fence_after();
+        issue_dv(ntiles - 1);
+        if (warp_all(mbar_wait(bar(KV_DS_FULL), (ntiles - 1) & 1, abort_flag, status))) {
           tc_fence_after();
-          mma_qk<D>(tdPt, dV0, dDO0 + static_cast<uint64_t>(ds) * kStep, idesc_s);
-          mma_commit_warp(bar(KV_DP_FULL));
-          ++n;
-        });
-        // dV and dK of the last query tile.
-        if (n > 0 && !warp_all(*abort_flag != 0) && warp_all(mbar_wait(bar(KV_P_FULL), (n - 1) & 1, abort_flag, status))) {
-          tc_fence_after();
-          issue_dv(n - 1);
-          if (warp_all(mbar_wait(bar(KV_DS_FULL), (n - 1) & 1, abort_flag, status))) {
-            tc_fence_after();
-            issue_dk(n - 1);
-            mma_commit_warp(bar(KV_ACC_DONE));
-          }
+          issue_dk(ntiles - 1);
+          mma_commit_warp(bar(KV_ACC_DONE));
         }
       }
       mma_commit_warp(bar(KV_DRAIN));
