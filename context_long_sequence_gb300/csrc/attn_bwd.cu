@@ -76,9 +76,6 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a, uint64_t b, 
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ float to_f32(float x) { return x; }
-
 // One warp per (attention rank, query head, 32 consecutive slots); lane i
 // takes slot t0 + i: D = rowsum(dO * O) over its row with 16-byte loads,
 // then -D and -LSE * log2(e) into the chunk-padded statistics layout
