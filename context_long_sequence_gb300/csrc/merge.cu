@@ -14,9 +14,9 @@
 //      at a time, and lane i computes the merged LSE and the weights
 //      e^(lse_p - lse) of its row for every part, parked in shared memory;
 //   2. the warp then walks its rows: a row's d floats of one part are 4d
-//      contiguous bytes (d/4 lanes, one float4 each; two rows at a time for
-//      d = 64), and each lane issues the loads of up to eight parts before
-//      it folds them.
+//      contiguous bytes (d/4 lanes, one float4 each; two rows per warp step
+//      for d = 64), and each lane issues the loads of up to eight parts of
+//      two such steps before it folds them.
 // Consecutive warps take consecutive heads of the same rows, so together
 // they sweep contiguous (row, head, d) ranges of every part.
 #include <cuda_bf16.h>
@@ -86,36 +86,51 @@ __global__ void __launch_bounds__(256) merge_kernel(int n_parts, int rows, int H
       if (valid) lse_out[static_cast<long long>(b) * per_batch + static_cast<long long>(h) * rows + row] = lse;
     }
     __syncwarp();
-    // 2. O rows, RPI at a time.
+    // 2. O rows, 2 * RPI at a time (two row groups' loads in flight).
     const float* ob = o_parts + static_cast<long long>(b) * n_parts * per_batch * D;
-    for (int j0 = 0; j0 < nrow; j0 += RPI) {
-      const int j = j0 + sub;
-      if (j < nrow) {
-        const long long off = (static_cast<long long>(row0 + j) * H + h) * D + c4 * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p0 = 0; p0 < n_parts; p0 += kBatch) {
-          float4 v[kBatch];
+    for (int j0 = 0; j0 < nrow; j0 += 2 * RPI) {
+      int jj[2];
+      bool in[2];
+      long long off[2];
+      float4 acc[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        jj[q] = j0 + q * RPI + sub;
+        in[q] = jj[q] < nrow;
+        off[q] = (static_cast<long long>(row0 + (in[q] ? jj[q] : 0)) * H + h) * D + c4 * 4;
+        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int p0 = 0; p0 < n_parts; p0 += kBatch) {
+        float4 v[2][kBatch];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int i = 0; i < kBatch; ++i)
-            if (p0 + i < n_parts) v[i] = __ldg(reinterpret_cast<const float4*>(ob + (p0 + i) * per_batch * D + off));
+            if (in[q] && p0 + i < n_parts)
+              v[q][i] = __ldg(reinterpret_cast<const float4*>(ob + (p0 + i) * per_batch * D + off[q]));
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
-            if (p0 + i < n_parts) {
-              const float wt = w[(p0 + i) * kRows + j];
-              acc.x = fmaf(wt, v[i].x, acc.x);
-              acc.y = fmaf(wt, v[i].y, acc.y);
-              acc.z = fmaf(wt, v[i].z, acc.z);
-              acc.w = fmaf(wt, v[i].w, acc.w);
+            if (in[q] && p0 + i < n_parts) {
+              const float wt = w[(p0 + i) * kRows + jj[q]];
+              acc[q].x = fmaf(wt, v[q][i].x, acc[q].x);
+              acc[q].y = fmaf(wt, v[q][i].y, acc[q].y);
+              acc[q].z = fmaf(wt, v[q][i].z, acc[q].z);
+              acc[q].w = fmaf(wt, v[q][i].w, acc[q].w);
             }
           }
-        }
-        const long long oi = static_cast<long long>(b) * per_batch * D + off;
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (!in[q]) continue;
+        const long long oi = static_cast<long long>(b) * per_batch * D + off[q];
         if (!CP_IN_BOUNDS(oi + 4 <= static_cast<long long>(batch) * per_batch * D, status)) continue;
         if (out_fp32)
-          *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc;
+          *reinterpret_cast<float4*>(static_cast<float*>(o_out) + oi) = acc[q];
         else
           *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oi) =
-              make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
+              make_uint2(pack2(acc[q].x, acc[q].y), pack2(acc[q].z, acc[q].w));
       }
     }
     __syncwarp();  // the next unit rewrites the weights
