@@ -401,6 +401,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in workloads.WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="the CPU baseline runs the oracle over every query row and head (minutes at L=16K) "
+                         "instead of a sample")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the measurements of the other four workloads after the main one")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
@@ -778,7 +781,7 @@ def main():
         if meta is not None:
             result["run"] = meta
         if world == 1 and not args.no_cpu_baseline and cpu is not None:
-            result["cpu_baseline"] = cpu_baseline(w, cpu, offsets, flops_fwd)
+            result["cpu_baseline"] = cpu_baseline(w, cpu, offsets, flops_fwd, full=args.cpu_full)
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.barrier()
@@ -962,13 +965,26 @@ def run_transport(args, w, offsets, flops_fwd, flops_step, warmup, world, rank, 
     return 0
 
 
-def cpu_baseline(w, cpu, offsets, flops_full):
+def cpu_baseline(w, cpu, offsets, flops_full, full=False):
     """The oracle, as it stands, on a bounded seeded sample of the workload,
-    with the time a full run would take at the sampled rate."""
+    with the time a full run would take at the sampled rate; or (full) over
+    every query row and head, timed."""
     heads = list(range(w.Hq))
+    cores = len(os.sched_getaffinity(0))
+    if full:
+        import oracle
+        per = oracle_rows_per_call(w.L, 256)
+        t0 = time.perf_counter()
+        for r0 in range(0, w.L, per):
+            oracle.attention_rows(cpu["q"], cpu["k"], cpu["v"], rows=np.arange(r0, min(w.L, r0 + per)),
+                                  offsets=offsets, heads=heads)
+        el = time.perf_counter() - t0
+        return {"value": round(flops_full / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": f"full run: all {w.L} query rows x {len(heads)} heads of {w.name} (fp64 numpy, "
+                          f"{per} rows per call)",
+                "full_run_flops": flops_full, "full_run_s_measured": round(el, 2)}
     rows = oracle_rows_per_call(w.L, 64)
     flops, el, calls = time_oracle(w, cpu, offsets, rows, heads, seed=0, min_seconds=10.0, max_calls=16)
-    cores = len(os.sched_getaffinity(0))
     rate = flops / el
     return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} x {rows} seeded random query rows x {len(heads)} heads of {w.name} "
