@@ -491,6 +491,8 @@ def main():
     # The rates behind the secondary bounds: exp2 per SM clock (one per
     # visible pair and head) and clocks per M128 N128 K16 MMA, measured here.
     ex2_per_clk, mma_clk = cpa.cp_measure_rates(stream=stream)
+    # And the fixed cost of a barrier check in the MMA-issuing warps.
+    bar_clk = cpa.cp_measure_barrier_check(stream=stream)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def fwd():
@@ -764,7 +766,8 @@ def main():
             "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v_.items()}
                         for k_, v_ in kern.items()},
             "hbm_peak_gbs": peaks["hbm_gbs"],
-            "secondary": secondary_bounds(ex2_per_clk, mma_clk, n_sm, clock_rec, w.d),
+            "secondary": dict(secondary_bounds(ex2_per_clk, mma_clk, n_sm, clock_rec, w.d),
+                              barrier_check_clk=round(bar_clk, 1)),
             "clocks": clock_rec,
             "wall_s_timed": round(t_wall, 3),
         }

@@ -119,6 +119,7 @@ def _L():
                                     ctypes.POINTER(ctypes.c_int64), _vp]
     lib.cp_debug_build.argtypes = []
     lib.cp_measure_rates.argtypes = [ctypes.POINTER(ctypes.c_double), _vp]
+    lib.cp_measure_barrier_check.argtypes = [ctypes.POINTER(ctypes.c_double), _vp]
     lib.cp_strerror.argtypes = [_i]
     lib.cp_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -130,7 +131,7 @@ EXPORTED = ["cp_plan_create", "cp_plan_destroy", "cp_index_map", "cp_workspace_s
             "cp_attn_fwd", "cp_attn_fwd_local", "cp_attn_fwd_rank", "cp_attn_fwd_noalloc", "cp_attn_bwd",
             "cp_attn_fwd_step", "cp_attn_bwd_delta", "cp_attn_bwd_step",
             "cp_merge_lse", "cp_get_status", "cp_get_status_detail", "cp_debug_build", "cp_strerror",
-            "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes", "cp_measure_rates"]
+            "cp_selftest_wait_timeout", "cp_selftest_bounds", "cp_tile_classes", "cp_measure_rates", "cp_measure_barrier_check"]
 
 
 class CPError(RuntimeError):
@@ -342,6 +343,13 @@ def cp_measure_rates(stream=None):
     out = (ctypes.c_double * 2)()
     _check(_L().cp_measure_rates(out, _stream(stream)), "cp_measure_rates")
     return float(out[0]), float(out[1])
+
+
+def cp_measure_barrier_check(stream=None) -> float:
+    """SM clocks per warp-wide check of a completed mbarrier phase."""
+    out = ctypes.c_double(0.0)
+    _check(_L().cp_measure_barrier_check(ctypes.byref(out), _stream(stream)), "cp_measure_barrier_check")
+    return float(out.value)
 
 
 def cp_debug_build() -> bool:

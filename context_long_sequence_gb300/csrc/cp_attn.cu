@@ -1209,6 +1209,69 @@ extern "C" int cp_measure_rates(double* out2, cudaStream_t stream) {
   return CP_OK;
 }
 
+// Latency of one warp-wide check of an mbarrier phase that has already
+// completed (try_wait in every lane, then a vote): what the MMA-issuing
+// warps pay at each wait between two MMA groups, pipe idle or not.  One warp,
+// a dependent chain: each check's barrier depends on the previous result.
+namespace {
+constexpr int kRateBarChecks = 256;
+
+__global__ void rate_bar_kernel(unsigned long long* cyc, int32_t* status) {
+  __shared__ __align__(8) uint64_t bars[2];
+  const uint32_t b0 = cpattn::smem_u32(&bars[0]);
+  if (threadIdx.x == 0) {
+    cpattn::mbar_init(b0, 1);
+    cpattn::mbar_init(b0 + 8, 1);
+    cpattn::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {  // phase 0 of both completes
+    cpattn::mbar_arrive(b0);
+    cpattn::mbar_arrive(b0 + 8);
+  }
+  __syncwarp();
+  uint32_t sel = 0;
+  const unsigned long long t0 = clock64();
+  for (int i = 0; i < kRateBarChecks; ++i) {
+    const bool ok = __all_sync(0xffffffffu, cpattn::mbar_wait(b0 + 8u * sel, 0, nullptr, status));
+    sel = ok ? (sel ^ 1u) : sel;
+  }
+  const unsigned long long t1 = clock64();
+  if (threadIdx.x == 0) {
+    cyc[0] = t1 - t0;
+    cyc[1] = sel;
+  }
+}
+}  // namespace
+
+extern "C" int cp_measure_barrier_check(double* cycles, cudaStream_t stream) {
+  if (!cycles) return CP_ERR_INVALID_ARG;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (major != 10 || minor != 3) return CP_ERR_ARCH;
+  int32_t* st = status_ptr();
+  if (!st) return CP_ERR_CUDA;
+  unsigned long long* d_cyc = nullptr;
+  if (cudaMalloc(&d_cyc, 2 * sizeof(unsigned long long)) != cudaSuccess) return CP_ERR_CUDA;
+  int rc = CP_OK;
+  // Twice; the second run is kept.
+  for (int rep = 0; rc == CP_OK && rep < 2; ++rep) {
+    rate_bar_kernel<<<1, 32, 0, stream>>>(d_cyc, st);
+    if (cudaGetLastError() != cudaSuccess) rc = CP_ERR_CUDA;
+  }
+  unsigned long long cyc[2] = {0, 0};
+  if (rc == CP_OK && (cudaMemcpyAsync(cyc, d_cyc, sizeof(cyc), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+                      cudaStreamSynchronize(stream) != cudaSuccess))
+    rc = CP_ERR_CUDA;
+  cudaFree(d_cyc);
+  if (rc != CP_OK) return rc;
+  *cycles = static_cast<double>(cyc[0]) / kRateBarChecks;
+  return CP_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Allocation-free emit-partials forward (cp_attn_fwd_noalloc).
 //

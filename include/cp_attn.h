@@ -371,6 +371,15 @@ int cp_selftest_bounds(int32_t block, int32_t *line, cudaStream_t stream);
  * CP_ERR_ARCH on a device other than sm_103. */
 int cp_measure_rates(double *out2, cudaStream_t stream);
 
+/* SM clocks per warp-wide check of an mbarrier phase that has already
+ * completed (mbarrier.try_wait in all 32 lanes, then a vote), measured as a
+ * dependent chain in one warp (no counterpart in the pages): the fixed cost
+ * that the MMA-issuing warp of each kernel pays at every barrier check
+ * between two groups of MMAs.  *cycles (host, 1 double).  Synchronous;
+ * CP_ERR_INVALID_ARG for a null pointer, CP_ERR_ARCH on a device other than
+ * sm_103. */
+int cp_measure_barrier_check(double *cycles, cudaStream_t stream);
+
 /* Allocation-free variant of the emit-partials forward (no counterpart in
  * the paper: it exists for callers, not for the method).
  *

@@ -83,6 +83,7 @@ def test_reshard_batch_argument_checks(cpa):
 
 def test_measure_rates_argument_check(cpa):
     assert cpa._L().cp_measure_rates(None, None) == cpa.CP_ERR_INVALID_ARG
+    assert cpa._L().cp_measure_barrier_check(None, None) == cpa.CP_ERR_INVALID_ARG
 
 
 def test_tile_classes_argument_checks(cpa):

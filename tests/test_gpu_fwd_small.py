@@ -344,3 +344,7 @@ def test_measure_rates(cpa):
     ex2, mma = cpa.cp_measure_rates()
     assert 4.0 <= ex2 <= 128.0, ex2
     assert 32.0 <= mma <= 256.0, mma
+    # A completed barrier's check: tens of clocks, far below a wait's limit.
+    bc = cpa.cp_measure_barrier_check()
+    assert 8.0 <= bc <= 2000.0, bc
+    assert cpa.cp_get_status() == 0
