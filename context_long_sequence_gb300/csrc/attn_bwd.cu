@@ -12,17 +12,18 @@
 // no atomics, deterministic:
 //   delta    D per (query, head)                           bandwidth-bound
 //   dkv      one CTA per 128-key tile and KV head: walks every visible
-//            query tile of every ring rank (ring order: the chunk of rank
-//            src visits ranks src, src+1, ...) and every query head of the
-//            group; S^T = K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T
-//            written back over them as packed bf16 and read from TMEM as
-//            the A operands of dV += P^T dO and dK += dS^T Q; dV and dK
-//            accumulated in TMEM; three Q and two dO tiles in flight
+//            query tile (one ring step: of the ranks the chunk visits; all
+//            steps in one launch: in position order) and every query head
+//            of the group; S^T = K Q^T and dP^T = V dO^T in TMEM, P^T and
+//            dS^T written back over them as packed bf16 and read from TMEM
+//            as the A operands of dV += P^T dO and dK += dS^T Q; dV and dK
+//            accumulated in TMEM; three Q and two dO tiles in flight, one
+//            barrier for a query tile's Q and dO
 //   dq       one CTA per 128-query tile and head: walks the visible key
-//            tiles in ring order like the forward; S = Q K^T (two TMEM
-//            buffers) and dP = dO V^T in TMEM, dS written back over dP and
-//            read from TMEM as the A operand of dQ += dS K; three K and two
-//            V tiles in flight
+//            tiles like the forward; Q in TMEM (S = Q K^T from TMEM), dO in
+//            shared memory (dP = dO V^T), S, dP, dS and dQ each in a TMEM
+//            buffer of its own, issued S_n, dP_n, dQ_{n-1}; four K and two
+//            V tiles in flight, one barrier for a key tile's K and V
 // Gradients of a KV chunk land on the rank that owns the chunk ([MTX]
 // nougat.kr "MaxText long-context training and KV parallelism", "Split heads
 // or rotate KV": the chunk's partial results travel with it).
